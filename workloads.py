@@ -1,0 +1,271 @@
+"""Seeded synthetic inputs for the Mamba2 SSD varlen prefill.
+
+Shared by the tests, the bench and the oracle's callers.  It holds none of the
+method's arithmetic: only random draws, request lengths, slot assignments and
+buffer shapes.  Every draw is seeded, so the same (config, seed, device) gives
+the same tensors.
+
+Value recipe (the same for every workload, following the workloads the SSD
+varlen pages describe):
+  x, B, C, z ~ N(0, 1); dt ~ N(0, 1) (softplus is applied by the method);
+  dt_bias ~ U(-2, -1); A = -exp(U(0, ln 16)); D ~ N(0, 1);
+  initial states in a pool of fp32 slots ~ N(0, 1) (tiny case) or N(0, 0.5^2).
+Tensor layouts (row-major, last index fastest): x, z, y (T,H,P); B, C (T,G,N);
+dt (T,H); dt_bias, A, D (H) fp32; states (..., H, P, N) fp32.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+
+@dataclass
+class Spec:
+    name: str
+    H: int
+    P: int
+    N: int
+    G: int
+    chunk_size: int
+    dtype: str                      # "bf16" or "fp32"
+    lengths: list | None = None     # fixed lengths, else drawn by length_recipe
+    length_recipe: str | None = None
+    has_D: bool = True
+    has_z: bool = False
+    init: str = "none"              # "none", "tiny_req2", "half_even", "all"
+    pool_slots: int = 0
+    init_std: float = 0.5
+    final_dense: bool = True        # write (R,H,P,N) final states
+    final_slots: bool = False       # write finals into distinct pool slots
+    export_chunks: bool = False
+    block_size: int = 0             # block-checkpoint scatter granularity (0 = off)
+    extra: dict = field(default_factory=dict)
+
+
+# The five workloads: a tiny fp32 correctness case and four bf16 layer shapes.
+CONFIGS: dict[str, Spec] = {
+    "tiny_fp32": Spec("tiny_fp32", H=4, P=16, N=16, G=1, chunk_size=16, dtype="fp32",
+                      lengths=[5, 17, 42], has_D=True, has_z=False, init="tiny_req2",
+                      pool_slots=3, init_std=1.0),
+    "uniform_8x2048": Spec("uniform_8x2048", H=80, P=64, N=128, G=1, chunk_size=256,
+                           dtype="bf16", lengths=[2048] * 8, has_D=True, has_z=True),
+    "varlen_lognormal_32k": Spec("varlen_lognormal_32k", H=128, P=64, N=128, G=8,
+                                 chunk_size=256, dtype="bf16", length_recipe="lognormal64",
+                                 has_D=True, has_z=False, init="half_even", pool_slots=256),
+    "long_131072": Spec("long_131072", H=64, P=64, N=128, G=1, chunk_size=128,
+                        dtype="bf16", lengths=[131072], has_D=True, has_z=False,
+                        export_chunks=True),
+    "block_ckpt_varlen": Spec("block_ckpt_varlen", H=64, P=128, N=128, G=8, chunk_size=128,
+                              dtype="bf16", length_recipe="uniform128", has_D=True,
+                              has_z=False, init="all", pool_slots=4096, final_dense=False,
+                              final_slots=True, block_size=1024),
+}
+CONFIG_ORDER = ["tiny_fp32", "uniform_8x2048", "varlen_lognormal_32k", "long_131072",
+                "block_ckpt_varlen"]
+CONFIG_SEED = {name: i for i, name in enumerate(CONFIG_ORDER)}
+
+
+def draw_lengths(spec: Spec, seed: int) -> list[int]:
+    if spec.lengths is not None:
+        return list(spec.lengths)
+    rng = np.random.default_rng(seed)
+    if spec.length_recipe == "lognormal64":
+        # 64 lognormal(mu = ln 400, sigma = 1) draws clipped to [1, 4096], then
+        # rescaled so the batch holds exactly 32768 tokens (shape kept).
+        raw = np.clip(rng.lognormal(mean=math.log(400.0), sigma=1.0, size=64), 1, 4096)
+        lens = np.clip(np.rint(raw * (32768.0 / raw.sum())), 1, 4096).astype(np.int64)
+        diff = 32768 - int(lens.sum())
+        i = 0
+        while diff != 0:
+            j = i % 64
+            step = 1 if diff > 0 else -1
+            if 1 <= lens[j] + step <= 4096:
+                lens[j] += step
+                diff -= step
+            i += 1
+        return [int(v) for v in lens]
+    if spec.length_recipe == "uniform128":
+        return [int(v) for v in rng.integers(1, 8193, size=128)]
+    raise ValueError(spec.length_recipe)
+
+
+def _randn(shape, gen, device, dtype, std=1.0):
+    t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def make_problem(spec: Spec | str, seed: int | None = None, device="cpu", lengths=None,
+                 num_computed=None, chunk_size=None, canary: float | None = None):
+    """Draw one batch.  Returns a dict of tensors plus integer settings.
+
+    lengths / num_computed / chunk_size override the spec (tests use this for
+    ragged and resumed cases).  canary: value written into every pool slot that
+    no request reads, so tests can check that untouched slots stay intact.
+    """
+    if isinstance(spec, str):
+        spec = CONFIGS[spec]
+    if seed is None:
+        seed = CONFIG_SEED.get(spec.name, 0)
+    lens = list(lengths) if lengths is not None else draw_lengths(spec, seed)
+    R = len(lens)
+    T = int(sum(lens))
+    H, P, N, G = spec.H, spec.P, spec.N, spec.G
+    dt_ = torch.float32 if spec.dtype == "fp32" else torch.bfloat16
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    rng = np.random.default_rng(seed + 1000)
+
+    cu = torch.zeros(R + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    prob = {
+        "spec": spec.name,
+        "lengths": lens,
+        "T": T, "R": R, "H": H, "P": P, "N": N, "G": G,
+        "chunk_size": int(chunk_size or spec.chunk_size),
+        "block_size": spec.block_size,
+        "export_chunks": spec.export_chunks,
+        "final_dense": spec.final_dense,
+        "dtype": spec.dtype,
+        "cu_seqlens": cu.to(dev),
+        "num_computed": None,
+    }
+    prob["x"] = _randn((T, H, P), gen, dev, dt_)
+    prob["dt"] = _randn((T, H), gen, dev, dt_)
+    prob["dt_bias"] = (torch.rand((H,), generator=gen, device=dev) * -1.0 - 1.0)
+    prob["A"] = -torch.exp(torch.rand((H,), generator=gen, device=dev) * math.log(16.0))
+    prob["B"] = _randn((T, G, N), gen, dev, dt_)
+    prob["C"] = _randn((T, G, N), gen, dev, dt_)
+    prob["D"] = _randn((H,), gen, dev, torch.float32) if spec.has_D else None
+    prob["z"] = _randn((T, H, P), gen, dev, dt_) if spec.has_z else None
+
+    if num_computed is not None:
+        prob["num_computed"] = torch.tensor(list(num_computed), dtype=torch.int32, device=dev)
+    ncomp = list(num_computed) if num_computed is not None else [0] * R
+
+    S = spec.pool_slots
+    init_slots = final_slots = block_table = None
+    pool = None
+    if spec.init == "tiny_req2":
+        init_slots = [-1] * R
+        init_slots[min(2, R - 1)] = 1
+    elif spec.init == "half_even":
+        perm = rng.permutation(S)
+        init_slots = [int(perm[i // 2]) if i % 2 == 0 else -1 for i in range(R)]
+    elif spec.init == "all":
+        perm = rng.permutation(S)
+        init_slots = [int(v) for v in perm[:R]]
+        used = R
+        if spec.final_slots:
+            final_slots = [int(v) for v in perm[used:used + R]]
+            used += R
+        if spec.block_size > 0:
+            bs = spec.block_size
+            W = max(1, max((ncomp[i] + lens[i]) // bs for i in range(R)))
+            block_table = np.full((R, W), -1, dtype=np.int32)
+            for i in range(R):
+                for j in range(ncomp[i] // bs, (ncomp[i] + lens[i]) // bs):
+                    block_table[i, j] = int(perm[used])
+                    used += 1
+            if used > S:
+                raise ValueError("pool too small for the block table")
+    if S > 0:
+        pool = torch.zeros((S, H, P, N), dtype=torch.float32, device=dev)
+        if canary is not None:
+            pool.fill_(canary)
+        if init_slots is not None:
+            for s in sorted({v for v in init_slots if v >= 0}):
+                pool[s] = _randn((H, P, N), gen, dev, torch.float32, spec.init_std)
+    prob["state_pool"] = pool
+    prob["init_slots"] = (torch.tensor(init_slots, dtype=torch.int32, device=dev)
+                          if init_slots is not None else None)
+    prob["final_slots"] = (torch.tensor(final_slots, dtype=torch.int32, device=dev)
+                           if final_slots is not None else None)
+    prob["block_table"] = (torch.from_numpy(block_table).to(dev)
+                           if block_table is not None else None)
+    return prob
+
+
+def to_oracle(prob: dict, requests=None) -> dict:
+    """Host float64/int64 copies of a problem, in the form oracle.forward takes.
+
+    Values are upcast exactly (bf16 and fp32 are both subsets of fp64).  With
+    ``requests`` only those requests' tokens are copied (repacked in order) and
+    the returned dict carries their original indices under "requests".
+    """
+    def h(t, dtype=np.float64):
+        return None if t is None else t.detach().to("cpu").to(torch.float64 if dtype == np.float64 else torch.int64).numpy()
+
+    cu = prob["cu_seqlens"].to("cpu").to(torch.int64).numpy()
+    out = {"chunk_size": prob["chunk_size"], "block_size": prob["block_size"],
+           "export_chunks": prob["export_chunks"]}
+    for k in ("dt_bias", "A", "D"):
+        out[k] = h(prob[k])
+    pool = prob["state_pool"]
+    if requests is None:
+        for k in ("x", "dt", "B", "C", "z"):
+            out[k] = h(prob[k])
+        out["cu_seqlens"] = cu
+        sel = list(range(len(cu) - 1))
+    else:
+        sel = list(requests)
+        pieces = {k: [] for k in ("x", "dt", "B", "C", "z")}
+        new_cu = [0]
+        for i in sel:
+            a, b = int(cu[i]), int(cu[i + 1])
+            for k in pieces:
+                if prob[k] is not None:
+                    pieces[k].append(prob[k][a:b].detach().to("cpu").to(torch.float64))
+            new_cu.append(new_cu[-1] + (b - a))
+        for k in pieces:
+            out[k] = (torch.cat(pieces[k]).numpy() if prob[k] is not None else None)
+        out["cu_seqlens"] = np.asarray(new_cu, dtype=np.int64)
+    out["requests"] = sel
+    nc = prob["num_computed"]
+    out["num_computed"] = None if nc is None else h(nc, np.int64)[sel]
+    for k in ("init_slots", "final_slots"):
+        out[k] = None if prob[k] is None else h(prob[k], np.int64)[sel]
+    bt = prob["block_table"]
+    out["block_table"] = None if bt is None else h(bt, np.int64)[sel]
+    if pool is not None:
+        used = set()
+        for k in ("init_slots", "final_slots"):
+            if out[k] is not None:
+                used.update(int(v) for v in out[k] if v >= 0)
+        if out["block_table"] is not None:
+            used.update(int(v) for v in out["block_table"].ravel() if v >= 0)
+        # Only the slots this selection touches are copied; the rest stay zero.
+        host_pool = np.zeros(tuple(pool.shape), dtype=np.float64) if requests is None else None
+        if requests is None:
+            host_pool = pool.detach().to("cpu").to(torch.float64).numpy()
+        else:
+            host_pool = _SparsePool(pool, used)
+        out["state_pool"] = host_pool
+    else:
+        out["state_pool"] = None
+    return out
+
+
+class _SparsePool:
+    """Host view of the few pool slots a sampled check touches (avoids copying 17 GB)."""
+
+    def __init__(self, pool, slots):
+        self.shape = tuple(pool.shape)
+        self.slots = {s: pool[s].detach().to("cpu").to(torch.float64).numpy() for s in slots}
+
+    def __getitem__(self, s):
+        return self.slots[int(s)]
+
+    def __setitem__(self, s, v):
+        self.slots[int(s)] = np.asarray(v, dtype=np.float64)
+
+    def copy(self):
+        c = _SparsePool.__new__(_SparsePool)
+        c.shape = self.shape
+        c.slots = {k: v.copy() for k, v in self.slots.items()}
+        return c
