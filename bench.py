@@ -1,0 +1,395 @@
+"""Benchmark: Mamba2 SSD varlen prefill tokens/s per layer on one GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config NAME] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path over one batch: the device metadata
+builder (plan) and the SSD forward (every kernel of the path), with inputs
+resident in HBM.  The workload is the uniform batch of 8 requests x 2048
+tokens, H=80, P=64, N=128, G=1, chunk_size=256, bf16 in / fp32 state, D skip
+and SiLU(z) gate (a ~2.7B Mamba2 layer).  Its inputs (~0.54 GB) exceed the
+129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy
+of the batch (independent problems: weak scaling, no data-path collective);
+value = tokens of all ranks / max-over-ranks time.
+
+--impl reference times the CPU fp64 oracle (the only reference there is: the
+pages ship no code) on this host's cores, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "uniform_8x2048"
+METRIC = "SSD varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
+KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc"]
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for d in KERNEL_SOURCES:
+        full = os.path.join(ROOT, d)
+        for name in sorted(os.listdir(full)):
+            if name.endswith((".cu", ".cuh")):
+                h.update(name.encode())
+                h.update(open(os.path.join(full, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def cost_model(prob, n_export_rows, n_block_writes):
+    """Bytes and flops one step must move / do at minimum (no chunk-state traffic).
+
+    bytes = x + y + z + B + C + dt in their dtype, + initial states read + final
+    states, chunk exports and block checkpoints written (fp32).
+    flops = T (4 P N H + Q P H + Q N G): the chunk-state and state-readout
+    contractions plus the causal halves of the intra-chunk products.
+    """
+    T, H, P, N, G = prob["T"], prob["H"], prob["P"], prob["N"], prob["G"]
+    Q = prob["chunk_size"]
+    el = 4 if prob["dtype"] == "fp32" else 2
+    tok_bytes = el * (T * H * P * (2 + (prob["z"] is not None)) + 2 * T * G * N + T * H)
+    st = H * P * N * 4
+    init_reads = 0
+    if prob["init_slots"] is not None:
+        init_reads = int((prob["init_slots"] >= 0).sum().item())
+    finals = 0
+    if prob.get("final_dense", True):
+        finals += prob["R"]
+    if prob["final_slots"] is not None:
+        finals += int((prob["final_slots"] >= 0).sum().item())
+    state_bytes = st * (init_reads + finals + n_export_rows + n_block_writes)
+    flops = T * (4 * P * N * H + Q * P * H + Q * N * G)
+    return {"bytes": tok_bytes + state_bytes, "flops": flops, "token_bytes": tok_bytes,
+            "state_bytes": state_bytes}
+
+
+def count_outputs(prob):
+    """Export rows and block-checkpoint writes of the batch (index arithmetic only)."""
+    cu = prob["cu_seqlens"].cpu().tolist()
+    nc = prob["num_computed"]
+    nc = [0] * prob["R"] if nc is None else nc.cpu().tolist()
+    Q = prob["chunk_size"]
+    rows = 0
+    blocks = 0
+    bt = prob["block_table"]
+    btl = None if bt is None else bt.cpu().tolist()
+    bs = prob["block_size"]
+    for i in range(prob["R"]):
+        L = cu[i + 1] - cu[i]
+        s = nc[i]
+        if L > 0:
+            rows += (s + L - 1) // Q - s // Q + 1
+        if btl is not None and bs > 0:
+            kb = (s // bs + 1) * bs
+            while kb <= s + L:
+                if btl[i][kb // bs - 1] >= 0:
+                    blocks += 1
+                kb += bs
+    return (rows if prob["export_chunks"] else 0), blocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        sms = sorted(r["sm"] for r in loaded)
+        reasons = set()
+        for r in loaded:
+            if r["hw"].lower() == "active":
+                reasons.add("hw_slowdown")
+            if r["hwt"].lower() == "active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].lower() == "active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"].lower() == "active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+def read_traffic(kernel_hash):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when the summary is absent or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == "dram_bytes_per_launch":
+            if parts[2] == kernel_hash:
+                return float(parts[1])
+    return None
+
+
+def cpu_baseline(prob, max_seconds=30.0):
+    """Time the fp64 oracle, as it stands, on this host's cores."""
+    import oracle
+    import workloads
+    ncores = os.cpu_count() or 1
+    # Sample: whole requests, as many as fit the CPU budget (15.7 us per token-head-core
+    # measured for P=64, N=128; scaled by P*N).
+    per = 16e-6 * prob["P"] * prob["N"] / (64 * 128)
+    lens = prob["lengths"]
+    sel = []
+    tok = 0
+    for i, L in enumerate(lens):
+        if sel and (tok + L) * prob["H"] * per / ncores > max_seconds:
+            break
+        sel.append(i)
+        tok += L
+    o = workloads.to_oracle(prob, requests=sel)
+    t0 = time.perf_counter()
+    oracle.forward(o, n_threads=ncores)
+    dt = time.perf_counter() - t0
+    return {"value": tok / dt, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+            "sample": f"{len(sel)} of {len(lens)} requests ({tok} tokens, all {prob['H']} heads), "
+                      f"fp64 token-by-token recurrence, {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    import workloads
+    if rank != 0:
+        return
+    prob = workloads.make_problem(args.config, device="cpu")
+    # Each step: a bounded sample (whole requests) sized so the run stays within minutes.
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(prob, max_seconds=budget)
+    vals = []
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline(prob, max_seconds=budget)
+        vals.append(last["value"])
+    value = sorted(vals)[len(vals) // 2]
+    T = prob["T"]
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": T / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.config, "T": T, "R": prob["R"], "H": prob["H"],
+                       "P": prob["P"], "N": prob["N"], "G": prob["G"],
+                       "chunk_size": prob["chunk_size"]},
+            "cpu_baseline": {**last, "value": value},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, local_rank, world = env_rank()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import mamba2_ssd_varlen_gb300 as m
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    m.load_library()
+    peaks = load_peaks()
+    prob = workloads.make_problem(args.config, device="cuda")
+    call = m.Call(prob)
+    stream = torch.cuda.current_stream()
+    n_rows, n_blocks = count_outputs(prob)
+    cost = cost_model(prob, n_rows, n_blocks)
+    kernels_per_forward = 1
+
+    def step():
+        call.make_plan()
+        call.forward()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert call.status() == 0, "device error during warm-up"
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(K):
+        e0, e1, e2 = ev[k]
+        e0.record(stream)
+        call.make_plan()
+        e1.record(stream)
+        call.forward()
+        e2.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = sorted(e1.elapsed_time(e2) for _, e1, e2 in ev)
+    plan_ms = sorted(e0.elapsed_time(e1) for e0, e1, _ in ev)
+    fwd_avg = sum(fwd_ms) / K
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert call.status() == 0, "device error during the timed region"
+    ms_per_step = total_ms / K
+    T = prob["T"]
+    value = T * world / (ms_per_step / 1e3)
+
+    # End to end through the public API: pinned host inputs -> device, plan,
+    # forward, result -> host, every step.
+    host_in = {k: prob[k].cpu().pin_memory() for k in ("x", "dt", "B", "C", "z", "cu_seqlens")
+               if prob[k] is not None}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    y_host = torch.empty(call.y.shape, dtype=call.y.dtype, pin_memory=True)
+    fs_host = (torch.empty(call.final_states.shape, dtype=torch.float32, pin_memory=True)
+               if call.final_states is not None else None)
+    d2h = y_host.numel() * y_host.element_size() + (0 if fs_host is None else fs_host.numel() * 4)
+
+    def e2e_step():
+        for k_, t_ in host_in.items():
+            prob[k_].copy_(t_, non_blocking=True)
+        call.make_plan()
+        call.forward()
+        y_host.copy_(call.y, non_blocking=True)
+        if fs_host is not None:
+            fs_host.copy_(call.final_states, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    KE = args.e2e_steps
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / KE
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    khash = kernel_source_hash()
+    achieved = cost["bytes"] / (fwd_avg / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": read_traffic(khash), "peak_source": peaks["source"],
+                "algorithmic_bytes": cost["bytes"], "algorithmic_flops": cost["flops"],
+                "kernel": "ssd_varlen_forward", "kernel_ms_avg": round(fwd_avg, 5),
+                "tensor_frac_of_peak": round(cost["flops"] / (fwd_avg / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob["dtype"] == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": args.config, "T": T, "R": prob["R"], "H": prob["H"],
+                       "P": prob["P"], "N": prob["N"], "G": prob["G"],
+                       "chunk_size": prob["chunk_size"], "global_batch": prob["R"], "seq_len": T // prob["R"],
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "roofline": roofline,
+            "plan_ms_median": plan_ms[K // 2], "forward_ms_median": fwd_ms[K // 2],
+            "gpu_launches": K * (1 + kernels_per_forward),
+            "clocks": clocks,
+            "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "kernel_hash": khash}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(workloads.make_problem(args.config, device="cpu"))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * ssd_varlen.h -- C ABI of the GB300 Mamba2 SSD varlen prefill library.
+ *
+ * The operation (one layer, one call):
+ *   Tokens of R requests are packed as x (T,H,P) with cu_seqlens (R+1) marking
+ *   where each request starts; there is no padding and no batch dimension
+ *   ("[Model] Mamba2 varlen and metadata refactor", Purpose item 1).  For every
+ *   request i and head h, with group g = h / (H/G), the SSD scan runs
+ *       dt'  = softplus(dt[t,h] + dt_bias[h])
+ *       h_t  = exp(dt' A[h]) h_{t-1} + dt' x[t,h,:] (outer) B[t,g,:]     (P x N)
+ *       y[t,h,:] = (h_t C[t,g,:] + D[h] x[t,h,:]) * silu(z[t,h,:])
+ *   starting from the request's initial state (a pool slot, or zeros), which
+ *   must decay from the request's first token even inside a partial first
+ *   chunk ("[Bugfix] Mamba2 SSD varlen bug fix initstates decay, improve test,
+ *   assert chunk pwr 2", instinctive explanation items 1-4).  chunk_size is a
+ *   power of two and does not change the result (same page, Purpose note).
+ *   Optional state outputs: the final state per request (dense and/or into a
+ *   pool slot), the state after every chunk (per-chunk intermediate-state
+ *   export), and the state at every block boundary scattered into pool slots
+ *   through a per-request block table ("Automatic prefix caching for GDN hybrid
+ *   models (mamba_cache_mode=all) with MTP speculative decoding", Purpose and
+ *   Kernels/layers: intermediate-state export, block-aligned checkpoint
+ *   scatter, dual read/write state anchors).
+ *
+ * Chunks are cut at ABSOLUTE positions: a request with s = num_computed[i]
+ * tokens already in its state covers positions [s, s+L_i); chunk boundaries are
+ * the multiples of chunk_size, block boundaries the multiples of block_size.
+ * Chunk j of request i is row chunk_first[i] + j of the export buffer, where
+ * chunk_first is the exclusive prefix sum of the per-request chunk counts; its
+ * exported state is the state after the chunk's last token.  A block boundary
+ * kb (s < kb <= s+L_i) writes the state after position kb-1 to
+ * state_pool[block_table[i*block_table_width + kb/block_size - 1]]; entries < 0
+ * are skipped.
+ *
+ * Layouts: row-major, last index fastest.  x, z, y (T,H,P); B, C (T,G,N);
+ * dt (T,H); dt_bias, A, D (H) fp32; states (..., H, P, N) fp32.
+ * x, dt, B, C, z, y share one dtype (bf16 or fp32).
+ *
+ * Ownership: the caller allocates every buffer, device workspace included;
+ * the library allocates nothing and launches only on the stream it is given.
+ * Every device pointer must be 16-byte aligned and every tensor contiguous.
+ *
+ * Errors: host-detectable problems return a negative ssd_status and launch
+ * nothing.  Problems only the device can see (a cu_seqlens entry out of
+ * order, a slot or table entry out of range) set bits in a device error word
+ * held in the workspace; the offending read is treated as zeros and the
+ * offending write is skipped.  Nothing traps.  ssd_varlen_status reads and
+ * clears the word (it synchronises the plan's stream).
+ */
+#ifndef SSD_VARLEN_H
+#define SSD_VARLEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum ssd_dtype { SSD_DTYPE_BF16 = 0, SSD_DTYPE_F32 = 1 };
+
+enum ssd_status {
+    SSD_OK = 0,
+    SSD_ERR_NULL = -1,          /* a required pointer is NULL */
+    SSD_ERR_DIMS = -2,          /* a size is out of range (T, R, H, P, N, G, slots) */
+    SSD_ERR_CHUNK_SIZE = -3,    /* chunk_size is not an integer power of 2 in [16, 256] */
+    SSD_ERR_GROUPS = -4,        /* H is not a multiple of G */
+    SSD_ERR_BLOCK_SIZE = -5,    /* block_size is not a multiple of chunk_size */
+    SSD_ERR_DTYPE = -6,         /* unknown dtype */
+    SSD_ERR_ALIGN = -7,         /* a device pointer is not 16-byte aligned */
+    SSD_ERR_WORKSPACE = -8,     /* workspace too small or misaligned */
+    SSD_ERR_PLAN = -9,          /* plan not built, or built for other dims */
+    SSD_ERR_CUDA = -10,         /* a CUDA runtime call failed */
+    SSD_ERR_UNSUPPORTED = -11   /* a combination this build does not handle */
+};
+
+/* Bits of the device error word (ssd_varlen_status). */
+#define SSD_DEVERR_CU_SEQLENS 0x1    /* cu_seqlens[0] != 0, decreasing, or cu[R] != T */
+#define SSD_DEVERR_NUM_COMPUTED 0x2  /* negative num_computed, or s + L beyond 2^31 - 1 */
+#define SSD_DEVERR_INIT_SLOT 0x4     /* init slot >= num_slots (read as zeros) */
+#define SSD_DEVERR_FINAL_SLOT 0x8    /* final slot >= num_slots (write skipped) */
+#define SSD_DEVERR_BLOCK_SLOT 0x10   /* block-table slot >= num_slots (write skipped) */
+#define SSD_DEVERR_BLOCK_TABLE 0x20  /* a boundary needs a column >= block_table_width */
+#define SSD_DEVERR_TIMEOUT 0x40      /* a bounded wait between CTAs gave up */
+
+/* Problem sizes.  Filled by the caller, copied into the plan. */
+typedef struct ssd_dims {
+    int64_t T;                 /* total tokens, >= 0 */
+    int32_t R;                 /* requests, >= 1 */
+    int32_t H, P, N, G;        /* heads, headdim, d_state, groups (H % G == 0) */
+    int32_t chunk_size;        /* power of 2 in [16, 256] */
+    int32_t dtype;             /* enum ssd_dtype of x, dt, B, C, z, y */
+    int32_t num_slots;         /* rows of state_pool (0 when no pool is used) */
+    int32_t block_size;        /* block-checkpoint granularity; 0 = no scatter */
+    int32_t block_table_width; /* columns of block_table */
+    int32_t reserved;          /* must be 0 */
+} ssd_dims;
+
+/* Per-batch plan: host-side handle to device metadata kept in the workspace.
+ * Built once per batch by ssd_varlen_plan and reused by every layer's
+ * ssd_varlen_forward while cu_seqlens / num_computed stay unchanged.  The
+ * fields are the library's; callers treat the struct as opaque. */
+typedef struct ssd_plan {
+    ssd_dims dims;
+    void *workspace;
+    size_t workspace_bytes;
+    const int32_t *cu_seqlens;
+    const int32_t *num_computed;
+    int64_t max_chunks;        /* bound on export rows: ceil(T/Q) + R */
+    int64_t max_segs;          /* bound on work segments */
+    int32_t seg_len;           /* tokens per work segment (multiple of 128) */
+    int32_t flags;
+    uint64_t magic;
+    cudaStream_t stream;       /* the stream the plan was built on */
+} ssd_plan;
+
+typedef struct ssd_inputs {
+    const void *x;             /* (T,H,P) */
+    const void *dt;            /* (T,H) */
+    const float *dt_bias;      /* (H) */
+    const float *A;            /* (H) */
+    const void *B;             /* (T,G,N) */
+    const void *C;             /* (T,G,N) */
+    const float *D;            /* (H) or NULL: no skip term */
+    const void *z;             /* (T,H,P) or NULL: no gate */
+    const int32_t *init_slots; /* (R) or NULL: every request starts from zeros; -1 = zeros */
+    float *state_pool;         /* (num_slots,H,P,N) or NULL; read through init_slots,
+                                  written through final_slots and block_table */
+} ssd_inputs;
+
+typedef struct ssd_outputs {
+    void *y;                   /* (T,H,P), required */
+    float *final_states;       /* (R,H,P,N) or NULL */
+    const int32_t *final_slots;/* (R) or NULL; -1 = do not write that request */
+    float *chunk_states;       /* (n_chunks,H,P,N) or NULL; n_chunks = ssd_varlen_count_chunks */
+    const int32_t *block_table;/* (R, block_table_width) or NULL; needs block_size > 0 */
+} ssd_outputs;
+
+/* Bytes of device workspace the plan and forward need for these dims. */
+size_t ssd_varlen_workspace_size(const ssd_dims *dims);
+
+/* Export rows for a batch, from HOST copies of cu_seqlens (R+1) and
+ * num_computed (R, or NULL for zeros).  Negative on bad input. */
+int64_t ssd_varlen_count_chunks(const int32_t *cu_seqlens_host, const int32_t *num_computed_host,
+                                int32_t R, int32_t chunk_size);
+
+/* Validates dims, then launches the device metadata builder on `stream`:
+ * per-request chunk and segment offsets and the segment work list, computed
+ * from cu_seqlens (device, R+1) and num_computed (device, R, or NULL) without
+ * a host synchronisation.  Fills *out.  The workspace (16-byte aligned, at
+ * least ssd_varlen_workspace_size bytes) holds the metadata until the next
+ * plan on it. */
+int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32_t *num_computed,
+                    void *workspace, size_t workspace_bytes, cudaStream_t stream, ssd_plan *out);
+
+/* One SSD varlen prefill over the planned batch, launched on `stream`
+ * (normally the plan's stream; another stream must be ordered after it).
+ * Writes y and whichever state outputs are non-NULL.  Write slots must not
+ * alias slots read in the same call. */
+int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out,
+                       cudaStream_t stream);
+
+/* Synchronises the plan's stream, returns the device error bits in
+ * *device_err and clears them.  Returns SSD_OK or SSD_ERR_CUDA. */
+int ssd_varlen_status(const ssd_plan *plan, int *device_err);
+
+/* Static description of a status code or device error bit set. */
+const char *ssd_varlen_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_VARLEN_H */

@@ -1,0 +1,234 @@
+"""Python binding of the GB300 Mamba2 SSD varlen prefill library (ctypes).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+libssd_varlen.so, called through its C ABI (include/ssd_varlen.h).  PyTorch
+only provides device memory and the current stream.  There is no CPU
+fallback: if the library is missing the calls raise.
+
+The functions keep the C names:
+  ssd_varlen_workspace_size(dims)                 -> bytes
+  ssd_varlen_count_chunks(cu_host, ncomp_host, Q) -> export rows
+  ssd_varlen_plan(dims, cu_seqlens, num_computed, workspace) -> Plan
+  ssd_varlen_forward(plan, inputs, outputs)
+  ssd_varlen_status(plan)                          -> device error bits
+  ssd_varlen_strerror(code)                        -> text
+and ``run(...)`` wires a whole call from torch tensors (tests and bench use it).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libssd_varlen.so")
+
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+
+DEVERR = {
+    "CU_SEQLENS": 0x1, "NUM_COMPUTED": 0x2, "INIT_SLOT": 0x4, "FINAL_SLOT": 0x8,
+    "BLOCK_SLOT": 0x10, "BLOCK_TABLE": 0x20, "TIMEOUT": 0x40,
+}
+STATUS = {
+    0: "OK", -1: "NULL", -2: "DIMS", -3: "CHUNK_SIZE", -4: "GROUPS", -5: "BLOCK_SIZE",
+    -6: "DTYPE", -7: "ALIGN", -8: "WORKSPACE", -9: "PLAN", -10: "CUDA", -11: "UNSUPPORTED",
+}
+EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
+            "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror"]
+
+c_i32, c_i64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+
+
+class ssd_dims(ctypes.Structure):
+    _fields_ = [("T", c_i64), ("R", c_i32), ("H", c_i32), ("P", c_i32), ("N", c_i32),
+                ("G", c_i32), ("chunk_size", c_i32), ("dtype", c_i32), ("num_slots", c_i32),
+                ("block_size", c_i32), ("block_table_width", c_i32), ("reserved", c_i32)]
+
+
+class ssd_plan(ctypes.Structure):
+    _fields_ = [("dims", ssd_dims), ("workspace", c_vp), ("workspace_bytes", ctypes.c_size_t),
+                ("cu_seqlens", c_vp), ("num_computed", c_vp), ("max_chunks", c_i64),
+                ("max_segs", c_i64), ("seg_len", c_i32), ("flags", c_i32),
+                ("magic", ctypes.c_uint64), ("stream", c_vp)]
+
+
+class ssd_inputs(ctypes.Structure):
+    _fields_ = [("x", c_vp), ("dt", c_vp), ("dt_bias", c_vp), ("A", c_vp), ("B", c_vp),
+                ("C", c_vp), ("D", c_vp), ("z", c_vp), ("init_slots", c_vp),
+                ("state_pool", c_vp)]
+
+
+class ssd_outputs(ctypes.Structure):
+    _fields_ = [("y", c_vp), ("final_states", c_vp), ("final_slots", c_vp),
+                ("chunk_states", c_vp), ("block_table", c_vp)]
+
+
+class SsdError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({ssd_varlen_strerror(code)})")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library():
+    """Load libssd_varlen.so (built by build.py).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.ssd_varlen_workspace_size.argtypes = [ctypes.POINTER(ssd_dims)]
+    lib.ssd_varlen_workspace_size.restype = ctypes.c_size_t
+    lib.ssd_varlen_count_chunks.argtypes = [c_vp, c_vp, c_i32, c_i32]
+    lib.ssd_varlen_count_chunks.restype = c_i64
+    lib.ssd_varlen_plan.argtypes = [ctypes.POINTER(ssd_dims), c_vp, c_vp, c_vp, ctypes.c_size_t,
+                                    c_vp, ctypes.POINTER(ssd_plan)]
+    lib.ssd_varlen_plan.restype = ctypes.c_int
+    lib.ssd_varlen_forward.argtypes = [ctypes.POINTER(ssd_plan), ctypes.POINTER(ssd_inputs),
+                                       ctypes.POINTER(ssd_outputs), c_vp]
+    lib.ssd_varlen_forward.restype = ctypes.c_int
+    lib.ssd_varlen_status.argtypes = [ctypes.POINTER(ssd_plan), ctypes.POINTER(ctypes.c_int)]
+    lib.ssd_varlen_status.restype = ctypes.c_int
+    lib.ssd_varlen_strerror.argtypes = [ctypes.c_int]
+    lib.ssd_varlen_strerror.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_dims(T, R, H, P, N, G, chunk_size, dtype, num_slots=0, block_size=0,
+              block_table_width=0) -> ssd_dims:
+    return ssd_dims(int(T), int(R), int(H), int(P), int(N), int(G), int(chunk_size), int(dtype),
+                    int(num_slots), int(block_size), int(block_table_width), 0)
+
+
+def ssd_varlen_strerror(code: int) -> str:
+    return load_library().ssd_varlen_strerror(int(code)).decode()
+
+
+def ssd_varlen_workspace_size(dims: ssd_dims) -> int:
+    return int(load_library().ssd_varlen_workspace_size(ctypes.byref(dims)))
+
+
+def ssd_varlen_count_chunks(cu_host, ncomp_host, chunk_size) -> int:
+    import numpy as np
+    cu = np.ascontiguousarray(cu_host, dtype=np.int32)
+    nc = None if ncomp_host is None else np.ascontiguousarray(ncomp_host, dtype=np.int32)
+    n = load_library().ssd_varlen_count_chunks(
+        cu.ctypes.data_as(c_vp), None if nc is None else nc.ctypes.data_as(c_vp),
+        cu.shape[0] - 1, int(chunk_size))
+    if n < 0:
+        raise SsdError(int(n), "ssd_varlen_count_chunks")
+    return int(n)
+
+
+def ssd_varlen_plan(dims: ssd_dims, cu_seqlens, num_computed, workspace, stream=None) -> ssd_plan:
+    plan = ssd_plan()
+    rc = load_library().ssd_varlen_plan(ctypes.byref(dims), _ptr(cu_seqlens), _ptr(num_computed),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream), ctypes.byref(plan))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_plan")
+    return plan
+
+
+def ssd_varlen_forward(plan: ssd_plan, inputs: ssd_inputs, outputs: ssd_outputs, stream=None):
+    rc = load_library().ssd_varlen_forward(ctypes.byref(plan), ctypes.byref(inputs),
+                                           ctypes.byref(outputs), _stream(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_forward")
+
+
+def ssd_varlen_status(plan: ssd_plan) -> int:
+    v = ctypes.c_int(0)
+    rc = load_library().ssd_varlen_status(ctypes.byref(plan), ctypes.byref(v))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_status")
+    return int(v.value)
+
+
+def make_inputs(x, dt, dt_bias, A, B, C, D=None, z=None, init_slots=None, state_pool=None):
+    return ssd_inputs(_ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                      _ptr(z), _ptr(init_slots), _ptr(state_pool))
+
+
+def make_outputs(y, final_states=None, final_slots=None, chunk_states=None, block_table=None):
+    return ssd_outputs(_ptr(y), _ptr(final_states), _ptr(final_slots), _ptr(chunk_states),
+                       _ptr(block_table))
+
+
+class Call:
+    """One planned batch: the tensors, the plan and the pre-built argument structs."""
+
+    def __init__(self, prob: dict, want_final=True, want_chunks=None, stream=None):
+        import torch
+        self.prob = prob
+        x = prob["x"]
+        dev = x.device
+        T, H, P = x.shape
+        N = prob["B"].shape[2]
+        G = prob["B"].shape[1]
+        R = prob["cu_seqlens"].shape[0] - 1
+        Q = int(prob["chunk_size"])
+        dtype = DTYPE_F32 if x.dtype == torch.float32 else DTYPE_BF16
+        pool = prob.get("state_pool")
+        bt = prob.get("block_table")
+        self.dims = make_dims(T, R, H, P, N, G, Q, dtype,
+                              num_slots=0 if pool is None else pool.shape[0],
+                              block_size=int(prob.get("block_size") or 0),
+                              block_table_width=0 if bt is None else bt.shape[1])
+        self.workspace = torch.empty(ssd_varlen_workspace_size(self.dims), dtype=torch.uint8,
+                                     device=dev)
+        self.y = torch.empty_like(x)
+        self.final_states = (torch.empty((R, H, P, N), dtype=torch.float32, device=dev)
+                             if want_final and prob.get("final_dense", True) else None)
+        export = prob.get("export_chunks") if want_chunks is None else want_chunks
+        self.chunk_states = None
+        if export:
+            cu_h = prob["cu_seqlens"].cpu().numpy()
+            nc = prob.get("num_computed")
+            nrows = ssd_varlen_count_chunks(cu_h, None if nc is None else nc.cpu().numpy(), Q)
+            self.chunk_states = torch.empty((max(nrows, 1), H, P, N), dtype=torch.float32,
+                                            device=dev)
+        self.inputs = make_inputs(x, prob["dt"], prob["dt_bias"], prob["A"], prob["B"],
+                                  prob["C"], prob.get("D"), prob.get("z"),
+                                  prob.get("init_slots"), pool)
+        self.outputs = make_outputs(self.y, self.final_states, prob.get("final_slots"),
+                                    self.chunk_states, bt)
+        self.stream = stream
+        self.plan = None
+
+    def make_plan(self):
+        self.plan = ssd_varlen_plan(self.dims, self.prob["cu_seqlens"],
+                                    self.prob.get("num_computed"), self.workspace, self.stream)
+        return self.plan
+
+    def forward(self):
+        ssd_varlen_forward(self.plan, self.inputs, self.outputs, self.stream)
+
+    def __call__(self):
+        self.make_plan()
+        self.forward()
+        return self
+
+    def status(self) -> int:
+        return ssd_varlen_status(self.plan)
+
+
+def run(prob: dict, **kw) -> Call:
+    """Plan and run one call on the current stream; returns the Call (outputs on it)."""
+    return Call(prob, **kw)()

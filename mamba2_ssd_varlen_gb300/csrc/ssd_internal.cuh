@@ -1,0 +1,87 @@
+// ssd_internal.cuh -- shared declarations of the SSD varlen library (device + host).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd_varlen.h"
+
+namespace ssd {
+
+constexpr uint64_t kPlanMagic = 0x5353445641524C31ull;  // "SSDVARL1"
+constexpr int kHdrInts = 64;                             // header words at the workspace start
+// Header word indices.
+constexpr int kHdrErr = 0;       // device error bits (SSD_DEVERR_*)
+constexpr int kHdrChunks = 1;    // export rows of the batch
+constexpr int kHdrSegs = 2;      // work segments of the batch
+constexpr int kHdrTicket = 3;    // reserved for in-order work tickets
+
+// Byte offsets of the workspace regions (each 256-byte aligned).
+struct WsLayout {
+    size_t hdr, req_first_chunk, req_first_seg, segs, seg_state, seg_decay, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// One work segment: a run of consecutive tokens of one request that a CTA walks.
+// Segments split requests at absolute multiples of seg_len.
+struct Seg {
+    int32_t req;        // request index
+    int32_t tok;        // first packed token index
+    int32_t len;        // tokens (0 only for an empty request)
+    int32_t abs_start;  // absolute position of the first token (num_computed + offset)
+};
+
+// Everything a forward kernel needs, by value.
+struct FwdParams {
+    // sizes
+    int64_t T;
+    int32_t R, H, P, N, G, Q;
+    int32_t num_slots, block_size, bt_width;
+    int32_t seg_len;
+    // plan metadata (device)
+    const int32_t *cu_seqlens;
+    const int32_t *num_computed;
+    int32_t *hdr;
+    const int32_t *req_first_chunk;
+    const int32_t *req_first_seg;
+    const Seg *segs;
+    float *seg_state;   // (max_segs, H, P, N) workspace: a segment's state (see kernels)
+    float *seg_decay;   // (max_segs, H) workspace
+    // inputs
+    const void *x, *dt, *B, *C, *z;
+    const float *dt_bias, *A, *D;
+    const int32_t *init_slots;
+    float *pool;
+    // outputs
+    void *y;
+    float *final_states;
+    const int32_t *final_slots;
+    float *chunk_states;
+    const int32_t *block_table;
+};
+
+// ---- device helpers -------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// softplus(v) = log(1 + e^v); the identity above 20 (where the two agree to fp32).
+__device__ __forceinline__ float softplus_f32(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+__device__ __forceinline__ float silu_f32(float v) { return v / (1.f + expf(-v)); }
+
+__device__ __forceinline__ void set_err(int32_t *hdr, int bits) { atomicOr(hdr + kHdrErr, bits); }
+
+// ---- launchers (defined in the .cu files) ---------------------------------
+cudaError_t launch_plan(const int32_t *cu, const int32_t *ncomp, int32_t R, int64_t T, int32_t Q,
+                        int32_t seg_len, int64_t max_segs, int32_t *hdr, int32_t *req_first_chunk,
+                        int32_t *req_first_seg, Seg *segs, cudaStream_t stream);
+
+cudaError_t launch_recurrent(const FwdParams &p, int dtype, cudaStream_t stream);
+
+}  // namespace ssd

@@ -1,0 +1,133 @@
+// ssd_plan.cu -- device-side varlen metadata builder, run once per batch.
+//
+// "[Model] Mamba2 varlen and metadata refactor", Purpose item 2: the varlen
+// metadata is computed once while the batch is prepared, not inside the first
+// layer's forward.  Here that metadata is, from cu_seqlens (and the optional
+// num_computed_tokens of each request):
+//   * req_first_chunk[i]: the request's first row in the chunk-state export
+//     (exclusive prefix sum of chunk counts; chunks cut at absolute multiples
+//     of chunk_size, so a resumed request's first chunk may be partial);
+//   * req_first_seg[i] and the segment list: runs of at most seg_len tokens,
+//     cut at absolute multiples of seg_len, that the forward kernels walk;
+//   * validation bits for the device error word.
+// One CTA of 1024 threads; no host synchronisation.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Block-wide exclusive scan of two counters; returns the block totals.
+__device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
+    __shared__ int wa[32], wb[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int va = __shfl_up_sync(0xffffffffu, ia, o), vb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) { ia += va; ib += vb; }
+    }
+    if (lane == 31) { wa[warp] = ia; wb[warp] = ib; }
+    __syncthreads();
+    if (warp == 0) {
+        int sa = wa[lane], sb = wb[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int va = __shfl_up_sync(0xffffffffu, sa, o), vb = __shfl_up_sync(0xffffffffu, sb, o);
+            if (lane >= o) { sa += va; sb += vb; }
+        }
+        wa[lane] = sa;
+        wb[lane] = sb;
+    }
+    __syncthreads();
+    const int pa = warp ? wa[warp - 1] : 0, pb = warp ? wb[warp - 1] : 0;
+    ea = pa + ia - a;
+    eb = pb + ib - b;
+    ta = wa[31];
+    tb = wb[31];
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, int32_t R, int64_t T,
+            int32_t Q, int32_t seg_len, int64_t max_segs, int32_t *hdr,
+            int32_t *__restrict__ req_first_chunk, int32_t *__restrict__ req_first_seg,
+            Seg *__restrict__ segs) {
+    __shared__ int s_err;
+    if (threadIdx.x == 0) s_err = 0;
+    __syncthreads();
+    int err = 0;
+    int carry_c = 0, carry_s = 0;
+    for (int base = 0; base < R; base += kPlanThreads) {
+        const int i = base + threadIdx.x;
+        int nc = 0, ns = 0;
+        if (i < R) {
+            const int64_t a = cu[i], b = cu[i + 1];
+            int64_t L = b - a;
+            int64_t s = ncomp ? (int64_t)ncomp[i] : 0;
+            if (L < 0 || (i == 0 && a != 0)) { err |= SSD_DEVERR_CU_SEQLENS; L = 0; }
+            if (s < 0 || s + L > 0x7fffffffLL) { err |= SSD_DEVERR_NUM_COMPUTED; s = 0; }
+            if (L > 0) {
+                nc = (int)((s + L - 1) / Q - s / Q + 1);
+                ns = (int)((s + L - 1) / seg_len - s / seg_len + 1);
+            } else {
+                ns = 1;  // an empty request still gets one (empty) segment: final = initial
+            }
+        }
+        int ec, es, tc, ts;
+        block_scan2(nc, ns, ec, es, tc, ts);
+        if (i < R) {
+            req_first_chunk[i] = carry_c + ec;
+            req_first_seg[i] = carry_s + es;
+        }
+        carry_c += tc;
+        carry_s += ts;
+    }
+    if (threadIdx.x == 0) {
+        if ((int64_t)cu[R] != T) err |= SSD_DEVERR_CU_SEQLENS;
+        req_first_chunk[R] = carry_c;
+        req_first_seg[R] = carry_s;
+    }
+    if (err) atomicOr(&s_err, err);
+    __syncthreads();
+    const int all_err = s_err;
+    const bool bad = (all_err & (SSD_DEVERR_CU_SEQLENS | SSD_DEVERR_NUM_COMPUTED)) != 0 ||
+                     (int64_t)carry_s > max_segs;
+    if (threadIdx.x == 0) {
+        hdr[kHdrErr] = all_err;
+        hdr[kHdrChunks] = bad ? 0 : carry_c;
+        hdr[kHdrSegs] = bad ? 0 : carry_s;
+        hdr[kHdrTicket] = 0;
+    }
+    if (bad) return;  // forward kernels see zero segments and write nothing
+    __syncthreads();
+    // Fill the segment list (one thread per request; long requests loop).
+    for (int i = threadIdx.x; i < R; i += kPlanThreads) {
+        const int64_t a = cu[i], L = (int64_t)cu[i + 1] - a;
+        const int64_t s = ncomp ? (int64_t)ncomp[i] : 0;
+        const int first = req_first_seg[i], cnt = req_first_seg[i + 1] - first;
+        if (L == 0) {
+            segs[first] = Seg{i, (int32_t)a, 0, (int32_t)s};
+            continue;
+        }
+        const int64_t s0 = s / seg_len;
+        for (int k = 0; k < cnt; ++k) {
+            const int64_t lo = max(s, (s0 + k) * (int64_t)seg_len);
+            const int64_t hi = min(s + L, (s0 + k + 1) * (int64_t)seg_len);
+            segs[first + k] = Seg{i, (int32_t)(a + (lo - s)), (int32_t)(hi - lo), (int32_t)lo};
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t *cu, const int32_t *ncomp, int32_t R, int64_t T, int32_t Q,
+                        int32_t seg_len, int64_t max_segs, int32_t *hdr, int32_t *req_first_chunk,
+                        int32_t *req_first_seg, Seg *segs, cudaStream_t stream) {
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, ncomp, R, T, Q, seg_len, max_segs, hdr,
+                                                req_first_chunk, req_first_seg, segs);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,127 @@
+"""C-ABI library: loads, exports every declared symbol, host-side validation (CPU only).
+
+No call here reaches the GPU: every argument error is caught by the host code
+before any launch, so these run on a machine without a CUDA device.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import mamba2_ssd_varlen_gb300 as m
+from oracle import checkpoints
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mamba2_ssd_varlen_gb300 import build
+    build.build()
+    return m.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssd_varlen.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_varlen_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert set(declared) == set(m.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_struct_sizes_match_header(lib):
+    # ssd_dims: int64 + 11 int32 = 56 bytes; the binding mirrors the header.
+    assert ctypes.sizeof(m.ssd_dims) == 56
+    assert ctypes.sizeof(m.ssd_inputs) == 10 * 8
+    assert ctypes.sizeof(m.ssd_outputs) == 5 * 8
+
+
+def _dims(**kw):
+    base = dict(T=64, R=3, H=4, P=16, N=16, G=1, chunk_size=16, dtype=m.DTYPE_F32,
+                num_slots=3, block_size=0, block_table_width=0)
+    base.update(kw)
+    return m.make_dims(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk_size=17), -3), (dict(chunk_size=8), -3), (dict(chunk_size=512), -3),
+    (dict(chunk_size=0), -3), (dict(G=3), -4), (dict(H=0), -2), (dict(R=0), -2),
+    (dict(T=-1), -2), (dict(dtype=7), -6), (dict(block_size=24), -5),
+    (dict(block_size=-16), -5), (dict(N=48), -11), (dict(P=512), -2),
+])
+def test_plan_rejects_bad_dims_before_launch(lib, kw, code):
+    d = _dims(**kw)
+    plan = m.ssd_plan()
+    rc = lib.ssd_varlen_plan(ctypes.byref(d), ctypes.c_void_p(0x1000), None,
+                             ctypes.c_void_p(0x2000), 1 << 20, None, ctypes.byref(plan))
+    assert rc == code
+    assert lib.ssd_varlen_workspace_size(ctypes.byref(d)) == 0
+
+
+def test_plan_null_and_workspace_checks(lib):
+    d = _dims()
+    plan = m.ssd_plan()
+    ws = lib.ssd_varlen_workspace_size(ctypes.byref(d))
+    assert ws > 0 and ws % 256 == 0
+    assert lib.ssd_varlen_plan(ctypes.byref(d), None, None, ctypes.c_void_p(0x2000), ws, None,
+                               ctypes.byref(plan)) == -1
+    assert lib.ssd_varlen_plan(ctypes.byref(d), ctypes.c_void_p(0x1000), None,
+                               ctypes.c_void_p(0x2008), ws, None, ctypes.byref(plan)) == -8
+    assert lib.ssd_varlen_plan(ctypes.byref(d), ctypes.c_void_p(0x1000), None,
+                               ctypes.c_void_p(0x2000), ws - 1, None, ctypes.byref(plan)) == -8
+    assert lib.ssd_varlen_plan(ctypes.byref(d), ctypes.c_void_p(0x1002), None,
+                               ctypes.c_void_p(0x2000), ws, None, ctypes.byref(plan)) == -7
+
+
+def test_forward_rejects_unplanned_and_bad_pointers(lib):
+    plan = m.ssd_plan()
+    inp = m.ssd_inputs()
+    out = m.ssd_outputs()
+    assert lib.ssd_varlen_forward(ctypes.byref(plan), ctypes.byref(inp), ctypes.byref(out), None) == -9
+    # A plan-shaped struct with the right magic but NULL tensors fails the NULL check.
+    plan.dims = _dims()
+    plan.magic = 0x5353445641524C31
+    plan.workspace = 0x10000
+    plan.workspace_bytes = 1 << 30
+    plan.seg_len = 2048
+    assert lib.ssd_varlen_forward(ctypes.byref(plan), ctypes.byref(inp), ctypes.byref(out), None) == -1
+    good = 0x100000
+    inp = m.ssd_inputs(good, good, good, good, good, good, None, None, None, None)
+    out = m.ssd_outputs(good, None, None, None, None)
+    bad = m.ssd_inputs(good + 8, good, good, good, good, good, None, None, None, None)
+    assert lib.ssd_varlen_forward(ctypes.byref(plan), ctypes.byref(bad), ctypes.byref(out), None) == -7
+    # Using slots without a pool.
+    withslots = m.ssd_inputs(good, good, good, good, good, good, None, None, good, None)
+    assert lib.ssd_varlen_forward(ctypes.byref(plan), ctypes.byref(withslots), ctypes.byref(out), None) == -1
+    # A block table without block_size.
+    plan.dims = _dims(block_size=0)
+    bt_out = m.ssd_outputs(good, None, None, None, good)
+    pool_in = m.ssd_inputs(good, good, good, good, good, good, None, None, None, good)
+    assert lib.ssd_varlen_forward(ctypes.byref(plan), ctypes.byref(pool_in), ctypes.byref(bt_out), None) == -5
+
+
+def test_strerror_names_the_power_of_two_rule(lib):
+    assert "power of 2" in m.ssd_varlen_strerror(-3)
+    assert m.ssd_varlen_strerror(0) == "ok"
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_count_chunks_matches_checkpoint_definition(lib, seed):
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 20))
+    lens = rng.integers(0, 700, R)
+    ncomp = rng.integers(0, 1000, R)
+    cu = np.zeros(R + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    for Q in (16, 32, 64, 128, 256):
+        _, first = checkpoints.checkpoint_records(lens, ncomp, Q)
+        assert m.ssd_varlen_count_chunks(cu, ncomp, Q) == first[-1]
+        _, first0 = checkpoints.checkpoint_records(lens, None, Q)
+        assert m.ssd_varlen_count_chunks(cu, None, Q) == first0[-1]

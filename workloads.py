@@ -191,72 +191,78 @@ def make_problem(spec: Spec | str, seed: int | None = None, device="cpu", length
     return prob
 
 
-def to_oracle(prob: dict, requests=None) -> dict:
+def to_oracle(prob: dict, requests=None, heads=None) -> dict:
     """Host float64/int64 copies of a problem, in the form oracle.forward takes.
 
     Values are upcast exactly (bf16 and fp32 are both subsets of fp64).  With
-    ``requests`` only those requests' tokens are copied (repacked in order) and
-    the returned dict carries their original indices under "requests".
+    ``requests`` only those requests' tokens are copied (repacked in order); the
+    original indices are kept under "requests".  With ``heads`` only those
+    heads are copied; each selected head then gets its own group (its B and C
+    columns are copied alongside), which leaves every head's inputs unchanged.
     """
-    def h(t, dtype=np.float64):
-        return None if t is None else t.detach().to("cpu").to(torch.float64 if dtype == np.float64 else torch.int64).numpy()
+    def f64(t):
+        return None if t is None else t.detach().to("cpu").to(torch.float64).numpy()
 
-    cu = prob["cu_seqlens"].to("cpu").to(torch.int64).numpy()
+    def i64(t):
+        return None if t is None else t.detach().to("cpu").to(torch.int64).numpy()
+
+    H = prob["H"]
+    G = prob["G"]
+    hsel = list(range(H)) if heads is None else [int(h) for h in heads]
+    gsel = [h // (H // G) for h in hsel] if heads is not None else list(range(G))
+    cu = i64(prob["cu_seqlens"])
+    sel = list(range(len(cu) - 1)) if requests is None else [int(i) for i in requests]
     out = {"chunk_size": prob["chunk_size"], "block_size": prob["block_size"],
-           "export_chunks": prob["export_chunks"]}
-    for k in ("dt_bias", "A", "D"):
-        out[k] = h(prob[k])
-    pool = prob["state_pool"]
-    if requests is None:
-        for k in ("x", "dt", "B", "C", "z"):
-            out[k] = h(prob[k])
-        out["cu_seqlens"] = cu
-        sel = list(range(len(cu) - 1))
-    else:
-        sel = list(requests)
-        pieces = {k: [] for k in ("x", "dt", "B", "C", "z")}
-        new_cu = [0]
-        for i in sel:
-            a, b = int(cu[i]), int(cu[i + 1])
-            for k in pieces:
-                if prob[k] is not None:
-                    pieces[k].append(prob[k][a:b].detach().to("cpu").to(torch.float64))
-            new_cu.append(new_cu[-1] + (b - a))
+           "export_chunks": prob["export_chunks"], "requests": sel, "heads": hsel}
+    out["dt_bias"] = f64(prob["dt_bias"])[hsel]
+    out["A"] = f64(prob["A"])[hsel]
+    out["D"] = None if prob["D"] is None else f64(prob["D"])[hsel]
+    hidx = torch.tensor(hsel, dtype=torch.long)
+    gidx = torch.tensor(gsel, dtype=torch.long)
+    pieces = {k: [] for k in ("x", "dt", "B", "C", "z")}
+    new_cu = [0]
+    for i in sel:
+        a, b = int(cu[i]), int(cu[i + 1])
         for k in pieces:
-            out[k] = (torch.cat(pieces[k]).numpy() if prob[k] is not None else None)
-        out["cu_seqlens"] = np.asarray(new_cu, dtype=np.int64)
-    out["requests"] = sel
+            t = prob[k]
+            if t is None:
+                continue
+            t = t[a:b].detach().to("cpu")
+            t = t.index_select(1, gidx if k in ("B", "C") else hidx)
+            pieces[k].append(t.to(torch.float64))
+        new_cu.append(new_cu[-1] + (b - a))
+    for k in pieces:
+        out[k] = torch.cat(pieces[k]).numpy() if prob[k] is not None else None
+    out["cu_seqlens"] = np.asarray(new_cu, dtype=np.int64)
     nc = prob["num_computed"]
-    out["num_computed"] = None if nc is None else h(nc, np.int64)[sel]
+    out["num_computed"] = None if nc is None else i64(nc)[sel]
     for k in ("init_slots", "final_slots"):
-        out[k] = None if prob[k] is None else h(prob[k], np.int64)[sel]
+        out[k] = None if prob[k] is None else i64(prob[k])[sel]
     bt = prob["block_table"]
-    out["block_table"] = None if bt is None else h(bt, np.int64)[sel]
-    if pool is not None:
+    out["block_table"] = None if bt is None else i64(bt)[sel]
+    pool = prob["state_pool"]
+    if pool is None:
+        out["state_pool"] = None
+    elif requests is None and heads is None:
+        out["state_pool"] = f64(pool)
+    else:
         used = set()
         for k in ("init_slots", "final_slots"):
             if out[k] is not None:
                 used.update(int(v) for v in out[k] if v >= 0)
         if out["block_table"] is not None:
             used.update(int(v) for v in out["block_table"].ravel() if v >= 0)
-        # Only the slots this selection touches are copied; the rest stay zero.
-        host_pool = np.zeros(tuple(pool.shape), dtype=np.float64) if requests is None else None
-        if requests is None:
-            host_pool = pool.detach().to("cpu").to(torch.float64).numpy()
-        else:
-            host_pool = _SparsePool(pool, used)
-        out["state_pool"] = host_pool
-    else:
-        out["state_pool"] = None
+        out["state_pool"] = _SparsePool(pool, used, hidx)
     return out
 
 
 class _SparsePool:
     """Host view of the few pool slots a sampled check touches (avoids copying 17 GB)."""
 
-    def __init__(self, pool, slots):
-        self.shape = tuple(pool.shape)
-        self.slots = {s: pool[s].detach().to("cpu").to(torch.float64).numpy() for s in slots}
+    def __init__(self, pool, slots, hidx):
+        self.shape = (pool.shape[0], len(hidx)) + tuple(pool.shape[2:])
+        self.slots = {s: pool[s].detach().to("cpu").index_select(0, hidx).to(torch.float64).numpy()
+                      for s in slots}
 
     def __getitem__(self, s):
         return self.slots[int(s)]
