@@ -124,7 +124,7 @@ def test_packed_equals_separate_runs():
         sub = dict(prob)
         a, b = cu[i], cu[i + 1]
         for k in ("x", "dt", "B", "C", "z"):
-            sub[k] = prob[k][a:b].contiguous()
+            sub[k] = prob[k][a:b].clone()
         sub["cu_seqlens"] = torch.tensor([0, L], dtype=torch.int32, device="cuda")
         if L == 0:
             continue
@@ -146,13 +146,13 @@ def test_split_state_resume(k):
     whole = m.run(prob)
     pre = dict(prob)
     for key in ("x", "dt", "B", "C", "z"):
-        pre[key] = prob[key][:k].contiguous()
+        pre[key] = prob[key][:k].clone()
     pre["cu_seqlens"] = torch.tensor([0, k], dtype=torch.int32, device="cuda")
     first = m.run(pre)
     torch.cuda.synchronize()
     post = dict(prob)
     for key in ("x", "dt", "B", "C", "z"):
-        post[key] = prob[key][k:].contiguous()
+        post[key] = prob[key][k:].clone()
     post["cu_seqlens"] = torch.tensor([0, L - k], dtype=torch.int32, device="cuda")
     post["num_computed"] = torch.tensor([k], dtype=torch.int32, device="cuda")
     post["state_pool"] = first.final_states.clone()
