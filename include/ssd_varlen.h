@@ -83,7 +83,8 @@ enum ssd_status {
 #define SSD_DEVERR_FINAL_SLOT 0x8    /* final slot >= num_slots (write skipped) */
 #define SSD_DEVERR_BLOCK_SLOT 0x10   /* block-table slot >= num_slots (write skipped) */
 #define SSD_DEVERR_BLOCK_TABLE 0x20  /* a boundary needs a column >= block_table_width */
-#define SSD_DEVERR_TIMEOUT 0x40      /* a bounded wait between CTAs gave up */
+#define SSD_DEVERR_TIMEOUT 0x40      /* a bounded wait inside a kernel gave up (work skipped) */
+#define SSD_DEVERR_INTERNAL 0x80     /* a kernel could not start (shared-memory alignment) */
 
 /* Problem sizes.  Filled by the caller, copied into the plan. */
 typedef struct ssd_dims {

@@ -27,7 +27,7 @@ DTYPE_F32 = 1
 
 DEVERR = {
     "CU_SEQLENS": 0x1, "NUM_COMPUTED": 0x2, "INIT_SLOT": 0x4, "FINAL_SLOT": 0x8,
-    "BLOCK_SLOT": 0x10, "BLOCK_TABLE": 0x20, "TIMEOUT": 0x40,
+    "BLOCK_SLOT": 0x10, "BLOCK_TABLE": 0x20, "TIMEOUT": 0x40, "INTERNAL": 0x80,
 }
 STATUS = {
     0: "OK", -1: "NULL", -2: "DIMS", -3: "CHUNK_SIZE", -4: "GROUPS", -5: "BLOCK_SIZE",

@@ -175,7 +175,8 @@ int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_out
     p.chunk_states = out->chunk_states;
     p.block_table = out->block_table;
     if (d->T == 0 && !out->final_states && !out->final_slots) return SSD_OK;
-    cudaError_t e = launch_recurrent(p, d->dtype, stream);
+    cudaError_t e = chunk_tc_supported(p, d->dtype) ? launch_chunk_tc(p, plan->max_segs, stream)
+                                                    : launch_recurrent(p, d->dtype, stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

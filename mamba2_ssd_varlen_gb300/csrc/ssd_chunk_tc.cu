@@ -1,0 +1,737 @@
+// ssd_chunk_tc.cu -- the fused chunked SSD scan on Blackwell tensor cores (bf16).
+//
+// One CTA walks one (segment, head) work item piece by piece with the running
+// state kept in tensor memory (TMEM) for the whole segment, so chunk states
+// never travel through HBM.  A piece is a tile of at most 128 tokens: pieces
+// are cut at absolute multiples of the tile size Qi and also end where a
+// segment or a request ends.  Per piece the kernel evaluates the SSD chunk
+// decomposition of h_t = exp(dt'_t A) h_{t-1} + dt'_t x_t (outer) B_t:
+//   cs_t      = inclusive sum of dt'_s A over the piece, from its first token
+//   CB        = C B^T                                  (bmm_chunk, tcgen05)
+//   M[t,s]    = CB[t,s] exp(cs_t - cs_s) dt'_s, s <= t (the causal mask L o CB)
+//   y_intra   = M x                                    (tcgen05, M read from TMEM)
+//   y_inter   = exp(cs_t) C h_prev^T                   (tcgen05)
+//   y         = (y_intra + y_inter + D x) * silu(z)
+//   h_new^T   = exp(cs_last) h_prev^T + B^T (w x),  w_t = exp(cs_last - cs_t) dt'_t
+// cs is measured from the piece's first valid token, so an initial state (or
+// the state carried in from the previous piece) decays from exactly that
+// token: the initial-state decay fix of the "[Bugfix] Mamba2 SSD varlen bug fix
+// initstates decay" page.  Exported chunk states, block checkpoints and final
+// states are read out of TMEM at the piece boundaries where they fall.
+//
+// Precision: rounding an operand to bf16 loses 8 bits, which breaks the 5e-3
+// tolerance on y.  The three operands that are not exact bf16 inputs -- M,
+// the carried state h and the weighted inputs w x -- are each split into
+// bf16 hi + lo parts and their products issued twice into the fp32
+// accumulator.  CB, x, B and C are exact bf16 and go in once.
+//
+// Roles (192 threads): warp 0 issues the TMA loads, warp 1 issues the MMAs
+// (one lane) and owns the TMEM allocation, warps 2-5 are the math warps:
+// thread r of the math group owns TMEM lane r = tile row r.  Every wait is a
+// bounded mbarrier wait; on a timeout the CTA records SSD_DEVERR_TIMEOUT,
+// drains what it issued and exits.
+//
+// A second mode (STATE_ONLY) computes, for each segment that is not the last
+// of its request, the segment's end state from a zero state and its total
+// decay; seg_pass_kernel chains them so that all segments of a long request
+// run in parallel.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "sm100.cuh"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+using namespace sm100;
+
+constexpr int kThreads = 192;
+constexpr int kRows = 128;                   // tile rows (tokens per piece, at most)
+constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
+
+template <int P>
+struct __align__(1024) TcSmem {
+    static constexpr int kXBytes = kRows * P * 2;
+    uint8_t x[kXBytes];          // x tile: P/64 sub-tiles of 128 rows x 128 B
+    uint8_t b[kRows * 128 * 2];  // B tile: 2 sub-tiles (n 0-63, 64-127)
+    uint8_t c[kRows * 128 * 2];  // C tile
+    uint8_t xd_hi[kXBytes];      // w x, hi and lo parts (MN-major B operand)
+    uint8_t xd_lo[kXBytes];
+    uint8_t h_hi[128 * P * 2];   // h^T (rows n, P columns), hi and lo parts
+    uint8_t h_lo[128 * P * 2];
+    float cs[2][kRows];          // per-piece cumulative decay, double-buffered by piece parity
+    float dtp[2][kRows];         // per-piece dt'
+    uint64_t full, empty, cb_full, m_full, xd_full, h_full, y_full, s_full, y_empty, cs_ready;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct TcMaps {
+    CUtensorMap x, b, c;
+};
+
+struct Item {
+    int seg, head, req;
+    int tok, len;
+    int64_t abs0;            // absolute position of the segment's first token
+    int64_t req_s, req_end;  // request's num_computed and absolute end
+    bool first_seg, last_seg;
+};
+
+__device__ __forceinline__ bool load_item(const FwdParams &p, int w, bool state_only, Item &it) {
+    const int nseg = p.hdr[kHdrSegs];
+    it.seg = w / p.H;
+    it.head = w % p.H;
+    if (it.seg >= nseg) return false;
+    const Seg sg = p.segs[it.seg];
+    it.req = sg.req;
+    it.tok = sg.tok;
+    it.len = sg.len;
+    it.abs0 = sg.abs_start;
+    it.first_seg = it.seg == p.req_first_seg[it.req];
+    it.last_seg = it.seg == p.req_first_seg[it.req + 1] - 1;
+    it.req_s = p.num_computed ? (int64_t)p.num_computed[it.req] : 0;
+    it.req_end = it.req_s + (int64_t)p.cu_seqlens[it.req + 1] - p.cu_seqlens[it.req];
+    if (state_only && it.last_seg) return false;  // the last segment's end state is never chained
+    return true;
+}
+
+// Pieces of a segment: tiles of at most Qi tokens cut at absolute multiples of Qi.
+struct Pieces {
+    int64_t abs, end;
+    int tok, Qi;
+    __device__ bool next(int &t0, int &len, int64_t &abs_end) {
+        if (abs >= end) return false;
+        const int64_t e = min(end, (abs / Qi + 1) * (int64_t)Qi);
+        t0 = tok;
+        len = (int)(e - abs);
+        abs_end = e;
+        tok += len;
+        abs = e;
+        return true;
+    }
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *hdr) {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, kWaitNs)) return true;
+    *abort_flag = 1;
+    atomicOr(hdr + kHdrErr, SSD_DEVERR_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// v ~= hi + lo with hi = bf16(v) and lo = bf16(v - hi): 16 significant bits.
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16x2(a, b);
+    lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+}
+
+// Row n of the state (P values) -> bf16 hi/lo copies of h^T row n (MN-major tile).
+template <int P>
+__device__ __forceinline__ void write_h_copy(TcSmem<P> &s, int n, int pcol0, const uint32_t (&v)[32]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            split2(__uint_as_float(v[c8 * 8 + 2 * e]), __uint_as_float(v[c8 * 8 + 2 * e + 1]), hi[e], lo[e]);
+        const int pcol = pcol0 + c8 * 8;
+        const uint32_t off = (pcol >> 6) * 16384 + sw128_off(n, (pcol & 63) >> 3);
+        *reinterpret_cast<uint4 *>(s.h_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(s.h_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+template <int P, bool STATE_ONLY>
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int Qi) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // The tiles need 1024-byte alignment (swizzle atoms); the dynamic shared
+    // window starts there on this architecture.  Refuse to run otherwise.
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
+        return;
+    }
+    TcSmem<P> &s = *reinterpret_cast<TcSmem<P> *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = &s.abort_flag;
+    constexpr uint32_t kColCB = 0, kColYi = 128, kColYe = 128 + P, kColH = 128 + 2 * P;
+    constexpr int kPB = P / 64;  // 64-column blocks of P
+    const size_t slot_elems = (size_t)p.H * P * 128;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&s.full, 1);
+        mbar_init(&s.empty, 5);
+        mbar_init(&s.cb_full, 1);
+        mbar_init(&s.m_full, 4);
+        mbar_init(&s.xd_full, 4);
+        mbar_init(&s.h_full, 4);
+        mbar_init(&s.y_full, 1);
+        mbar_init(&s.s_full, 1);
+        mbar_init(&s.y_empty, 4);
+        mbar_init(&s.cs_ready, 4);
+        s.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s.tmem_base;
+    const uint32_t n_work = (uint32_t)p.hdr[kHdrSegs] * (uint32_t)p.H;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&maps.x);
+            prefetch_tmap(&maps.b);
+            if (!STATE_ONLY) prefetch_tmap(&maps.c);
+            uint32_t pc = 0;
+            bool ok = true;
+            const uint32_t bytes = kRows * (P + 128 + (STATE_ONLY ? 0 : 128)) * 2;
+            for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+                Item it;
+                if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+                const int g = it.head / (p.H / p.G);
+                Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
+                int t0, len;
+                int64_t ae;
+                while (pcs.next(t0, len, ae)) {
+                    if (pc > 0 && !wait_bar(&s.empty, (pc - 1) & 1, abort_flag, p.hdr)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.full, bytes);
+                    for (int q = 0; q < kPB; ++q) tma_load_3d(s.x + q * 16384, &maps.x, &s.full, q * 64, it.head, t0);
+                    tma_load_3d(s.b, &maps.b, &s.full, 0, g, t0);
+                    tma_load_3d(s.b + 16384, &maps.b, &s.full, 64, g, t0);
+                    if (!STATE_ONLY) {
+                        tma_load_3d(s.c, &maps.c, &s.full, 0, g, t0);
+                        tma_load_3d(s.c + 16384, &maps.c, &s.full, 64, g, t0);
+                    }
+                    ++pc;
+                }
+            }
+            // Never leave a copy in flight: wait for the last issued load.
+            if (pc > 0) mbar_wait(&s.full, (pc - 1) & 1, kWaitNs);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sx = smem_u32(s.x), sb = smem_u32(s.b), sc = smem_u32(s.c);
+            const uint32_t sxh = smem_u32(s.xd_hi), sxl = smem_u32(s.xd_lo);
+            const uint32_t shh = smem_u32(s.h_hi), shl = smem_u32(s.h_lo);
+            constexpr uint32_t i_cb = idesc_bf16_f32(128, 128, false, false);  // C (K-major) x B^T (K-major)
+            constexpr uint32_t i_y = idesc_bf16_f32(128, P, false, true);      // K-major A x MN-major B
+            constexpr uint32_t i_s = idesc_bf16_f32(128, P, true, true);       // B^T (MN-major) x wx (MN-major)
+            uint32_t pc = 0;
+            bool ok = true;
+            for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+                Item it;
+                if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+                Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
+                int t0, len;
+                int64_t ae;
+                while (pcs.next(t0, len, ae)) {
+                    const uint32_t ph = pc & 1, pph = (pc - 1) & 1;
+                    if (!wait_bar(&s.full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                    tc_fence_after();
+                    if (!STATE_ONLY) {
+                        // CB = C B^T.  The CB/M columns are free once the previous
+                        // piece's intra MMA (committed to y_full) has completed.
+                        if (pc > 0 && !wait_bar(&s.y_full, pph, abort_flag, p.hdr)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(tbase + kColCB, sdesc_sw128(sc + ko, 16, 1024), sdesc_sw128(sb + ko, 16, 1024),
+                                   i_cb, kk > 0);
+                        }
+                        mma_commit(&s.cb_full);
+                        // y_inter = C h^T (h in hi + lo): needs the state copy and a drained Ye.
+                        if (!wait_bar(&s.h_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                        if (pc > 0 && !wait_bar(&s.y_empty, pph, abort_flag, p.hdr)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {
+                            const uint32_t hb = part ? shl : shh;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                mma_ss(tbase + kColYe, sdesc_sw128(sc + ko, 16, 1024),
+                                       sdesc_sw128(hb + kk * 2048, 16384, 1024), i_y, (part | kk) != 0);
+                            }
+                        }
+                    }
+                    // h^T += B^T (w x); the math warps have already scaled h^T by the piece decay.
+                    if (!wait_bar(&s.xd_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t xb = part ? sxl : sxh;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ss(tbase + kColH, sdesc_sw128(sb + kk * 2048, 16384, 1024),
+                                   sdesc_sw128(xb + kk * 2048, 16384, 1024), i_s, 1);
+                    }
+                    mma_commit(&s.s_full);
+                    if (!STATE_ONLY) {
+                        // y_intra = M x with M (hi, lo) in TMEM over the CB columns:
+                        // 32-column block j holds s in [32j, 32j+32): hi in its first
+                        // 16 columns, lo in the next 16 (two bf16 per column).
+                        if (!wait_bar(&s.m_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t acol = kColCB + (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                                mma_ts(tbase + kColYi, tbase + acol, sdesc_sw128(sx + kk * 2048, 16384, 1024), i_y,
+                                       (part | kk) != 0);
+                            }
+                        }
+                        mma_commit(&s.y_full);
+                    }
+                    mma_commit(&s.empty);
+                    ++pc;
+                }
+            }
+            // Drain: every issued MMA completes before TMEM is freed.
+            if (pc > 0) {
+                mbar_wait(&s.s_full, (pc - 1) & 1, kWaitNs);
+                if (!STATE_ONLY) mbar_wait(&s.y_full, (pc - 1) & 1, kWaitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ math warps
+        const int q = warp & 3;       // TMEM lane quadrant of this warp
+        const int r = q * 32 + lane;  // tile row / TMEM lane owned by this thread
+        const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
+        const __nv_bfloat16 *__restrict__ dtv = static_cast<const __nv_bfloat16 *>(p.dt);
+        const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
+        __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
+        uint32_t pc = 0;
+        bool ok = true;
+        for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+            Item it;
+            if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+            const int hh = it.head;
+            const float dtb = p.dt_bias[hh], Ah = p.A[hh];
+            const float Dh = (!STATE_ONLY && p.D) ? p.D[hh] : 0.f;
+
+            // ---- entering state: initial slot (first segment) or the chained state
+            const float *src = nullptr;
+            if (!STATE_ONLY) {
+                if (it.first_seg) {
+                    if (p.init_slots) {
+                        const int slot = p.init_slots[it.req];
+                        if (slot >= p.num_slots) {
+                            if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
+                        } else if (slot >= 0) {
+                            src = p.pool + (size_t)slot * slot_elems;
+                        }
+                    }
+                } else {
+                    src = p.seg_state + (size_t)(it.seg - 1) * slot_elems;
+                }
+            }
+            if (!STATE_ONLY && it.len == 0) {
+                // Empty request: its final state is its initial state.
+                float *fd = p.final_states ? p.final_states + (size_t)it.req * slot_elems : nullptr;
+                float *fs = nullptr;
+                if (p.final_slots) {
+                    const int fslot = p.final_slots[it.req];
+                    if (fslot >= p.num_slots) {
+                        if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
+                    } else if (fslot >= 0) {
+                        fs = p.pool + (size_t)fslot * slot_elems;
+                    }
+                }
+                for (int pp = 0; pp < P; ++pp) {
+                    const size_t e = ((size_t)hh * P + pp) * 128 + r;
+                    const float v = src ? src[e] : 0.f;
+                    if (fd) fd[e] = v;
+                    if (fs) fs[e] = v;
+                }
+                continue;
+            }
+            // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
+#pragma unroll 1
+            for (int j = 0; j < P / 32; ++j) {
+                uint32_t v[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    v[k] = src ? __float_as_uint(src[((size_t)hh * P + j * 32 + k) * 128 + r]) : 0u;
+                tmem_st32(tl + kColH + j * 32, v);
+                if (!STATE_ONLY) write_h_copy<P>(s, r, j * 32, v);
+            }
+            tmem_st_wait();
+            if (!STATE_ONLY) {
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.h_full);
+            }
+
+            float decay_sum = 0.f;  // sum of dt' A over the segment (STATE_ONLY)
+            Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
+            int t0, len;
+            int64_t ae;
+            bool have_piece = pcs.next(t0, len, ae);
+            while (have_piece) {
+                const uint32_t ph = pc & 1;
+                int nt0 = 0, nlen = 0;
+                int64_t nae = 0;
+                const bool has_next = pcs.next(nt0, nlen, nae);
+                // ---- A: dt' and the in-piece inclusive cumulative decay.  Every
+                // math warp scans all 128 rows itself (lane l: rows 4l..4l+3), so
+                // no cross-warp prefix is needed.
+                float dl[4], cl[4];
+                float run = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = lane * 4 + k;
+                    dl[k] = 0.f;
+                    if (row < len) dl[k] = softplus_f32(__bfloat162float(dtv[(size_t)(t0 + row) * p.H + hh]) + dtb);
+                    run += dl[k] * Ah;
+                    cl[k] = run;
+                }
+                float incl = run;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const float excl = incl - run;
+                const float cs_last = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cl[k] += excl;
+                // this warp publishes its own 32 rows (lanes 8q..8q+7 hold them)
+                if ((lane >> 3) == q) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        s.cs[ph][lane * 4 + k] = cl[k];
+                        s.dtp[ph][lane * 4 + k] = dl[k];
+                    }
+                }
+                // own row r = 32q + lane lives in lane 8q + lane/4, slot lane%4
+                const int src_lane = 8 * q + (lane >> 2);
+                float cs = 0.f, d = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float cv = __shfl_sync(0xffffffffu, cl[k], src_lane);
+                    const float dv = __shfl_sync(0xffffffffu, dl[k], src_lane);
+                    if ((lane & 3) == k) {
+                        cs = cv;
+                        d = dv;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.cs_ready);
+                decay_sum += cs_last;
+                const float decay = expf(cs_last);
+                if (!wait_bar(&s.full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                // ---- B: scale h^T by the piece decay; w x (hi, lo) tiles
+#pragma unroll 1
+                for (int j = 0; j < P / 32; ++j) {
+                    uint32_t v[32];
+                    tmem_ld32(tl + kColH + j * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * decay);
+                    tmem_st32(tl + kColH + j * 32, v);
+                }
+                {
+                    const float wr = (r < len) ? expf(cs_last - cs) * d : 0.f;
+#pragma unroll
+                    for (int cb = 0; cb < P / 8; ++cb) {
+                        const uint32_t off = (cb >> 3) * 16384 + sw128_off(r, cb & 7);
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(s.x + off);
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split2(bf16lo_to_f32(xw[e]) * wr, bf16hi_to_f32(xw[e]) * wr, hi[e], lo[e]);
+                        *reinterpret_cast<uint4 *>(s.xd_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(s.xd_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                tmem_st_wait();
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.xd_full);
+                if (STATE_ONLY) {
+                    if (lane == 0) mbar_arrive(&s.empty);
+                } else {
+                    // ---- C: causal decayed mask M = CB o L o dt' -> TMEM (hi, lo), in place
+                    if (!wait_bar(&s.cs_ready, ph, abort_flag, p.hdr)) { ok = false; break; }
+                    if (!wait_bar(&s.cb_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                    tc_fence_after();
+                    const float *csv = s.cs[ph];
+                    const float *dv = s.dtp[ph];
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t hi[16], lo[16];
+                        if (j > q) {  // every column of the block lies above this warp's rows
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
+                        } else {
+                            uint32_t v[32];
+                            tmem_ld32(tl + kColCB + j * 32, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const int s0 = j * 32 + 2 * k;
+                                float m0 = 0.f, m1 = 0.f;
+                                if (s0 <= r && s0 < len) m0 = __uint_as_float(v[2 * k]) * expf(cs - csv[s0]) * dv[s0];
+                                if (s0 + 1 <= r && s0 + 1 < len)
+                                    m1 = __uint_as_float(v[2 * k + 1]) * expf(cs - csv[s0 + 1]) * dv[s0 + 1];
+                                split2(m0, m1, hi[k], lo[k]);
+                            }
+                        }
+                        tmem_st16(tl + kColCB + j * 32, hi);
+                        tmem_st16(tl + kColCB + j * 32 + 16, lo);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.m_full);
+                    // ---- D: epilogue y = (y_intra + exp(cs) y_inter + D x) * silu(z)
+                    if (!wait_bar(&s.y_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                    tc_fence_after();
+                    const float ecs = expf(cs);
+                    const size_t yrow = ((size_t)(t0 + r) * p.H + hh) * P;
+#pragma unroll 1
+                    for (int j = 0; j < P / 32; ++j) {
+                        uint32_t vi[32], ve[32];
+                        tmem_ld32(tl + kColYi + j * 32, vi);
+                        tmem_ld32(tl + kColYe + j * 32, ve);
+                        tmem_ld_wait();
+                        if (r < len) {
+#pragma unroll
+                            for (int c8 = 0; c8 < 4; ++c8) {
+                                const int pcol = j * 32 + c8 * 8;
+                                const uint4 xv = *reinterpret_cast<const uint4 *>(
+                                    s.x + (pcol >> 6) * 16384 + sw128_off(r, (pcol & 63) >> 3));
+                                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                                uint4 zq = make_uint4(0, 0, 0, 0);
+                                if (zv) zq = *reinterpret_cast<const uint4 *>(zv + yrow + pcol);
+                                const uint32_t zw[4] = {zq.x, zq.y, zq.z, zq.w};
+                                uint32_t out[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int k0 = c8 * 8 + 2 * e;
+                                    float y0 = __uint_as_float(vi[k0]) + ecs * __uint_as_float(ve[k0]) +
+                                               Dh * bf16lo_to_f32(xw[e]);
+                                    float y1 = __uint_as_float(vi[k0 + 1]) + ecs * __uint_as_float(ve[k0 + 1]) +
+                                               Dh * bf16hi_to_f32(xw[e]);
+                                    if (zv) {
+                                        y0 *= silu_f32(bf16lo_to_f32(zw[e]));
+                                        y1 *= silu_f32(bf16hi_to_f32(zw[e]));
+                                    }
+                                    out[e] = pack_bf16x2(y0, y1);
+                                }
+                                *reinterpret_cast<uint4 *>(yv + yrow + pcol) =
+                                    make_uint4(out[0], out[1], out[2], out[3]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&s.y_empty);
+                        mbar_arrive(&s.empty);
+                    }
+                }
+                // ---- E: the state after the piece
+                if (!wait_bar(&s.s_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                tc_fence_after();
+                const bool seg_end = !has_next;
+                const bool req_end = (ae == it.req_end);
+                float *dsts[4];
+                int nd = 0;
+                if (!STATE_ONLY) {
+                    if (p.chunk_states && (ae % p.Q == 0 || req_end)) {
+                        const int64_t row = (int64_t)p.req_first_chunk[it.req] + (ae - 1) / p.Q - it.req_s / p.Q;
+                        dsts[nd++] = p.chunk_states + (size_t)row * slot_elems;
+                    }
+                    if (p.block_table && p.block_size > 0 && ae % p.block_size == 0) {
+                        const int64_t col = ae / p.block_size - 1;
+                        if (col >= p.bt_width) {
+                            if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_TABLE);
+                        } else {
+                            const int bslot = p.block_table[(size_t)it.req * p.bt_width + col];
+                            if (bslot >= p.num_slots) {
+                                if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_SLOT);
+                            } else if (bslot >= 0) {
+                                dsts[nd++] = p.pool + (size_t)bslot * slot_elems;
+                            }
+                        }
+                    }
+                    if (req_end) {
+                        if (p.final_states) dsts[nd++] = p.final_states + (size_t)it.req * slot_elems;
+                        if (p.final_slots) {
+                            const int fslot = p.final_slots[it.req];
+                            if (fslot >= p.num_slots) {
+                                if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
+                            } else if (fslot >= 0) {
+                                dsts[nd++] = p.pool + (size_t)fslot * slot_elems;
+                            }
+                        }
+                    }
+                } else if (seg_end) {
+                    dsts[nd++] = p.seg_state + (size_t)it.seg * slot_elems;
+                    if (r == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = expf(decay_sum);
+                }
+                const bool need_copy = !STATE_ONLY && !seg_end;
+                if (need_copy || nd > 0) {
+#pragma unroll 1
+                    for (int j = 0; j < P / 32; ++j) {
+                        uint32_t v[32];
+                        tmem_ld32(tl + kColH + j * 32, v);
+                        tmem_ld_wait();
+                        for (int dd = 0; dd < nd; ++dd) {
+                            float *dst = dsts[dd] + ((size_t)hh * P + j * 32) * 128 + r;
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) dst[(size_t)k * 128] = __uint_as_float(v[k]);
+                        }
+                        if (need_copy) write_h_copy<P>(s, r, j * 32, v);
+                    }
+                    if (need_copy) {
+                        fence_async_smem();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&s.h_full);
+                    }
+                }
+                ++pc;
+                t0 = nt0;
+                len = nlen;
+                ae = nae;
+                have_piece = has_next;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+// Chains the segment end states of each request:
+//   h <- initial state;  for every segment k but the last:
+//   h <- decay_k h + S_k  and store it in slot k (= entering state of segment k+1).
+template <int P>
+__global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
+    const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
+    if (p.hdr[kHdrSegs] == 0 || i >= p.R) return;
+    const int first = p.req_first_seg[i], cnt = p.req_first_seg[i + 1] - first;
+    if (cnt <= 1) return;
+    const size_t pn = (size_t)P * 128, slot_elems = (size_t)p.H * pn;
+    const float *init = nullptr;
+    if (p.init_slots) {
+        const int slot = p.init_slots[i];
+        if (slot >= 0 && slot < p.num_slots) init = p.pool + (size_t)slot * slot_elems + hh * pn;
+    }
+    for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
+        float4 h = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < cnt - 1; ++k) {
+            const float dk = p.seg_decay[(size_t)(first + k) * p.H + hh];
+            float4 *sp = reinterpret_cast<float4 *>(p.seg_state + (size_t)(first + k) * slot_elems + hh * pn + e);
+            const float4 sv = *sp;
+            h = make_float4(fmaf(dk, h.x, sv.x), fmaf(dk, h.y, sv.y), fmaf(dk, h.z, sv.z), fmaf(dk, h.w, sv.w));
+            *sp = h;
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 3-D bf16 map over a row-major (d2, d1, d0) tensor; box = 64 x 1 x 128 with the 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *g, uint64_t d0, uint64_t d1, uint64_t d2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t dims[3] = {d0, d1, d2 > 0 ? d2 : 1};
+    const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)kRows};
+    const uint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(g), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int P>
+cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t stream) {
+    TcMaps maps;
+    if (!make_map(&maps.x, p.x, P, p.H, p.T) || !make_map(&maps.b, p.B, 128, p.G, p.T) ||
+        !make_map(&maps.c, p.C, 128, p.G, p.T))
+        return cudaErrorInvalidValue;
+    const int smem = (int)sizeof(TcSmem<P>);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_items));
+    ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    seg_pass_kernel<P><<<(unsigned)((int64_t)p.R * p.H), 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ssd_chunk_tc_kernel<P, false><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_tc_supported(const FwdParams &p, int dtype) {
+    return dtype == SSD_DTYPE_BF16 && (p.P == 64 || p.P == 128) && p.N == 128;
+}
+
+int chunk_tc_tile(const FwdParams &p) {
+    int qi = kRows;
+    if (p.chunk_states && p.Q < qi) qi = p.Q;
+    if (p.block_table && p.block_size > 0) {
+        const int low = p.block_size & -p.block_size;  // largest power of two dividing block_size
+        if (low < qi) qi = low;
+    }
+    return qi;
+}
+
+cudaError_t launch_chunk_tc(const FwdParams &p, int64_t max_segs, cudaStream_t stream) {
+    const int Qi = chunk_tc_tile(p);
+    const int64_t max_items = max_segs * p.H;
+    return p.P == 64 ? launch_p<64>(p, Qi, max_items, stream) : launch_p<128>(p, Qi, max_items, stream);
+}
+
+}  // namespace ssd

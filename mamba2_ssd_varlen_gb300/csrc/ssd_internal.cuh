@@ -84,4 +84,9 @@ cudaError_t launch_plan(const int32_t *cu, const int32_t *ncomp, int32_t R, int6
 
 cudaError_t launch_recurrent(const FwdParams &p, int dtype, cudaStream_t stream);
 
+// Tensor-core chunked path (bf16, P in {64, 128}, N = 128).
+bool chunk_tc_supported(const FwdParams &p, int dtype);
+int chunk_tc_tile(const FwdParams &p);
+cudaError_t launch_chunk_tc(const FwdParams &p, int64_t max_segs, cudaStream_t stream);
+
 }  // namespace ssd

@@ -87,6 +87,19 @@ def test_ragged_batch_every_output(Q):
     run_full(prob)
 
 
+@pytest.mark.parametrize("P", [64, 128])
+def test_long_requests_span_several_segments(P):
+    # Requests longer than one work segment (2048 tokens) are split into
+    # segments whose entering states are chained on the device; one starts
+    # mid-chunk (num_computed 1000) from an initial state.
+    spec = workloads.Spec("long", H=2, P=P, N=128, G=1, chunk_size=128, dtype="bf16",
+                          has_D=True, has_z=True, init="all", pool_slots=64, final_slots=True,
+                          export_chunks=True, block_size=1024)
+    prob = workloads.make_problem(spec, seed=31, device="cuda", lengths=[5000, 4096, 3],
+                                  num_computed=[1000, 0, 2047], canary=1.5)
+    run_full(prob)
+
+
 def test_initial_state_decay_in_first_chunk_768_tokens_q128():
     # The larger failing shape of the initial-state decay bugfix (768 tokens,
     # chunk_size 128), with an initial state and a resume offset inside a chunk.
