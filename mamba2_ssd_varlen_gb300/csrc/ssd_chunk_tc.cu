@@ -19,17 +19,26 @@
 // initstates decay" page.  Exported chunk states, block checkpoints and final
 // states are read out of TMEM at the piece boundaries where they fall.
 //
+// D x is folded into the diagonal of M, so y_intra already carries the skip.
+//
 // Precision: rounding an operand to bf16 loses 8 bits, which breaks the 5e-3
 // tolerance on y.  The three operands that are not exact bf16 inputs -- M,
 // the carried state h and the weighted inputs w x -- are each split into
 // bf16 hi + lo parts and their products issued twice into the fp32
 // accumulator.  CB, x, B and C are exact bf16 and go in once.
 //
-// Roles (192 threads): warp 0 issues the TMA loads, warp 1 issues the MMAs
-// (one lane) and owns the TMEM allocation, warps 2-5 are the math warps:
-// thread r of the math group owns TMEM lane r = tile row r.  Every wait is a
-// bounded mbarrier wait; on a timeout the CTA records SSD_DEVERR_TIMEOUT,
-// drains what it issued and exits.
+// Roles (320 threads, warp-specialised):
+//   warp 0  TMA producer: x (+ z) tiles into a double-buffered stage, B and C
+//           tiles into one stage released as soon as the state MMA has read them;
+//   warp 1  MMA issuer (one lane) and TMEM owner;
+//   G1      warps 2-5: decay scan, w x split tiles, causal mask (one warp per
+//           TMEM lane quadrant; thread r owns tile row r);
+//   G2      warps 6-9: state bookkeeping, epilogue (y staged in the finished x
+//           tile and stored with coalesced writes), chunk/block/final states.
+// G1 can run a piece ahead of G2, and the y accumulators are double-buffered in
+// TMEM (P = 64), so the mask of one piece overlaps the epilogue of the last.
+// Every wait is a bounded mbarrier wait; on a timeout the CTA records
+// SSD_DEVERR_TIMEOUT, drains what it issued and exits.
 //
 // A second mode (STATE_ONLY) computes, for each segment that is not the last
 // of its request, the segment's end state from a zero state and its total
@@ -38,6 +47,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstddef>
 
 #include "sm100.cuh"
 #include "ssd_internal.cuh"
@@ -46,29 +56,64 @@ namespace ssd {
 namespace {
 using namespace sm100;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                // producer, MMA, 4 G1 math warps, 4 G2 math warps
 constexpr int kRows = 128;                   // tile rows (tokens per piece, at most)
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Per-P layout choices.  P = 64 has room to double-buffer the x/z stage and the
+// y accumulators and to keep the state update S in its own TMEM columns;
+// P = 128 fills shared memory and TMEM with one of each and updates the state
+// in place.
+template <int P>
+struct TcCfg {
+    static constexpr int kNS = (P == 64) ? 2 : 1;     // x/z stages
+    static constexpr int kNY = (P == 64) ? 2 : 1;     // y_intra / y_inter accumulator pairs in TMEM
+    static constexpr bool kSepS = (P == 64);          // state update in its own columns
+    static constexpr bool kZTile = (P == 64);         // z staged by TMA
+    static constexpr int kXBytes = kRows * P * 2;
+    // TMEM columns: CB/M [0,128), then kNY pairs (y_intra, y_inter), then h^T, then S.
+    __host__ __device__ static constexpr uint32_t col_yi(int yb) { return 128 + yb * 2 * P; }
+    __host__ __device__ static constexpr uint32_t col_ye(int yb) { return 128 + yb * 2 * P + P; }
+    static constexpr uint32_t kColH = 128 + kNY * 2 * P;
+    static constexpr uint32_t kColS = kColH + P;      // only when kSepS
+    static_assert(kColH + P * (kSepS ? 2 : 1) <= 512, "TMEM columns");
+};
 
 template <int P>
 struct __align__(1024) TcSmem {
-    static constexpr int kXBytes = kRows * P * 2;
-    uint8_t x[kXBytes];          // x tile: P/64 sub-tiles of 128 rows x 128 B
-    uint8_t b[kRows * 128 * 2];  // B tile: 2 sub-tiles (n 0-63, 64-127)
-    uint8_t c[kRows * 128 * 2];  // C tile
-    uint8_t xd_hi[kXBytes];      // w x, hi and lo parts (MN-major B operand)
-    uint8_t xd_lo[kXBytes];
-    uint8_t h_hi[128 * P * 2];   // h^T (rows n, P columns), hi and lo parts
+    using Cfg = TcCfg<P>;
+    uint8_t x[Cfg::kNS * Cfg::kXBytes];  // x tiles; a finished stage also stages y for the store
+    uint8_t b[kRows * 128 * 2];          // B tile: 2 sub-tiles (n 0-63, 64-127)
+    uint8_t c[kRows * 128 * 2];          // C tile
+    uint8_t xd_hi[Cfg::kXBytes];         // w x, hi and lo parts (MN-major B operand)
+    uint8_t xd_lo[Cfg::kXBytes];
+    uint8_t h_hi[128 * P * 2];           // h^T (rows n, P columns), hi and lo parts
     uint8_t h_lo[128 * P * 2];
-    float cs[2][kRows];          // per-piece cumulative decay, double-buffered by piece parity
-    float dtp[2][kRows];         // per-piece dt'
-    uint64_t full, empty, cb_full, m_full, xd_full, h_full, y_full, s_full, y_empty, cs_ready;
+    uint8_t z[Cfg::kZTile ? Cfg::kNS * Cfg::kXBytes : 16];  // last: a stub must not shift the tiles
+    float cs2[2][kRows];                 // per-piece cumulative decay (log2 units), by piece parity
+    float dtp[2][kRows];                 // per-piece dt'
+    uint64_t full_x[2], empty_x[2], full_bc, empty_bc;
+    uint64_t cb_full, m_full, m_done;
+    uint64_t y_full[2], y_empty[2];
+    uint64_t xd_full, s_free, s_full, h_full;
+    uint64_t cs_ready[2];
     uint32_t tmem_base;
     int abort_flag;
 };
 
+// Every operand tile must start on a 1024-byte swizzle-atom boundary.
+#define SSD_TILE_ALIGNED(P_, m) static_assert(offsetof(TcSmem<P_>, m) % 1024 == 0, "tile " #m " misaligned")
+SSD_TILE_ALIGNED(64, b); SSD_TILE_ALIGNED(64, c); SSD_TILE_ALIGNED(64, xd_hi); SSD_TILE_ALIGNED(64, xd_lo);
+SSD_TILE_ALIGNED(64, h_hi); SSD_TILE_ALIGNED(64, h_lo); SSD_TILE_ALIGNED(64, z);
+SSD_TILE_ALIGNED(128, b); SSD_TILE_ALIGNED(128, c); SSD_TILE_ALIGNED(128, xd_hi); SSD_TILE_ALIGNED(128, xd_lo);
+SSD_TILE_ALIGNED(128, h_hi); SSD_TILE_ALIGNED(128, h_lo);
+static_assert(sizeof(TcSmem<64>) <= 232448, "P = 64 tiles exceed the 227 KB shared-memory limit");
+static_assert(sizeof(TcSmem<128>) <= 232448, "P = 128 tiles exceed the 227 KB shared-memory limit");
+#undef SSD_TILE_ALIGNED
+
 struct TcMaps {
-    CUtensorMap x, b, c;
+    CUtensorMap x, b, c, z;
 };
 
 struct Item {
@@ -123,13 +168,27 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 2^x on the special-function unit (flushes denormal results to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// silu(v) = v / (1 + e^-v)
+__device__ __forceinline__ float silu_fast(float v) { return v * fast_rcp(1.f + fast_exp2(-v * kLog2e)); }
+
 // v ~= hi + lo with hi = bf16(v) and lo = bf16(v - hi): 16 significant bits.
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
     hi = pack_bf16x2(a, b);
     lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
 }
 
-// Row n of the state (P values) -> bf16 hi/lo copies of h^T row n (MN-major tile).
+// 32 columns (p0 .. p0+31) of state row n -> bf16 hi/lo copies of h^T row n (MN-major tile).
 template <int P>
 __device__ __forceinline__ void write_h_copy(TcSmem<P> &s, int n, int pcol0, const uint32_t (&v)[32]) {
 #pragma unroll
@@ -145,9 +204,24 @@ __device__ __forceinline__ void write_h_copy(TcSmem<P> &s, int n, int pcol0, con
     }
 }
 
+// Barrier phases.  Every barrier completes once per piece of the CTA's running
+// piece count pc, once per stage use (x/z stages, y accumulator pairs:
+// pc / depth), or once per two pieces (cs_ready, indexed by pc & 1).  No waiter
+// can fall two phases behind: each barrier's next phase needs an arrival that
+// comes after every waiter of the current one.
+//
+// Per piece the MMA warp issues CB = C B^T, y_inter = C h^T, the state update
+// B^T (w x) -- after which B and C are released to the producer -- and last
+// y_intra = M x, which waits for the mask.  G2 reads the state out (which
+// frees the state columns and the h^T copy for the next piece) before it runs
+// the epilogue, so the state chain never waits for a mask or an epilogue.
+__device__ __forceinline__ uint32_t par(uint32_t use) { return use & 1u; }
+
 template <int P, bool STATE_ONLY>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int Qi) {
+    using Cfg = TcCfg<P>;
+    using Smem = TcSmem<P>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // The tiles need 1024-byte alignment (swizzle atoms); the dynamic shared
     // window starts there on this architecture.  Refuse to run otherwise.
@@ -155,24 +229,31 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
         return;
     }
-    TcSmem<P> &s = *reinterpret_cast<TcSmem<P> *>(smem_raw);
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &s.abort_flag;
-    constexpr uint32_t kColCB = 0, kColYi = 128, kColYe = 128 + P, kColH = 128 + 2 * P;
+    constexpr int kNS = Cfg::kNS, kNY = Cfg::kNY;
     constexpr int kPB = P / 64;  // 64-column blocks of P
     const size_t slot_elems = (size_t)p.H * P * 128;
+    const bool z_tile = Cfg::kZTile && !STATE_ONLY && p.z != nullptr;
 
     if (threadIdx.x == 0) {
-        mbar_init(&s.full, 1);
-        mbar_init(&s.empty, 5);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.full_x[i], 1);
+            mbar_init(&s.empty_x[i], 1 + 4);
+            mbar_init(&s.y_full[i], 1);
+            mbar_init(&s.y_empty[i], 4);
+            mbar_init(&s.cs_ready[i], 4);
+        }
+        mbar_init(&s.full_bc, 1);
+        mbar_init(&s.empty_bc, 1);
         mbar_init(&s.cb_full, 1);
         mbar_init(&s.m_full, 4);
+        mbar_init(&s.m_done, 1);
         mbar_init(&s.xd_full, 4);
-        mbar_init(&s.h_full, 4);
-        mbar_init(&s.y_full, 1);
+        mbar_init(&s.s_free, 4);
         mbar_init(&s.s_full, 1);
-        mbar_init(&s.y_empty, 4);
-        mbar_init(&s.cs_ready, 4);
+        mbar_init(&s.h_full, 4);
         s.abort_flag = 0;
         fence_mbar_init();
     }
@@ -192,9 +273,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             prefetch_tmap(&maps.x);
             prefetch_tmap(&maps.b);
             if (!STATE_ONLY) prefetch_tmap(&maps.c);
+            if (z_tile) prefetch_tmap(&maps.z);
             uint32_t pc = 0;
             bool ok = true;
-            const uint32_t bytes = kRows * (P + 128 + (STATE_ONLY ? 0 : 128)) * 2;
+            const uint32_t xbytes = Cfg::kXBytes * (z_tile ? 2 : 1);
+            const uint32_t bcbytes = kRows * 128 * 2 * (STATE_ONLY ? 1 : 2);
             for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
                 Item it;
                 if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
@@ -203,33 +286,45 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 int t0, len;
                 int64_t ae;
                 while (pcs.next(t0, len, ae)) {
-                    if (pc > 0 && !wait_bar(&s.empty, (pc - 1) & 1, abort_flag, p.hdr)) {
+                    const int st = pc % kNS;
+                    if (pc >= (uint32_t)kNS && !wait_bar(&s.empty_x[st], par(pc / kNS - 1), abort_flag, p.hdr)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&s.full, bytes);
-                    for (int q = 0; q < kPB; ++q) tma_load_3d(s.x + q * 16384, &maps.x, &s.full, q * 64, it.head, t0);
-                    tma_load_3d(s.b, &maps.b, &s.full, 0, g, t0);
-                    tma_load_3d(s.b + 16384, &maps.b, &s.full, 64, g, t0);
+                    mbar_arrive_expect_tx(&s.full_x[st], xbytes);
+                    uint8_t *xs = s.x + st * Cfg::kXBytes;
+                    for (int q = 0; q < kPB; ++q) tma_load_3d(xs + q * 16384, &maps.x, &s.full_x[st], q * 64, it.head, t0);
+                    if (z_tile) tma_load_3d(s.z + st * Cfg::kXBytes, &maps.z, &s.full_x[st], 0, it.head, t0);
+                    if (pc >= 1 && !wait_bar(&s.empty_bc, par(pc - 1), abort_flag, p.hdr)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.full_bc, bcbytes);
+                    tma_load_3d(s.b, &maps.b, &s.full_bc, 0, g, t0);
+                    tma_load_3d(s.b + 16384, &maps.b, &s.full_bc, 64, g, t0);
                     if (!STATE_ONLY) {
-                        tma_load_3d(s.c, &maps.c, &s.full, 0, g, t0);
-                        tma_load_3d(s.c + 16384, &maps.c, &s.full, 64, g, t0);
+                        tma_load_3d(s.c, &maps.c, &s.full_bc, 0, g, t0);
+                        tma_load_3d(s.c + 16384, &maps.c, &s.full_bc, 64, g, t0);
                     }
                     ++pc;
                 }
             }
-            // Never leave a copy in flight: wait for the last issued load.
-            if (pc > 0) mbar_wait(&s.full, (pc - 1) & 1, kWaitNs);
+            // Never leave a copy in flight: wait for the last issued loads.
+            if (pc > 0) {
+                mbar_wait(&s.full_bc, par(pc - 1), kWaitNs);
+                mbar_wait(&s.full_x[(pc - 1) % kNS], par((pc - 1) / kNS), kWaitNs);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t sx = smem_u32(s.x), sb = smem_u32(s.b), sc = smem_u32(s.c);
+            const uint32_t sb = smem_u32(s.b), sc = smem_u32(s.c);
             const uint32_t sxh = smem_u32(s.xd_hi), sxl = smem_u32(s.xd_lo);
             const uint32_t shh = smem_u32(s.h_hi), shl = smem_u32(s.h_lo);
             constexpr uint32_t i_cb = idesc_bf16_f32(128, 128, false, false);  // C (K-major) x B^T (K-major)
             constexpr uint32_t i_y = idesc_bf16_f32(128, P, false, true);      // K-major A x MN-major B
             constexpr uint32_t i_s = idesc_bf16_f32(128, P, true, true);       // B^T (MN-major) x wx (MN-major)
+            const uint32_t colS = Cfg::kSepS ? Cfg::kColS : Cfg::kColH;
             uint32_t pc = 0;
             bool ok = true;
             for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
@@ -239,24 +334,25 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 int t0, len;
                 int64_t ae;
                 while (pcs.next(t0, len, ae)) {
-                    const uint32_t ph = pc & 1, pph = (pc - 1) & 1;
-                    if (!wait_bar(&s.full, ph, abort_flag, p.hdr)) { ok = false; break; }
-                    tc_fence_after();
+                    const int st = pc % kNS, yb = pc % kNY;
+                    if (!wait_bar(&s.full_bc, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                     if (!STATE_ONLY) {
-                        // CB = C B^T.  The CB/M columns are free once the previous
-                        // piece's intra MMA (committed to y_full) has completed.
-                        if (pc > 0 && !wait_bar(&s.y_full, pph, abort_flag, p.hdr)) { ok = false; break; }
+                        // CB = C B^T, once the previous piece's y_intra has read M out of these columns.
+                        if (pc > 0 && !wait_bar(&s.m_done, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tbase + kColCB, sdesc_sw128(sc + ko, 16, 1024), sdesc_sw128(sb + ko, 16, 1024),
-                                   i_cb, kk > 0);
+                            mma_ss(tbase, sdesc_sw128(sc + ko, 16, 1024), sdesc_sw128(sb + ko, 16, 1024), i_cb, kk > 0);
                         }
                         mma_commit(&s.cb_full);
-                        // y_inter = C h^T (h in hi + lo): needs the state copy and a drained Ye.
-                        if (!wait_bar(&s.h_full, ph, abort_flag, p.hdr)) { ok = false; break; }
-                        if (pc > 0 && !wait_bar(&s.y_empty, pph, abort_flag, p.hdr)) { ok = false; break; }
+                        // y_inter = C h^T (h in hi + lo) into accumulator pair yb,
+                        // once the epilogue of the piece that last used the pair is done.
+                        if (!wait_bar(&s.h_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                        if (pc >= (uint32_t)kNY && !wait_bar(&s.y_empty[yb], par(pc / kNY - 1), abort_flag, p.hdr)) {
+                            ok = false;
+                            break;
+                        }
                         tc_fence_after();
 #pragma unroll
                         for (int part = 0; part < 2; ++part) {
@@ -264,67 +360,238 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                mma_ss(tbase + kColYe, sdesc_sw128(sc + ko, 16, 1024),
+                                mma_ss(tbase + Cfg::col_ye(yb), sdesc_sw128(sc + ko, 16, 1024),
                                        sdesc_sw128(hb + kk * 2048, 16384, 1024), i_y, (part | kk) != 0);
                             }
                         }
                     }
-                    // h^T += B^T (w x); the math warps have already scaled h^T by the piece decay.
-                    if (!wait_bar(&s.xd_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                    // state update: S = B^T (w x)  (or h^T += ... in place)
+                    if (!wait_bar(&s.xd_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                    if (!wait_bar(&s.s_free, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         const uint32_t xb = part ? sxl : sxh;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_ss(tbase + kColH, sdesc_sw128(sb + kk * 2048, 16384, 1024),
-                                   sdesc_sw128(xb + kk * 2048, 16384, 1024), i_s, 1);
+                            mma_ss(tbase + colS, sdesc_sw128(sb + kk * 2048, 16384, 1024),
+                                   sdesc_sw128(xb + kk * 2048, 16384, 1024), i_s,
+                                   Cfg::kSepS ? (uint32_t)((part | kk) != 0) : 1u);
                     }
                     mma_commit(&s.s_full);
-                    if (!STATE_ONLY) {
+                    mma_commit(&s.empty_bc);  // B and C have no further reader in this piece
+                    if (STATE_ONLY) {
+                        mma_commit(&s.empty_x[st]);
+                    } else {
                         // y_intra = M x with M (hi, lo) in TMEM over the CB columns:
                         // 32-column block j holds s in [32j, 32j+32): hi in its first
                         // 16 columns, lo in the next 16 (two bf16 per column).
-                        if (!wait_bar(&s.m_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                        if (!wait_bar(&s.m_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                        if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                         tc_fence_after();
+                        const uint32_t sx = smem_u32(s.x + st * Cfg::kXBytes);
 #pragma unroll
                         for (int part = 0; part < 2; ++part) {
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
-                                const uint32_t acol = kColCB + (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                                mma_ts(tbase + kColYi, tbase + acol, sdesc_sw128(sx + kk * 2048, 16384, 1024), i_y,
-                                       (part | kk) != 0);
+                                const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                                mma_ts(tbase + Cfg::col_yi(yb), tbase + acol, sdesc_sw128(sx + kk * 2048, 16384, 1024),
+                                       i_y, (part | kk) != 0);
                             }
                         }
-                        mma_commit(&s.y_full);
+                        mma_commit(&s.empty_x[st]);
+                        mma_commit(&s.m_done);
+                        mma_commit(&s.y_full[yb]);
                     }
-                    mma_commit(&s.empty);
                     ++pc;
                 }
             }
             // Drain: every issued MMA completes before TMEM is freed.
             if (pc > 0) {
-                mbar_wait(&s.s_full, (pc - 1) & 1, kWaitNs);
-                if (!STATE_ONLY) mbar_wait(&s.y_full, (pc - 1) & 1, kWaitNs);
+                mbar_wait(&s.s_full, par(pc - 1), kWaitNs);
+                if (!STATE_ONLY) mbar_wait(&s.y_full[(pc - 1) % kNY], par((pc - 1) / kNY), kWaitNs);
             }
         }
-    } else {
-        // ------------------------------------------------------------ math warps
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ G1: scan, w x, mask
         const int q = warp & 3;       // TMEM lane quadrant of this warp
         const int r = q * 32 + lane;  // tile row / TMEM lane owned by this thread
         const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
-        const __nv_bfloat16 *__restrict__ dtv = static_cast<const __nv_bfloat16 *>(p.dt);
+        const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
+        uint32_t pc = 0;
+        bool ok = true;
+        for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+            Item it;
+            if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+            if (it.len == 0) continue;
+            const int hh = it.head;
+            const float dtb = p.dt_bias[hh], Ah2 = p.A[hh] * kLog2e;
+            const float Dh = (!STATE_ONLY && p.D) ? p.D[hh] : 0.f;
+            Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
+            int t0, len;
+            int64_t ae;
+            bool have_piece = pcs.next(t0, len, ae);
+            // raw bf16 bits of dt for the coming piece, one piece ahead (lane l: rows 4l..4l+3)
+            uint32_t dt_raw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int row = lane * 4 + k;
+                dt_raw[k] = (have_piece && row < len) ? dt16[(size_t)(t0 + row) * p.H + hh] : 0u;
+            }
+            while (have_piece) {
+                const int st = pc % kNS;
+                int nt0 = 0, nlen = 0;
+                int64_t nae = 0;
+                const bool has_next = pcs.next(nt0, nlen, nae);
+                // ---- dt' and the in-piece inclusive cumulative decay (log2 units).
+                // Every G1 warp scans all 128 rows itself: no cross-warp prefix.
+                float dl[4], cl[4];
+                float run = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = lane * 4 + k;
+                    dl[k] = row < len ? softplus_f32(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
+                    run += dl[k] * Ah2;
+                    cl[k] = run;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = lane * 4 + k;
+                    dt_raw[k] = (has_next && row < nlen) ? dt16[(size_t)(nt0 + row) * p.H + hh] : 0u;
+                }
+                float incl = run;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const float excl = incl - run;
+                const float cs2_last = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cl[k] += excl;
+                if ((lane >> 3) == q) {  // publish this quadrant's 32 rows
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        s.cs2[pc & 1][lane * 4 + k] = cl[k];
+                        s.dtp[pc & 1][lane * 4 + k] = dl[k];
+                    }
+                }
+                // own row r = 32q + lane lives in lane 8q + lane/4, slot lane%4;
+                // the quadrant's reference row 32q - 1 in lane 8q - 1, slot 3.
+                const int src_lane = 8 * q + (lane >> 2);
+                float cs2 = 0.f, d = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float cv = __shfl_sync(0xffffffffu, cl[k], src_lane);
+                    const float dv = __shfl_sync(0xffffffffu, dl[k], src_lane);
+                    if ((lane & 3) == k) {
+                        cs2 = cv;
+                        d = dv;
+                    }
+                }
+                const float cs2_ref = __shfl_sync(0xffffffffu, cl[3], (8 * q + 31) & 31);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.cs_ready[pc & 1]);
+                // ---- w x (hi, lo) tiles; the previous state MMA must have read them
+                if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
+                if (pc > 0 && !wait_bar(&s.s_full, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
+                {
+                    const float wr = (r < len) ? fast_exp2(cs2_last - cs2) * d : 0.f;
+                    const uint8_t *xs = s.x + st * Cfg::kXBytes;
+#pragma unroll
+                    for (int cb = 0; cb < P / 8; ++cb) {
+                        const uint32_t off = (cb >> 3) * 16384 + sw128_off(r, cb & 7);
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + off);
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split2(bf16lo_to_f32(xw[e]) * wr, bf16hi_to_f32(xw[e]) * wr, hi[e], lo[e]);
+                        *reinterpret_cast<uint4 *>(s.xd_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(s.xd_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.xd_full);
+                if (!STATE_ONLY) {
+                    // ---- causal decayed mask M = CB o L o dt' (+ D on the diagonal),
+                    // written back over CB in TMEM as bf16 hi/lo.  Below the diagonal
+                    // (column block j < q) exp(cs_r - cs_s) = u_r v_s with both factors
+                    // <= 1 around the reference row 32q - 1; the diagonal block is
+                    // evaluated directly.
+                    if (!wait_bar(&s.cs_ready[pc & 1], par(pc >> 1), abort_flag, p.hdr)) { ok = false; break; }
+                    if (!wait_bar(&s.cb_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t colCB = 0;
+                    const float *cs2v = s.cs2[pc & 1];
+                    const float *dv = s.dtp[pc & 1];
+                    const float u_r = fast_exp2(cs2 - cs2_ref);
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t hi[16], lo[16];
+                        if (j > q) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
+                        } else {
+                            uint32_t v[32];
+                            tmem_ld32(tl + colCB + j * 32, v);
+                            if (j < q) {
+                                const int sl = j * 32 + lane;
+                                const float wl = fast_exp2(cs2_ref - cs2v[sl]) * dv[sl];
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) {
+                                    const float w0 = __shfl_sync(0xffffffffu, wl, 2 * k);
+                                    const float w1 = __shfl_sync(0xffffffffu, wl, 2 * k + 1);
+                                    split2(__uint_as_float(v[2 * k]) * w0 * u_r, __uint_as_float(v[2 * k + 1]) * w1 * u_r,
+                                           hi[k], lo[k]);
+                                }
+                            } else {
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) {
+                                    const int s0 = j * 32 + 2 * k;
+                                    float m0 = 0.f, m1 = 0.f;
+                                    if (s0 <= r) m0 = __uint_as_float(v[2 * k]) * fast_exp2(cs2 - cs2v[s0]) * dv[s0];
+                                    if (s0 + 1 <= r)
+                                        m1 = __uint_as_float(v[2 * k + 1]) * fast_exp2(cs2 - cs2v[s0 + 1]) * dv[s0 + 1];
+                                    if (s0 == r) m0 += Dh;
+                                    if (s0 + 1 == r) m1 += Dh;
+                                    split2(m0, m1, hi[k], lo[k]);
+                                }
+                            }
+                        }
+                        tmem_st16(tl + colCB + j * 32, hi);
+                        tmem_st16(tl + colCB + j * 32 + 16, lo);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.m_full);
+                }
+                ++pc;
+                t0 = nt0;
+                len = nlen;
+                ae = nae;
+                have_piece = has_next;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ G2: state, epilogue, outputs
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
         const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
+        const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
         uint32_t pc = 0;
         bool ok = true;
         for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
             Item it;
             if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
             const int hh = it.head;
-            const float dtb = p.dt_bias[hh], Ah = p.A[hh];
-            const float Dh = (!STATE_ONLY && p.D) ? p.D[hh] : 0.f;
-
+            const float dtb = p.dt_bias[hh], Ah2 = p.A[hh] * kLog2e;
             // ---- entering state: initial slot (first segment) or the chained state
             const float *src = nullptr;
             if (!STATE_ONLY) {
@@ -368,39 +635,47 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
                     v[k] = src ? __float_as_uint(src[((size_t)hh * P + j * 32 + k) * 128 + r]) : 0u;
-                tmem_st32(tl + kColH + j * 32, v);
+                tmem_st32(tl + Cfg::kColH + j * 32, v);
                 if (!STATE_ONLY) write_h_copy<P>(s, r, j * 32, v);
             }
             tmem_st_wait();
-            if (!STATE_ONLY) {
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.h_full);
+            if (!STATE_ONLY) fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (!STATE_ONLY) mbar_arrive(&s.h_full);
+                if (Cfg::kSepS) mbar_arrive(&s.s_free);  // S columns are free for the first piece
             }
 
-            float decay_sum = 0.f;  // sum of dt' A over the segment (STATE_ONLY)
+            float decay_sum2 = 0.f;  // sum of dt' A log2(e) over the segment (STATE_ONLY)
             Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
             int t0, len;
             int64_t ae;
             bool have_piece = pcs.next(t0, len, ae);
+            uint32_t dt_raw[4];  // raw bf16 dt of the coming piece (lane l: rows 4l..4l+3)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int row = lane * 4 + k;
+                dt_raw[k] = (have_piece && row < len) ? dt16[(size_t)(t0 + row) * p.H + hh] : 0u;
+            }
             while (have_piece) {
-                const uint32_t ph = pc & 1;
+                const int st = pc % kNS, yb = pc % kNY;
                 int nt0 = 0, nlen = 0;
                 int64_t nae = 0;
                 const bool has_next = pcs.next(nt0, nlen, nae);
-                // ---- A: dt' and the in-piece inclusive cumulative decay.  Every
-                // math warp scans all 128 rows itself (lane l: rows 4l..4l+3), so
-                // no cross-warp prefix is needed.
-                float dl[4], cl[4];
-                float run = 0.f;
+                // ---- this warp's own scan of the piece (same arithmetic as G1)
+                float run = 0.f, cl[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int row = lane * 4 + k;
-                    dl[k] = 0.f;
-                    if (row < len) dl[k] = softplus_f32(__bfloat162float(dtv[(size_t)(t0 + row) * p.H + hh]) + dtb);
-                    run += dl[k] * Ah;
+                    const float dk = row < len ? softplus_f32(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
+                    run += dk * Ah2;
                     cl[k] = run;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = lane * 4 + k;
+                    dt_raw[k] = (has_next && row < nlen) ? dt16[(size_t)(nt0 + row) * p.H + hh] : 0u;
                 }
                 float incl = run;
 #pragma unroll
@@ -408,150 +683,35 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     const float v = __shfl_up_sync(0xffffffffu, incl, o);
                     if (lane >= o) incl += v;
                 }
+                const float cs2_last = __shfl_sync(0xffffffffu, incl, 31);
                 const float excl = incl - run;
-                const float cs_last = __shfl_sync(0xffffffffu, incl, 31);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cl[k] += excl;
-                // this warp publishes its own 32 rows (lanes 8q..8q+7 hold them)
-                if ((lane >> 3) == q) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        s.cs[ph][lane * 4 + k] = cl[k];
-                        s.dtp[ph][lane * 4 + k] = dl[k];
-                    }
-                }
-                // own row r = 32q + lane lives in lane 8q + lane/4, slot lane%4
+                float cs2 = 0.f;
                 const int src_lane = 8 * q + (lane >> 2);
-                float cs = 0.f, d = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float cv = __shfl_sync(0xffffffffu, cl[k], src_lane);
-                    const float dv = __shfl_sync(0xffffffffu, dl[k], src_lane);
-                    if ((lane & 3) == k) {
-                        cs = cv;
-                        d = dv;
-                    }
+                    const float cv = __shfl_sync(0xffffffffu, cl[k] + excl, src_lane);
+                    if ((lane & 3) == k) cs2 = cv;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.cs_ready);
-                decay_sum += cs_last;
-                const float decay = expf(cs_last);
-                if (!wait_bar(&s.full, ph, abort_flag, p.hdr)) { ok = false; break; }
-                // ---- B: scale h^T by the piece decay; w x (hi, lo) tiles
+                const float decay = fast_exp2(cs2_last);
+                decay_sum2 += cs2_last;
+                if (!Cfg::kSepS) {
+                    // in-place state update: scale h^T before the state MMA adds B^T (w x)
 #pragma unroll 1
-                for (int j = 0; j < P / 32; ++j) {
-                    uint32_t v[32];
-                    tmem_ld32(tl + kColH + j * 32, v);
-                    tmem_ld_wait();
+                    for (int j = 0; j < P / 32; ++j) {
+                        uint32_t v[32];
+                        tmem_ld32(tl + Cfg::kColH + j * 32, v);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * decay);
-                    tmem_st32(tl + kColH + j * 32, v);
-                }
-                {
-                    const float wr = (r < len) ? expf(cs_last - cs) * d : 0.f;
-#pragma unroll
-                    for (int cb = 0; cb < P / 8; ++cb) {
-                        const uint32_t off = (cb >> 3) * 16384 + sw128_off(r, cb & 7);
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(s.x + off);
-                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split2(bf16lo_to_f32(xw[e]) * wr, bf16hi_to_f32(xw[e]) * wr, hi[e], lo[e]);
-                        *reinterpret_cast<uint4 *>(s.xd_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(s.xd_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    }
-                }
-                tmem_st_wait();
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.xd_full);
-                if (STATE_ONLY) {
-                    if (lane == 0) mbar_arrive(&s.empty);
-                } else {
-                    // ---- C: causal decayed mask M = CB o L o dt' -> TMEM (hi, lo), in place
-                    if (!wait_bar(&s.cs_ready, ph, abort_flag, p.hdr)) { ok = false; break; }
-                    if (!wait_bar(&s.cb_full, ph, abort_flag, p.hdr)) { ok = false; break; }
-                    tc_fence_after();
-                    const float *csv = s.cs[ph];
-                    const float *dv = s.dtp[ph];
-#pragma unroll 1
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t hi[16], lo[16];
-                        if (j > q) {  // every column of the block lies above this warp's rows
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
-                        } else {
-                            uint32_t v[32];
-                            tmem_ld32(tl + kColCB + j * 32, v);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                const int s0 = j * 32 + 2 * k;
-                                float m0 = 0.f, m1 = 0.f;
-                                if (s0 <= r && s0 < len) m0 = __uint_as_float(v[2 * k]) * expf(cs - csv[s0]) * dv[s0];
-                                if (s0 + 1 <= r && s0 + 1 < len)
-                                    m1 = __uint_as_float(v[2 * k + 1]) * expf(cs - csv[s0 + 1]) * dv[s0 + 1];
-                                split2(m0, m1, hi[k], lo[k]);
-                            }
-                        }
-                        tmem_st16(tl + kColCB + j * 32, hi);
-                        tmem_st16(tl + kColCB + j * 32 + 16, lo);
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * decay);
+                        tmem_st32(tl + Cfg::kColH + j * 32, v);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&s.m_full);
-                    // ---- D: epilogue y = (y_intra + exp(cs) y_inter + D x) * silu(z)
-                    if (!wait_bar(&s.y_full, ph, abort_flag, p.hdr)) { ok = false; break; }
-                    tc_fence_after();
-                    const float ecs = expf(cs);
-                    const size_t yrow = ((size_t)(t0 + r) * p.H + hh) * P;
-#pragma unroll 1
-                    for (int j = 0; j < P / 32; ++j) {
-                        uint32_t vi[32], ve[32];
-                        tmem_ld32(tl + kColYi + j * 32, vi);
-                        tmem_ld32(tl + kColYe + j * 32, ve);
-                        tmem_ld_wait();
-                        if (r < len) {
-#pragma unroll
-                            for (int c8 = 0; c8 < 4; ++c8) {
-                                const int pcol = j * 32 + c8 * 8;
-                                const uint4 xv = *reinterpret_cast<const uint4 *>(
-                                    s.x + (pcol >> 6) * 16384 + sw128_off(r, (pcol & 63) >> 3));
-                                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                                uint4 zq = make_uint4(0, 0, 0, 0);
-                                if (zv) zq = *reinterpret_cast<const uint4 *>(zv + yrow + pcol);
-                                const uint32_t zw[4] = {zq.x, zq.y, zq.z, zq.w};
-                                uint32_t out[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int k0 = c8 * 8 + 2 * e;
-                                    float y0 = __uint_as_float(vi[k0]) + ecs * __uint_as_float(ve[k0]) +
-                                               Dh * bf16lo_to_f32(xw[e]);
-                                    float y1 = __uint_as_float(vi[k0 + 1]) + ecs * __uint_as_float(ve[k0 + 1]) +
-                                               Dh * bf16hi_to_f32(xw[e]);
-                                    if (zv) {
-                                        y0 *= silu_f32(bf16lo_to_f32(zw[e]));
-                                        y1 *= silu_f32(bf16hi_to_f32(zw[e]));
-                                    }
-                                    out[e] = pack_bf16x2(y0, y1);
-                                }
-                                *reinterpret_cast<uint4 *>(yv + yrow + pcol) =
-                                    make_uint4(out[0], out[1], out[2], out[3]);
-                            }
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&s.y_empty);
-                        mbar_arrive(&s.empty);
-                    }
+                    if (lane == 0) mbar_arrive(&s.s_free);
                 }
-                // ---- E: the state after the piece
-                if (!wait_bar(&s.s_full, ph, abort_flag, p.hdr)) { ok = false; break; }
+                // ---- the state after the piece: read out first (it feeds the next piece)
+                if (!wait_bar(&s.s_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                 tc_fence_after();
                 const bool seg_end = !has_next;
                 const bool req_end = (ae == it.req_end);
@@ -588,15 +748,25 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     }
                 } else if (seg_end) {
                     dsts[nd++] = p.seg_state + (size_t)it.seg * slot_elems;
-                    if (r == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = expf(decay_sum);
+                    if (r == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = fast_exp2(decay_sum2);
                 }
                 const bool need_copy = !STATE_ONLY && !seg_end;
-                if (need_copy || nd > 0) {
+                if (Cfg::kSepS || need_copy || nd > 0) {
 #pragma unroll 1
                     for (int j = 0; j < P / 32; ++j) {
                         uint32_t v[32];
-                        tmem_ld32(tl + kColH + j * 32, v);
-                        tmem_ld_wait();
+                        tmem_ld32(tl + Cfg::kColH + j * 32, v);
+                        if (Cfg::kSepS) {
+                            uint32_t sv[32];
+                            tmem_ld32(tl + Cfg::kColS + j * 32, sv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                v[k] = __float_as_uint(fmaf(decay, __uint_as_float(v[k]), __uint_as_float(sv[k])));
+                            tmem_st32(tl + Cfg::kColH + j * 32, v);
+                        } else {
+                            tmem_ld_wait();
+                        }
                         for (int dd = 0; dd < nd; ++dd) {
                             float *dst = dsts[dd] + ((size_t)hh * P + j * 32) * 128 + r;
 #pragma unroll
@@ -604,12 +774,78 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         }
                         if (need_copy) write_h_copy<P>(s, r, j * 32, v);
                     }
-                    if (need_copy) {
-                        fence_async_smem();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&s.h_full);
+                    if (Cfg::kSepS) tmem_st_wait();
+                    if (need_copy) fence_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (need_copy) mbar_arrive(&s.h_full);
+                        if (Cfg::kSepS && has_next) mbar_arrive(&s.s_free);  // S read: next state MMA may go
                     }
+                }
+                if (STATE_ONLY) {
+                    if (lane == 0) mbar_arrive(&s.empty_x[st]);
+                } else {
+                    // ---- epilogue: y = (y_intra + exp(cs) y_inter) * silu(z), staged
+                    // in this stage's x tile, then stored with coalesced 16-byte writes.
+                    if (!wait_bar(&s.y_full[yb], par(pc / kNY), abort_flag, p.hdr)) { ok = false; break; }
+                    tc_fence_after();
+                    const float ecs = fast_exp2(cs2);
+                    uint8_t *ys = s.x + st * Cfg::kXBytes;
+                    const uint8_t *zs = s.z + (Cfg::kZTile ? st * Cfg::kXBytes : 0);
+                    const size_t yrow = ((size_t)(t0 + r) * p.H + hh) * P;
+#pragma unroll 1
+                    for (int j = 0; j < P / 32; ++j) {
+                        uint32_t vi[32], ve[32];
+                        tmem_ld32(tl + Cfg::col_yi(yb) + j * 32, vi);
+                        tmem_ld32(tl + Cfg::col_ye(yb) + j * 32, ve);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const int pcol = j * 32 + c8 * 8;
+                            const uint32_t off = (pcol >> 6) * 16384 + sw128_off(r, (pcol & 63) >> 3);
+                            uint32_t zw[4] = {0u, 0u, 0u, 0u};
+                            if (z_tile) {
+                                const uint4 zq = *reinterpret_cast<const uint4 *>(zs + off);
+                                zw[0] = zq.x; zw[1] = zq.y; zw[2] = zq.z; zw[3] = zq.w;
+                            } else if (zv && r < len) {
+                                const uint4 zq = *reinterpret_cast<const uint4 *>(zv + yrow + pcol);
+                                zw[0] = zq.x; zw[1] = zq.y; zw[2] = zq.z; zw[3] = zq.w;
+                            }
+                            uint32_t out[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int k0 = c8 * 8 + 2 * e;
+                                float y0 = fmaf(ecs, __uint_as_float(ve[k0]), __uint_as_float(vi[k0]));
+                                float y1 = fmaf(ecs, __uint_as_float(ve[k0 + 1]), __uint_as_float(vi[k0 + 1]));
+                                if (zv) {
+                                    y0 *= silu_fast(bf16lo_to_f32(zw[e]));
+                                    y1 *= silu_fast(bf16hi_to_f32(zw[e]));
+                                }
+                                out[e] = pack_bf16x2(y0, y1);
+                            }
+                            *reinterpret_cast<uint4 *>(ys + off) = make_uint4(out[0], out[1], out[2], out[3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.y_empty[yb]);
+                    // coalesced copy of this warp's 32 rows: lane l takes 16-byte chunk
+                    // (l mod P/8) of row 32q + l / (P/8) + k (32 / (P/8))
+                    constexpr int kCh = P / 8;            // 16-byte chunks per row
+                    constexpr int kRowsPerIt = 32 / kCh;  // rows per warp-wide step
+#pragma unroll 4
+                    for (int it2 = 0; it2 < 32 / kRowsPerIt; ++it2) {
+                        const int rr = q * 32 + it2 * kRowsPerIt + lane / kCh;
+                        const int ch = lane % kCh;
+                        if (rr < len) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(ys + (ch >> 3) * 16384 + sw128_off(rr, ch & 7));
+                            *reinterpret_cast<uint4 *>(yv + ((size_t)(t0 + rr) * p.H + hh) * P + ch * 8) = v;
+                        }
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.empty_x[st]);
                 }
                 ++pc;
                 t0 = nt0;
@@ -686,7 +922,7 @@ template <int P>
 cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t stream) {
     TcMaps maps;
     if (!make_map(&maps.x, p.x, P, p.H, p.T) || !make_map(&maps.b, p.B, 128, p.G, p.T) ||
-        !make_map(&maps.c, p.C, 128, p.G, p.T))
+        !make_map(&maps.c, p.C, 128, p.G, p.T) || !make_map(&maps.z, p.z ? p.z : p.x, P, p.H, p.T))
         return cudaErrorInvalidValue;
     const int smem = (int)sizeof(TcSmem<P>);
     static bool attr_done = false;
