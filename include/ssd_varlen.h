@@ -170,6 +170,38 @@ int ssd_varlen_status(const ssd_plan *plan, int *device_err);
 /* Static description of a status code or device error bit set. */
 const char *ssd_varlen_strerror(int code);
 
+/* ---- Forward without a caller-provided workspace -------------------------
+ * Not described by the pages (there is no counterpart there): it exists for
+ * callers that cannot allocate device memory for a workspace -- a plugin
+ * running inside a serving process or framework that owns the device memory
+ * pool, or a latency-critical loop where cudaMalloc (which can synchronise the
+ * device and can fail under memory pressure) is not allowed.
+ *
+ * Runs the same metadata builder and forward as ssd_varlen_plan +
+ * ssd_varlen_forward, with the workspace taken from a fixed array in device
+ * memory that the library owns: SSD_STATIC_SCRATCH_BYTES bytes, held on each
+ * GPU that loads the library until the process exits.  The function itself
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call);
+ * the caller still allocates every input and output buffer.
+ *
+ * - Problems whose workspace (ssd_varlen_workspace_size) exceeds
+ *   SSD_STATIC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before any
+ *   launch; invalid dims return the same codes as ssd_varlen_plan.
+ * - The first call on a device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress); make that first call before any
+ *   stream capture on the device.
+ * - Every call shares the one array, which keeps the previous call's
+ *   contents.  Calls whose GPU work overlaps (different streams or host
+ *   threads without ordering) race on it: order them on one stream.  Each
+ *   call's metadata builder rewrites the error word and counters first.
+ * - plan_out (nullable) receives the plan of this call, valid until the next
+ *   call; pass it to ssd_varlen_status to read this call's device errors.
+ */
+#define SSD_STATIC_SCRATCH_BYTES (32u << 20)
+int ssd_varlen_forward_static(const ssd_dims *dims, const int32_t *cu_seqlens, const int32_t *num_computed,
+                              const ssd_inputs *in, const ssd_outputs *out, cudaStream_t stream,
+                              ssd_plan *plan_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -12,6 +12,7 @@ The functions keep the C names:
   ssd_varlen_forward(plan, inputs, outputs)
   ssd_varlen_status(plan)                          -> device error bits
   ssd_varlen_strerror(code)                        -> text
+  ssd_varlen_forward_static(...)   (C only: forward without a caller workspace)
 and ``run(...)`` wires a whole call from torch tensors (tests and bench use it).
 """
 from __future__ import annotations
@@ -34,7 +35,10 @@ STATUS = {
     -6: "DTYPE", -7: "ALIGN", -8: "WORKSPACE", -9: "PLAN", -10: "CUDA", -11: "UNSUPPORTED",
 }
 EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
-            "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror"]
+            "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror",
+            "ssd_varlen_forward_static"]
+# Size of the library-owned scratch array used by ssd_varlen_forward_static.
+STATIC_SCRATCH_BYTES = 32 << 20
 
 c_i32, c_i64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
 
@@ -95,6 +99,10 @@ def load_library():
     lib.ssd_varlen_status.restype = ctypes.c_int
     lib.ssd_varlen_strerror.argtypes = [ctypes.c_int]
     lib.ssd_varlen_strerror.restype = ctypes.c_char_p
+    lib.ssd_varlen_forward_static.argtypes = [ctypes.POINTER(ssd_dims), c_vp, c_vp,
+                                              ctypes.POINTER(ssd_inputs), ctypes.POINTER(ssd_outputs),
+                                              c_vp, ctypes.POINTER(ssd_plan)]
+    lib.ssd_varlen_forward_static.restype = ctypes.c_int
     _lib = lib
     return lib
 
