@@ -27,14 +27,16 @@
 // bf16 hi + lo parts and their products issued twice into the fp32
 // accumulator.  CB, x, B and C are exact bf16 and go in once.
 //
-// Roles (320 threads, warp-specialised):
+// Roles (576 threads, warp-specialised):
 //   warp 0  TMA producer: x (+ z) tiles into a double-buffered stage, B and C
 //           tiles into one stage released as soon as the state MMA has read them;
 //   warp 1  MMA issuer (one lane) and TMEM owner;
-//   G1      warps 2-5: decay scan, w x split tiles, causal mask (one warp per
-//           TMEM lane quadrant; thread r owns tile row r);
-//   G2      warps 6-9: state bookkeeping, epilogue (y staged in the finished x
+//   G1      warps 2-9: decay scan, w x split tiles, causal mask;
+//   G2      warps 10-17: state bookkeeping, epilogue (y staged in the finished x
 //           tile and stored with coalesced writes), chunk/block/final states.
+// Each of G1 and G2 has two warps per TMEM lane quadrant (thread r owns tile
+// row / TMEM lane r) that split the columns; many warps per role hide the
+// latency of TMEM and shared-memory traffic.
 // G1 can run a piece ahead of G2, and the y accumulators are double-buffered in
 // TMEM (P = 64), so the mask of one piece overlaps the epilogue of the last.
 // Every wait is a bounded mbarrier wait; on a timeout the CTA records
@@ -56,7 +58,8 @@ namespace ssd {
 namespace {
 using namespace sm100;
 
-constexpr int kThreads = 320;                // producer, MMA, 4 G1 math warps, 4 G2 math warps
+constexpr int kMathPerRole = 8;              // G1 and G2 warps each (two per TMEM lane quadrant)
+constexpr int kThreads = 64 + 32 * 2 * kMathPerRole;  // producer, MMA, G1, G2
 constexpr int kRows = 128;                   // tile rows (tokens per piece, at most)
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
 constexpr float kLog2e = 1.4426950408889634f;
@@ -179,6 +182,15 @@ __device__ __forceinline__ float fast_rcp(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float fast_lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// softplus(v) = ln 2 * log2(1 + 2^(v log2 e)); the identity above 20
+__device__ __forceinline__ float softplus_fast(float v) {
+    return v > 20.f ? v : 0.69314718055994531f * fast_lg2(1.f + fast_exp2(v * kLog2e));
+}
 // silu(v) = v / (1 + e^-v)
 __device__ __forceinline__ float silu_fast(float v) { return v * fast_rcp(1.f + fast_exp2(-v * kLog2e)); }
 
@@ -188,11 +200,11 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
     lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
 }
 
-// 32 columns (p0 .. p0+31) of state row n -> bf16 hi/lo copies of h^T row n (MN-major tile).
+// 16 columns (p0 .. p0+15) of state row n -> bf16 hi/lo copies of h^T row n.
 template <int P>
-__device__ __forceinline__ void write_h_copy(TcSmem<P> &s, int n, int pcol0, const uint32_t (&v)[32]) {
+__device__ __forceinline__ void write_h_copy16(TcSmem<P> &s, int n, int pcol0, const uint32_t (&v)[16]) {
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
+    for (int c8 = 0; c8 < 2; ++c8) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -240,20 +252,20 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.full_x[i], 1);
-            mbar_init(&s.empty_x[i], 1 + 4);
+            mbar_init(&s.empty_x[i], 1 + kMathPerRole);
             mbar_init(&s.y_full[i], 1);
-            mbar_init(&s.y_empty[i], 4);
-            mbar_init(&s.cs_ready[i], 4);
+            mbar_init(&s.y_empty[i], kMathPerRole);
+            mbar_init(&s.cs_ready[i], kMathPerRole);
         }
         mbar_init(&s.full_bc, 1);
         mbar_init(&s.empty_bc, 1);
         mbar_init(&s.cb_full, 1);
-        mbar_init(&s.m_full, 4);
+        mbar_init(&s.m_full, kMathPerRole);
         mbar_init(&s.m_done, 1);
-        mbar_init(&s.xd_full, 4);
-        mbar_init(&s.s_free, 4);
+        mbar_init(&s.xd_full, kMathPerRole);
+        mbar_init(&s.s_free, kMathPerRole);
         mbar_init(&s.s_full, 1);
-        mbar_init(&s.h_full, 4);
+        mbar_init(&s.h_full, kMathPerRole);
         s.abort_flag = 0;
         fence_mbar_init();
     }
@@ -384,8 +396,8 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         mma_commit(&s.empty_x[st]);
                     } else {
                         // y_intra = M x with M (hi, lo) in TMEM over the CB columns:
-                        // 32-column block j holds s in [32j, 32j+32): hi in its first
-                        // 16 columns, lo in the next 16 (two bf16 per column).
+                        // the 16 columns [16k, 16k+16) hold s in [16k, 16k+16): hi in
+                        // the first 8 columns, lo in the next 8 (two bf16 per column).
                         if (!wait_bar(&s.m_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                         if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                         tc_fence_after();
@@ -394,7 +406,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         for (int part = 0; part < 2; ++part) {
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
-                                const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                                const uint32_t acol = kk * 16 + part * 8;
                                 mma_ts(tbase + Cfg::col_yi(yb), tbase + acol, sdesc_sw128(sx + kk * 2048, 16384, 1024),
                                        i_y, (part | kk) != 0);
                             }
@@ -412,10 +424,13 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (!STATE_ONLY) mbar_wait(&s.y_full[(pc - 1) % kNY], par((pc - 1) / kNY), kWaitNs);
             }
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------------------------ G1: scan, w x, mask
-        const int q = warp & 3;       // TMEM lane quadrant of this warp
-        const int r = q * 32 + lane;  // tile row / TMEM lane owned by this thread
+        // Eight warps, two per TMEM lane quadrant q = warp % 4; the pair splits
+        // the columns (hf).  Thread r of a pair owns tile row / TMEM lane r.
+        const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
+        const int r = q * 32 + lane;
         const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
         const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
         uint32_t pc = 0;
@@ -432,11 +447,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             int64_t ae;
             bool have_piece = pcs.next(t0, len, ae);
             // raw bf16 bits of dt for the coming piece, one piece ahead (lane l: rows 4l..4l+3)
-            uint32_t dt_raw[4];
+            uint32_t dt_raw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int row = lane * 4 + k;
-                dt_raw[k] = (have_piece && row < len) ? dt16[(size_t)(t0 + row) * p.H + hh] : 0u;
+                if (have_piece && row < len) dt_raw[k] = __ldg(dt16 + (size_t)(t0 + row) * p.H + hh);
             }
             while (have_piece) {
                 const int st = pc % kNS;
@@ -444,20 +459,21 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 int64_t nae = 0;
                 const bool has_next = pcs.next(nt0, nlen, nae);
                 // ---- dt' and the in-piece inclusive cumulative decay (log2 units).
-                // Every G1 warp scans all 128 rows itself: no cross-warp prefix.
+                // Every math warp scans all 128 rows itself: no cross-warp prefix.
                 float dl[4], cl[4];
                 float run = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int row = lane * 4 + k;
-                    dl[k] = row < len ? softplus_f32(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
+                    dl[k] = row < len ? softplus_fast(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
                     run += dl[k] * Ah2;
                     cl[k] = run;
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 4; ++k) {  // next piece's dt: predicated loads, consumed one piece later
                     const int row = lane * 4 + k;
-                    dt_raw[k] = (has_next && row < nlen) ? dt16[(size_t)(nt0 + row) * p.H + hh] : 0u;
+                    dt_raw[k] = 0u;
+                    if (has_next && row < nlen) dt_raw[k] = __ldg(dt16 + (size_t)(nt0 + row) * p.H + hh);
                 }
                 float incl = run;
 #pragma unroll
@@ -469,7 +485,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 const float cs2_last = __shfl_sync(0xffffffffu, incl, 31);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) cl[k] += excl;
-                if ((lane >> 3) == q) {  // publish this quadrant's 32 rows
+                if (hf == 0 && (lane >> 3) == q) {  // publish this quadrant's 32 rows
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         s.cs2[pc & 1][lane * 4 + k] = cl[k];
@@ -492,14 +508,16 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 const float cs2_ref = __shfl_sync(0xffffffffu, cl[3], (8 * q + 31) & 31);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.cs_ready[pc & 1]);
-                // ---- w x (hi, lo) tiles; the previous state MMA must have read them
+                // ---- w x (hi, lo) tiles, this warp's half of the columns; the
+                // previous state MMA must have read the tiles
                 if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                 if (pc > 0 && !wait_bar(&s.s_full, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
                 {
                     const float wr = (r < len) ? fast_exp2(cs2_last - cs2) * d : 0.f;
                     const uint8_t *xs = s.x + st * Cfg::kXBytes;
-#pragma unroll
-                    for (int cb = 0; cb < P / 8; ++cb) {
+#pragma unroll 2
+                    for (int cc = 0; cc < P / 16; ++cc) {
+                        const int cb = hf * (P / 16) + cc;  // 16-byte chunk (8 columns)
                         const uint32_t off = (cb >> 3) * 16384 + sw128_off(r, cb & 7);
                         const uint4 xv = *reinterpret_cast<const uint4 *>(xs + off);
                         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -516,54 +534,58 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (lane == 0) mbar_arrive(&s.xd_full);
                 if (!STATE_ONLY) {
                     // ---- causal decayed mask M = CB o L o dt' (+ D on the diagonal),
-                    // written back over CB in TMEM as bf16 hi/lo.  Below the diagonal
-                    // (column block j < q) exp(cs_r - cs_s) = u_r v_s with both factors
+                    // written back over CB in TMEM as bf16 hi/lo, each 16-column
+                    // group in place of the CB columns it was computed from.  This
+                    // warp takes column blocks j = hf and hf + 2, 16 columns at a time.  Below
+                    // the diagonal (j < q) exp(cs_r - cs_s) = u_r v_s with both factors
                     // <= 1 around the reference row 32q - 1; the diagonal block is
                     // evaluated directly.
                     if (!wait_bar(&s.cs_ready[pc & 1], par(pc >> 1), abort_flag, p.hdr)) { ok = false; break; }
                     if (!wait_bar(&s.cb_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t colCB = 0;
                     const float *cs2v = s.cs2[pc & 1];
                     const float *dv = s.dtp[pc & 1];
                     const float u_r = fast_exp2(cs2 - cs2_ref);
 #pragma unroll 1
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t hi[16], lo[16];
-                        if (j > q) {
+                    for (int jb = 0; jb < 2; ++jb) {
+                        const int j = hf + 2 * jb;
+                        const float wl = (j < q) ? fast_exp2(cs2_ref - cs2v[j * 32 + lane]) * dv[j * 32 + lane] : 0.f;
+#pragma unroll 1
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const uint32_t col = j * 32 + h2 * 16;  // hi in [col, col+8), lo in [col+8, col+16)
+                            uint32_t hi[8], lo[8];
+                            if (j > q) {
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
-                        } else {
-                            uint32_t v[32];
-                            tmem_ld32(tl + colCB + j * 32, v);
-                            if (j < q) {
-                                const int sl = j * 32 + lane;
-                                const float wl = fast_exp2(cs2_ref - cs2v[sl]) * dv[sl];
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int k = 0; k < 16; ++k) {
-                                    const float w0 = __shfl_sync(0xffffffffu, wl, 2 * k);
-                                    const float w1 = __shfl_sync(0xffffffffu, wl, 2 * k + 1);
-                                    split2(__uint_as_float(v[2 * k]) * w0 * u_r, __uint_as_float(v[2 * k + 1]) * w1 * u_r,
-                                           hi[k], lo[k]);
-                                }
+                                for (int k = 0; k < 8; ++k) hi[k] = lo[k] = 0u;
                             } else {
+                                uint32_t v[16];
+                                tmem_ld16(tl + col, v);
                                 tmem_ld_wait();
+                                if (j < q) {
 #pragma unroll
-                                for (int k = 0; k < 16; ++k) {
-                                    const int s0 = j * 32 + 2 * k;
-                                    float m0 = 0.f, m1 = 0.f;
-                                    if (s0 <= r) m0 = __uint_as_float(v[2 * k]) * fast_exp2(cs2 - cs2v[s0]) * dv[s0];
-                                    if (s0 + 1 <= r)
-                                        m1 = __uint_as_float(v[2 * k + 1]) * fast_exp2(cs2 - cs2v[s0 + 1]) * dv[s0 + 1];
-                                    if (s0 == r) m0 += Dh;
-                                    if (s0 + 1 == r) m1 += Dh;
-                                    split2(m0, m1, hi[k], lo[k]);
+                                    for (int k = 0; k < 8; ++k) {
+                                        const float w0 = __shfl_sync(0xffffffffu, wl, h2 * 16 + 2 * k);
+                                        const float w1 = __shfl_sync(0xffffffffu, wl, h2 * 16 + 2 * k + 1);
+                                        split2(__uint_as_float(v[2 * k]) * w0 * u_r,
+                                               __uint_as_float(v[2 * k + 1]) * w1 * u_r, hi[k], lo[k]);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int k = 0; k < 8; ++k) {
+                                        const int s0 = j * 32 + h2 * 16 + 2 * k;
+                                        float m0 = 0.f, m1 = 0.f;
+                                        if (s0 <= r) m0 = __uint_as_float(v[2 * k]) * fast_exp2(cs2 - cs2v[s0]) * dv[s0];
+                                        if (s0 + 1 <= r)
+                                            m1 = __uint_as_float(v[2 * k + 1]) * fast_exp2(cs2 - cs2v[s0 + 1]) * dv[s0 + 1];
+                                        if (s0 == r) m0 += Dh;
+                                        if (s0 + 1 == r) m1 += Dh;
+                                        split2(m0, m1, hi[k], lo[k]);
+                                    }
                                 }
                             }
+                            tmem_st8(tl + col, hi);
+                            tmem_st8(tl + col + 8, lo);
                         }
-                        tmem_st16(tl + colCB + j * 32, hi);
-                        tmem_st16(tl + colCB + j * 32 + 16, lo);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -579,9 +601,13 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         }
     } else {
         // ------------------------------------------------------------ G2: state, epilogue, outputs
+        // Eight warps, two per quadrant; the pair splits the P columns.
         const int q = warp & 3;
+        const int hf = (warp - 10) >> 2;
         const int r = q * 32 + lane;
         const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
+        constexpr int kHalf = P / 2;              // columns per warp
+        const int c0 = hf * kHalf;                // first column of this warp
         const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
         const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
@@ -599,7 +625,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     if (p.init_slots) {
                         const int slot = p.init_slots[it.req];
                         if (slot >= p.num_slots) {
-                            if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
+                            if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
                         } else if (slot >= 0) {
                             src = p.pool + (size_t)slot * slot_elems;
                         }
@@ -615,12 +641,12 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (p.final_slots) {
                     const int fslot = p.final_slots[it.req];
                     if (fslot >= p.num_slots) {
-                        if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
+                        if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
                     } else if (fslot >= 0) {
                         fs = p.pool + (size_t)fslot * slot_elems;
                     }
                 }
-                for (int pp = 0; pp < P; ++pp) {
+                for (int pp = c0; pp < c0 + kHalf; ++pp) {
                     const size_t e = ((size_t)hh * P + pp) * 128 + r;
                     const float v = src ? src[e] : 0.f;
                     if (fd) fd[e] = v;
@@ -630,13 +656,12 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             }
             // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
 #pragma unroll 1
-            for (int j = 0; j < P / 32; ++j) {
-                uint32_t v[32];
+            for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                uint32_t v[16];
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    v[k] = src ? __float_as_uint(src[((size_t)hh * P + j * 32 + k) * 128 + r]) : 0u;
-                tmem_st32(tl + Cfg::kColH + j * 32, v);
-                if (!STATE_ONLY) write_h_copy<P>(s, r, j * 32, v);
+                for (int k = 0; k < 16; ++k) v[k] = src ? __float_as_uint(src[((size_t)hh * P + cs + k) * 128 + r]) : 0u;
+                tmem_st16(tl + Cfg::kColH + cs, v);
+                if (!STATE_ONLY) write_h_copy16<P>(s, r, cs, v);
             }
             tmem_st_wait();
             if (!STATE_ONLY) fence_async_smem();
@@ -652,11 +677,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             int t0, len;
             int64_t ae;
             bool have_piece = pcs.next(t0, len, ae);
-            uint32_t dt_raw[4];  // raw bf16 dt of the coming piece (lane l: rows 4l..4l+3)
+            uint32_t dt_raw[4] = {0u, 0u, 0u, 0u};  // raw bf16 dt of the coming piece (lane l: rows 4l..4l+3)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int row = lane * 4 + k;
-                dt_raw[k] = (have_piece && row < len) ? dt16[(size_t)(t0 + row) * p.H + hh] : 0u;
+                if (have_piece && row < len) dt_raw[k] = __ldg(dt16 + (size_t)(t0 + row) * p.H + hh);
             }
             while (have_piece) {
                 const int st = pc % kNS, yb = pc % kNY;
@@ -668,14 +693,15 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int row = lane * 4 + k;
-                    const float dk = row < len ? softplus_f32(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
+                    const float dk = row < len ? softplus_fast(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
                     run += dk * Ah2;
                     cl[k] = run;
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 4; ++k) {  // next piece's dt: predicated loads, consumed one piece later
                     const int row = lane * 4 + k;
-                    dt_raw[k] = (has_next && row < nlen) ? dt16[(size_t)(nt0 + row) * p.H + hh] : 0u;
+                    dt_raw[k] = 0u;
+                    if (has_next && row < nlen) dt_raw[k] = __ldg(dt16 + (size_t)(nt0 + row) * p.H + hh);
                 }
                 float incl = run;
 #pragma unroll
@@ -697,13 +723,13 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (!Cfg::kSepS) {
                     // in-place state update: scale h^T before the state MMA adds B^T (w x)
 #pragma unroll 1
-                    for (int j = 0; j < P / 32; ++j) {
-                        uint32_t v[32];
-                        tmem_ld32(tl + Cfg::kColH + j * 32, v);
+                    for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tl + Cfg::kColH + cs, v);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * decay);
-                        tmem_st32(tl + Cfg::kColH + j * 32, v);
+                        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * decay);
+                        tmem_st16(tl + Cfg::kColH + cs, v);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -725,11 +751,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     if (p.block_table && p.block_size > 0 && ae % p.block_size == 0) {
                         const int64_t col = ae / p.block_size - 1;
                         if (col >= p.bt_width) {
-                            if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_TABLE);
+                            if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_TABLE);
                         } else {
                             const int bslot = p.block_table[(size_t)it.req * p.bt_width + col];
                             if (bslot >= p.num_slots) {
-                                if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_SLOT);
+                                if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_SLOT);
                             } else if (bslot >= 0) {
                                 dsts[nd++] = p.pool + (size_t)bslot * slot_elems;
                             }
@@ -740,7 +766,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         if (p.final_slots) {
                             const int fslot = p.final_slots[it.req];
                             if (fslot >= p.num_slots) {
-                                if (r == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
+                                if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
                             } else if (fslot >= 0) {
                                 dsts[nd++] = p.pool + (size_t)fslot * slot_elems;
                             }
@@ -748,31 +774,31 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     }
                 } else if (seg_end) {
                     dsts[nd++] = p.seg_state + (size_t)it.seg * slot_elems;
-                    if (r == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = fast_exp2(decay_sum2);
+                    if (r == 0 && hf == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = fast_exp2(decay_sum2);
                 }
                 const bool need_copy = !STATE_ONLY && !seg_end;
                 if (Cfg::kSepS || need_copy || nd > 0) {
 #pragma unroll 1
-                    for (int j = 0; j < P / 32; ++j) {
-                        uint32_t v[32];
-                        tmem_ld32(tl + Cfg::kColH + j * 32, v);
+                    for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tl + Cfg::kColH + cs, v);
                         if (Cfg::kSepS) {
-                            uint32_t sv[32];
-                            tmem_ld32(tl + Cfg::kColS + j * 32, sv);
+                            uint32_t sv[16];
+                            tmem_ld16(tl + Cfg::kColS + cs, sv);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int k = 0; k < 32; ++k)
+                            for (int k = 0; k < 16; ++k)
                                 v[k] = __float_as_uint(fmaf(decay, __uint_as_float(v[k]), __uint_as_float(sv[k])));
-                            tmem_st32(tl + Cfg::kColH + j * 32, v);
+                            tmem_st16(tl + Cfg::kColH + cs, v);
                         } else {
                             tmem_ld_wait();
                         }
                         for (int dd = 0; dd < nd; ++dd) {
-                            float *dst = dsts[dd] + ((size_t)hh * P + j * 32) * 128 + r;
+                            float *dst = dsts[dd] + ((size_t)hh * P + cs) * 128 + r;
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) dst[(size_t)k * 128] = __uint_as_float(v[k]);
+                            for (int k = 0; k < 16; ++k) dst[(size_t)k * 128] = __uint_as_float(v[k]);
                         }
-                        if (need_copy) write_h_copy<P>(s, r, j * 32, v);
+                        if (need_copy) write_h_copy16<P>(s, r, cs, v);
                     }
                     if (Cfg::kSepS) tmem_st_wait();
                     if (need_copy) fence_async_smem();
@@ -795,14 +821,14 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     const uint8_t *zs = s.z + (Cfg::kZTile ? st * Cfg::kXBytes : 0);
                     const size_t yrow = ((size_t)(t0 + r) * p.H + hh) * P;
 #pragma unroll 1
-                    for (int j = 0; j < P / 32; ++j) {
-                        uint32_t vi[32], ve[32];
-                        tmem_ld32(tl + Cfg::col_yi(yb) + j * 32, vi);
-                        tmem_ld32(tl + Cfg::col_ye(yb) + j * 32, ve);
+                    for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                        uint32_t vi[16], ve[16];
+                        tmem_ld16(tl + Cfg::col_yi(yb) + cs, vi);
+                        tmem_ld16(tl + Cfg::col_ye(yb) + cs, ve);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            const int pcol = j * 32 + c8 * 8;
+                        for (int c8 = 0; c8 < 2; ++c8) {
+                            const int pcol = cs + c8 * 8;
                             const uint32_t off = (pcol >> 6) * 16384 + sw128_off(r, (pcol & 63) >> 3);
                             uint32_t zw[4] = {0u, 0u, 0u, 0u};
                             if (z_tile) {
@@ -830,14 +856,14 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&s.y_empty[yb]);
-                    // coalesced copy of this warp's 32 rows: lane l takes 16-byte chunk
-                    // (l mod P/8) of row 32q + l / (P/8) + k (32 / (P/8))
-                    constexpr int kCh = P / 8;            // 16-byte chunks per row
+                    // coalesced copy of this warp's half of its quadrant's 32 rows:
+                    // lane l takes 16-byte chunk (l mod P/16) of row 32q + l / (P/16) + k (512 / P)
+                    constexpr int kCh = P / 16;           // 16-byte chunks per half row
                     constexpr int kRowsPerIt = 32 / kCh;  // rows per warp-wide step
-#pragma unroll 4
+#pragma unroll 2
                     for (int it2 = 0; it2 < 32 / kRowsPerIt; ++it2) {
                         const int rr = q * 32 + it2 * kRowsPerIt + lane / kCh;
-                        const int ch = lane % kCh;
+                        const int ch = hf * kCh + lane % kCh;  // 16-byte chunk within the row
                         if (rr < len) {
                             const uint4 v = *reinterpret_cast<const uint4 *>(ys + (ch >> 3) * 16384 + sw128_off(rr, ch & 7));
                             *reinterpret_cast<uint4 *>(yv + ((size_t)(t0 + rr) * p.H + hh) * P + ch * 8) = v;
