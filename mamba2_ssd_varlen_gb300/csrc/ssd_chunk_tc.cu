@@ -59,7 +59,9 @@ namespace {
 using namespace sm100;
 
 constexpr int kMathPerRole = 8;              // G1 and G2 warps each (two per TMEM lane quadrant)
-constexpr int kThreads = 64 + 32 * 2 * kMathPerRole;  // producer, MMA, G1, G2
+constexpr int kWarpBC = 2 + 2 * kMathPerRole;   // B/C loader warp
+constexpr int kWarpZ = kWarpBC + 1;               // z loader warp
+constexpr int kThreads = 32 * (kWarpZ + 1);       // x/dt producer, MMA, G1, G2, B/C loader, z loader
 constexpr int kRows = 128;                   // tile rows (tokens per piece, at most)
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
 constexpr float kLog2e = 1.4426950408889634f;
@@ -74,6 +76,7 @@ struct TcCfg {
     static constexpr int kNY = (P == 64) ? 2 : 1;     // y_intra / y_inter accumulator pairs in TMEM
     static constexpr bool kSepS = (P == 64);          // state update in its own columns
     static constexpr bool kZTile = (P == 64);         // z staged by TMA
+    static constexpr bool kSepY = (P == 64);          // y staged in its own tile (else in the x tile)
     static constexpr int kXBytes = kRows * P * 2;
     // TMEM columns: CB/M [0,128), then kNY pairs (y_intra, y_inter), then h^T, then S.
     __host__ __device__ static constexpr uint32_t col_yi(int yb) { return 128 + yb * 2 * P; }
@@ -93,10 +96,12 @@ struct __align__(1024) TcSmem {
     uint8_t xd_lo[Cfg::kXBytes];
     uint8_t h_hi[128 * P * 2];           // h^T (rows n, P columns), hi and lo parts
     uint8_t h_lo[128 * P * 2];
+    uint8_t ystage[Cfg::kSepY ? Cfg::kXBytes : 0];           // y of the piece, for coalesced stores
     uint8_t z[Cfg::kZTile ? Cfg::kNS * Cfg::kXBytes : 16];  // last: a stub must not shift the tiles
+    uint16_t dt[2][kRows];               // raw bf16 dt of each x/z stage's piece (zero beyond its length)
     float cs2[2][kRows];                 // per-piece cumulative decay (log2 units), by piece parity
     float dtp[2][kRows];                 // per-piece dt'
-    uint64_t full_x[2], empty_x[2], full_bc, empty_bc;
+    uint64_t full_x[2], empty_x[2], full_z[2], empty_z[2], full_bc, empty_bc;
     uint64_t cb_full, m_full, m_done;
     uint64_t y_full[2], y_empty[2];
     uint64_t xd_full, s_free, s_full, h_full;
@@ -108,7 +113,7 @@ struct __align__(1024) TcSmem {
 // Every operand tile must start on a 1024-byte swizzle-atom boundary.
 #define SSD_TILE_ALIGNED(P_, m) static_assert(offsetof(TcSmem<P_>, m) % 1024 == 0, "tile " #m " misaligned")
 SSD_TILE_ALIGNED(64, b); SSD_TILE_ALIGNED(64, c); SSD_TILE_ALIGNED(64, xd_hi); SSD_TILE_ALIGNED(64, xd_lo);
-SSD_TILE_ALIGNED(64, h_hi); SSD_TILE_ALIGNED(64, h_lo); SSD_TILE_ALIGNED(64, z);
+SSD_TILE_ALIGNED(64, h_hi); SSD_TILE_ALIGNED(64, h_lo); SSD_TILE_ALIGNED(64, z); SSD_TILE_ALIGNED(64, ystage);
 SSD_TILE_ALIGNED(128, b); SSD_TILE_ALIGNED(128, c); SSD_TILE_ALIGNED(128, xd_hi); SSD_TILE_ALIGNED(128, xd_lo);
 SSD_TILE_ALIGNED(128, h_hi); SSD_TILE_ALIGNED(128, h_lo);
 static_assert(sizeof(TcSmem<64>) <= 232448, "P = 64 tiles exceed the 227 KB shared-memory limit");
@@ -161,6 +166,27 @@ struct Pieces {
     }
 };
 
+// The CTA's pieces in order across its work items (used to look one piece ahead).
+struct Cursor {
+    uint32_t w;
+    Item it;
+    Pieces pcs;
+    bool in_item;
+};
+__device__ __forceinline__ bool cursor_next(Cursor &c, const FwdParams &p, bool state_only, int Qi, uint32_t n_work,
+                                            int &t0, int &len, int64_t &ae) {
+    while (true) {
+        if (c.in_item && c.pcs.next(t0, len, ae)) return true;
+        c.in_item = false;
+        if (c.w >= n_work) return false;
+        const uint32_t w = c.w;
+        c.w += gridDim.x;
+        if (!load_item(p, (int)w, state_only, c.it)) continue;
+        c.pcs = Pieces{c.it.abs0, c.it.abs0 + c.it.len, c.it.tok, Qi};
+        c.in_item = true;
+    }
+}
+
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *hdr) {
     if (*abort_flag) return false;
     if (mbar_wait(bar, parity, kWaitNs)) return true;
@@ -191,13 +217,62 @@ __device__ __forceinline__ float fast_lg2(float x) {
 __device__ __forceinline__ float softplus_fast(float v) {
     return v > 20.f ? v : 0.69314718055994531f * fast_lg2(1.f + fast_exp2(v * kLog2e));
 }
-// silu(v) = v / (1 + e^-v)
-__device__ __forceinline__ float silu_fast(float v) { return v * fast_rcp(1.f + fast_exp2(-v * kLog2e)); }
 
-// v ~= hi + lo with hi = bf16(v) and lo = bf16(v - hi): 16 significant bits.
-__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
-    hi = pack_bf16x2(a, b);
-    lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+// ---- packed fp32 pairs (one 64-bit register pair) for the f32x2 instructions
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ void f2_get(uint64_t d, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16x2 word (low half first) -> the two values as an exact fp32 pair
+__device__ __forceinline__ uint64_t f2_bf16x2(uint32_t w) {
+    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// silu of a pair, v / (1 + e^-v), on the special-function unit (exp2 and an
+// approximate reciprocal, both to ~2^-22 relative).
+__device__ __forceinline__ uint64_t silu2(uint64_t z) {
+    float a, b;
+    f2_get(f2_mul(z, f2(-kLog2e, -kLog2e)), a, b);
+    const uint64_t den = f2_add(f2(fast_exp2(a), fast_exp2(b)), f2(1.f, 1.f));
+    float da, db;
+    f2_get(den, da, db);
+    return f2_mul(z, f2(fast_rcp(da), fast_rcp(db)));
+}
+
+// Pair (a, b) ~= hi + lo in bf16x2: hi is each value truncated to bf16 (its
+// upper 16 bits, exact), lo = bf16(v - hi) rounded; 16 significant bits kept.
+__device__ __forceinline__ void split_pair(uint64_t ab, uint32_t &hi, uint32_t &lo) {
+    uint32_t ua, ub;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(ua), "=r"(ub) : "l"(ab));
+    hi = __byte_perm(ua, ub, 0x7632);
+    const uint64_t rest = f2_sub(ab, f2(__uint_as_float(ua & 0xFFFF0000u), __uint_as_float(ub & 0xFFFF0000u)));
+    float ra, rb;
+    f2_get(rest, ra, rb);
+    lo = pack_bf16x2(ra, rb);
 }
 
 // 16 columns (p0 .. p0+15) of state row n -> bf16 hi/lo copies of h^T row n.
@@ -208,7 +283,7 @@ __device__ __forceinline__ void write_h_copy16(TcSmem<P> &s, int n, int pcol0, c
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            split2(__uint_as_float(v[c8 * 8 + 2 * e]), __uint_as_float(v[c8 * 8 + 2 * e + 1]), hi[e], lo[e]);
+            split_pair(f2(__uint_as_float(v[c8 * 8 + 2 * e]), __uint_as_float(v[c8 * 8 + 2 * e + 1])), hi[e], lo[e]);
         const int pcol = pcol0 + c8 * 8;
         const uint32_t off = (pcol >> 6) * 16384 + sw128_off(n, (pcol & 63) >> 3);
         *reinterpret_cast<uint4 *>(s.h_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -251,8 +326,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.full_x[i], 1);
-            mbar_init(&s.empty_x[i], 1 + kMathPerRole);
+            mbar_init(&s.full_x[i], 2);  // TMA bytes + the producer warp's dt stores
+            // x is released by the MMA that last reads it, plus G2 when y is staged in it
+            mbar_init(&s.empty_x[i], 1 + (Cfg::kSepY ? 0 : kMathPerRole));
+            mbar_init(&s.full_z[i], 1);
+            mbar_init(&s.empty_z[i], kMathPerRole);
             mbar_init(&s.y_full[i], 1);
             mbar_init(&s.y_empty[i], kMathPerRole);
             mbar_init(&s.cs_ready[i], kMathPerRole);
@@ -281,52 +359,58 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // Lane 0 issues the TMA loads; the whole warp stages each piece's dt (128
+        // strided bf16 values) into shared memory, loaded into registers one
+        // piece ahead so the staging never waits on global memory.
+        const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
         if (lane == 0) {
             prefetch_tmap(&maps.x);
-            prefetch_tmap(&maps.b);
-            if (!STATE_ONLY) prefetch_tmap(&maps.c);
-            if (z_tile) prefetch_tmap(&maps.z);
-            uint32_t pc = 0;
-            bool ok = true;
-            const uint32_t xbytes = Cfg::kXBytes * (z_tile ? 2 : 1);
-            const uint32_t bcbytes = kRows * 128 * 2 * (STATE_ONLY ? 1 : 2);
-            for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
-                Item it;
-                if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
-                const int g = it.head / (p.H / p.G);
-                Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
-                int t0, len;
-                int64_t ae;
-                while (pcs.next(t0, len, ae)) {
-                    const int st = pc % kNS;
-                    if (pc >= (uint32_t)kNS && !wait_bar(&s.empty_x[st], par(pc / kNS - 1), abort_flag, p.hdr)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&s.full_x[st], xbytes);
-                    uint8_t *xs = s.x + st * Cfg::kXBytes;
-                    for (int q = 0; q < kPB; ++q) tma_load_3d(xs + q * 16384, &maps.x, &s.full_x[st], q * 64, it.head, t0);
-                    if (z_tile) tma_load_3d(s.z + st * Cfg::kXBytes, &maps.z, &s.full_x[st], 0, it.head, t0);
-                    if (pc >= 1 && !wait_bar(&s.empty_bc, par(pc - 1), abort_flag, p.hdr)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&s.full_bc, bcbytes);
-                    tma_load_3d(s.b, &maps.b, &s.full_bc, 0, g, t0);
-                    tma_load_3d(s.b + 16384, &maps.b, &s.full_bc, 64, g, t0);
-                    if (!STATE_ONLY) {
-                        tma_load_3d(s.c, &maps.c, &s.full_bc, 0, g, t0);
-                        tma_load_3d(s.c + 16384, &maps.c, &s.full_bc, 64, g, t0);
-                    }
-                    ++pc;
-                }
-            }
-            // Never leave a copy in flight: wait for the last issued loads.
-            if (pc > 0) {
-                mbar_wait(&s.full_bc, par(pc - 1), kWaitNs);
-                mbar_wait(&s.full_x[(pc - 1) % kNS], par((pc - 1) / kNS), kWaitNs);
-            }
         }
+        uint32_t pc = 0;
+        bool ok = true;
+        const uint32_t xbytes = Cfg::kXBytes;
+        Cursor cur{blockIdx.x, Item{}, Pieces{}, false};
+        int t0 = 0, len = 0;
+        int64_t ae = 0;
+        bool have = cursor_next(cur, p, STATE_ONLY, Qi, n_work, t0, len, ae);
+        int head = cur.it.head;
+        uint16_t dtr[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (have && lane * 4 + k < len) dtr[k] = dt16[(size_t)(t0 + lane * 4 + k) * p.H + head];
+        while (ok && have) {
+            int nt0 = 0, nlen = 0;
+            int64_t nae = 0;
+            const bool nhave = cursor_next(cur, p, STATE_ONLY, Qi, n_work, nt0, nlen, nae);
+            const int nhead = cur.it.head;
+            const int st = pc % kNS;
+            bool good = true;
+            if (lane == 0 && pc >= (uint32_t)kNS) good = wait_bar(&s.empty_x[st], par(pc / kNS - 1), abort_flag, p.hdr);
+            if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&s.full_x[st], xbytes);
+                uint8_t *xs = s.x + st * Cfg::kXBytes;
+                for (int q = 0; q < kPB; ++q) tma_load_3d(xs + q * 16384, &maps.x, &s.full_x[st], q * 64, head, t0);
+            }
+            *reinterpret_cast<uint2 *>(&s.dt[st][lane * 4]) =
+                make_uint2((uint32_t)dtr[0] | ((uint32_t)dtr[1] << 16), (uint32_t)dtr[2] | ((uint32_t)dtr[3] << 16));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.full_x[st]);
+            // the next piece's dt, consumed one iteration later
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                dtr[k] = 0;
+                if (nhave && lane * 4 + k < nlen) dtr[k] = dt16[(size_t)(nt0 + lane * 4 + k) * p.H + nhead];
+            }
+            t0 = nt0;
+            len = nlen;
+            ae = nae;
+            head = nhead;
+            have = nhave;
+            ++pc;
+        }
+        // Never leave a copy in flight: wait for the last issued loads.
+        if (lane == 0 && pc > 0) mbar_wait(&s.full_x[(pc - 1) % kNS], par((pc - 1) / kNS), kWaitNs);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -432,7 +516,6 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         const int hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
-        const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
         uint32_t pc = 0;
         bool ok = true;
         for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
@@ -446,34 +529,27 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             int t0, len;
             int64_t ae;
             bool have_piece = pcs.next(t0, len, ae);
-            // raw bf16 bits of dt for the coming piece, one piece ahead (lane l: rows 4l..4l+3)
-            uint32_t dt_raw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int row = lane * 4 + k;
-                if (have_piece && row < len) dt_raw[k] = __ldg(dt16 + (size_t)(t0 + row) * p.H + hh);
-            }
             while (have_piece) {
                 const int st = pc % kNS;
                 int nt0 = 0, nlen = 0;
                 int64_t nae = 0;
                 const bool has_next = pcs.next(nt0, nlen, nae);
-                // ---- dt' and the in-piece inclusive cumulative decay (log2 units).
+                // ---- dt' and the in-piece inclusive cumulative decay (log2 units),
+                // from the dt the producer staged with this piece's x tile.
                 // Every math warp scans all 128 rows itself: no cross-warp prefix.
+                if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                 float dl[4], cl[4];
                 float run = 0.f;
+                {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(&s.dt[st][lane * 4]);
+                    const uint32_t rw[4] = {raw.x << 16, raw.x & 0xFFFF0000u, raw.y << 16, raw.y & 0xFFFF0000u};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int row = lane * 4 + k;
-                    dl[k] = row < len ? softplus_fast(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
-                    run += dl[k] * Ah2;
-                    cl[k] = run;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {  // next piece's dt: predicated loads, consumed one piece later
-                    const int row = lane * 4 + k;
-                    dt_raw[k] = 0u;
-                    if (has_next && row < nlen) dt_raw[k] = __ldg(dt16 + (size_t)(nt0 + row) * p.H + hh);
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = lane * 4 + k;
+                        dl[k] = row < len ? softplus_fast(__uint_as_float(rw[k]) + dtb) : 0.f;
+                        run += dl[k] * Ah2;
+                        cl[k] = run;
+                    }
                 }
                 float incl = run;
 #pragma unroll
@@ -510,7 +586,6 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (lane == 0) mbar_arrive(&s.cs_ready[pc & 1]);
                 // ---- w x (hi, lo) tiles, this warp's half of the columns; the
                 // previous state MMA must have read the tiles
-                if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                 if (pc > 0 && !wait_bar(&s.s_full, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
                 {
                     const float wr = (r < len) ? fast_exp2(cs2_last - cs2) * d : 0.f;
@@ -522,9 +597,9 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         const uint4 xv = *reinterpret_cast<const uint4 *>(xs + off);
                         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
                         uint32_t hi[4], lo[4];
+                        const uint64_t wr2 = f2(wr, wr);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split2(bf16lo_to_f32(xw[e]) * wr, bf16hi_to_f32(xw[e]) * wr, hi[e], lo[e]);
+                        for (int e = 0; e < 4; ++e) split_pair(f2_mul(f2_bf16x2(xw[e]), wr2), hi[e], lo[e]);
                         *reinterpret_cast<uint4 *>(s.xd_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4 *>(s.xd_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
@@ -535,8 +610,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (!STATE_ONLY) {
                     // ---- causal decayed mask M = CB o L o dt' (+ D on the diagonal),
                     // written back over CB in TMEM as bf16 hi/lo, each 16-column
-                    // group in place of the CB columns it was computed from.  This
-                    // warp takes column blocks j = hf and hf + 2, 16 columns at a time.  Below
+                    // group in place of the CB columns it was computed from.  Below
                     // the diagonal (j < q) exp(cs_r - cs_s) = u_r v_s with both factors
                     // <= 1 around the reference row 32q - 1; the diagonal block is
                     // evaluated directly.
@@ -546,46 +620,51 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     const float *cs2v = s.cs2[pc & 1];
                     const float *dv = s.dtp[pc & 1];
                     const float u_r = fast_exp2(cs2 - cs2_ref);
+                    // 16-column group g = 2j + hf of every 32-column block j: both warps of
+                    // the pair get half of the diagonal block and half of the rest.
 #pragma unroll 1
-                    for (int jb = 0; jb < 2; ++jb) {
-                        const int j = hf + 2 * jb;
-                        const float wl = (j < q) ? fast_exp2(cs2_ref - cs2v[j * 32 + lane]) * dv[j * 32 + lane] : 0.f;
-#pragma unroll 1
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const uint32_t col = j * 32 + h2 * 16;  // hi in [col, col+8), lo in [col+8, col+16)
-                            uint32_t hi[8], lo[8];
-                            if (j > q) {
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t col = j * 32 + hf * 16;  // hi in [col, col+8), lo in [col+8, col+16)
+                        uint32_t hi[8], lo[8];
+                        if (j > q) {
 #pragma unroll
-                                for (int k = 0; k < 8; ++k) hi[k] = lo[k] = 0u;
-                            } else {
-                                uint32_t v[16];
-                                tmem_ld16(tl + col, v);
-                                tmem_ld_wait();
-                                if (j < q) {
+                            for (int k = 0; k < 8; ++k) hi[k] = lo[k] = 0u;
+                        } else if (j < q) {
+                            uint32_t v[16];
+                            tmem_ld16(tl + col, v);
+                            const int sl = j * 32 + lane;
+                            const float wl = fast_exp2(cs2_ref - cs2v[sl]) * dv[sl];
+                            tmem_ld_wait();
+                            const uint64_t u2 = f2(u_r, u_r);
 #pragma unroll
-                                    for (int k = 0; k < 8; ++k) {
-                                        const float w0 = __shfl_sync(0xffffffffu, wl, h2 * 16 + 2 * k);
-                                        const float w1 = __shfl_sync(0xffffffffu, wl, h2 * 16 + 2 * k + 1);
-                                        split2(__uint_as_float(v[2 * k]) * w0 * u_r,
-                                               __uint_as_float(v[2 * k + 1]) * w1 * u_r, hi[k], lo[k]);
-                                    }
-                                } else {
-#pragma unroll
-                                    for (int k = 0; k < 8; ++k) {
-                                        const int s0 = j * 32 + h2 * 16 + 2 * k;
-                                        float m0 = 0.f, m1 = 0.f;
-                                        if (s0 <= r) m0 = __uint_as_float(v[2 * k]) * fast_exp2(cs2 - cs2v[s0]) * dv[s0];
-                                        if (s0 + 1 <= r)
-                                            m1 = __uint_as_float(v[2 * k + 1]) * fast_exp2(cs2 - cs2v[s0 + 1]) * dv[s0 + 1];
-                                        if (s0 == r) m0 += Dh;
-                                        if (s0 + 1 == r) m1 += Dh;
-                                        split2(m0, m1, hi[k], lo[k]);
-                                    }
-                                }
+                            for (int k = 0; k < 8; ++k) {
+                                const uint64_t w2 = f2(__shfl_sync(0xffffffffu, wl, hf * 16 + 2 * k),
+                                                       __shfl_sync(0xffffffffu, wl, hf * 16 + 2 * k + 1));
+                                const uint64_t cb2 = f2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                                split_pair(f2_mul(f2_mul(cb2, w2), u2), hi[k], lo[k]);
                             }
-                            tmem_st8(tl + col, hi);
-                            tmem_st8(tl + col + 8, lo);
+                        } else {
+                            uint32_t v[16];
+                            tmem_ld16(tl + col, v);
+                            tmem_ld_wait();
+                            const uint64_t r2 = f2(cs2, cs2);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const int s0 = col + 2 * k;
+                                const float2 c2 = *reinterpret_cast<const float2 *>(cs2v + s0);
+                                const float2 d2 = *reinterpret_cast<const float2 *>(dv + s0);
+                                float e0, e1;
+                                f2_get(f2_sub(r2, f2(c2.x, c2.y)), e0, e1);
+                                const uint64_t cb2 = f2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                                float m0, m1;
+                                f2_get(f2_mul(f2_mul(cb2, f2(fast_exp2(e0), fast_exp2(e1))), f2(d2.x, d2.y)), m0, m1);
+                                m0 = (s0 < r) ? m0 : ((s0 == r) ? m0 + Dh : 0.f);
+                                m1 = (s0 + 1 < r) ? m1 : ((s0 + 1 == r) ? m1 + Dh : 0.f);
+                                split_pair(f2(m0, m1), hi[k], lo[k]);
+                            }
                         }
+                        tmem_st8(tl + col, hi);
+                        tmem_st8(tl + col + 8, lo);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -599,7 +678,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 have_piece = has_next;
             }
         }
-    } else {
+    } else if (warp < kWarpBC) {
         // ------------------------------------------------------------ G2: state, epilogue, outputs
         // Eight warps, two per quadrant; the pair splits the P columns.
         const int q = warp & 3;
@@ -610,7 +689,6 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         const int c0 = hf * kHalf;                // first column of this warp
         const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
-        const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
         uint32_t pc = 0;
         bool ok = true;
         for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
@@ -677,31 +755,24 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             int t0, len;
             int64_t ae;
             bool have_piece = pcs.next(t0, len, ae);
-            uint32_t dt_raw[4] = {0u, 0u, 0u, 0u};  // raw bf16 dt of the coming piece (lane l: rows 4l..4l+3)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int row = lane * 4 + k;
-                if (have_piece && row < len) dt_raw[k] = __ldg(dt16 + (size_t)(t0 + row) * p.H + hh);
-            }
             while (have_piece) {
                 const int st = pc % kNS, yb = pc % kNY;
                 int nt0 = 0, nlen = 0;
                 int64_t nae = 0;
                 const bool has_next = pcs.next(nt0, nlen, nae);
                 // ---- this warp's own scan of the piece (same arithmetic as G1)
+                if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                 float run = 0.f, cl[4];
+                {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(&s.dt[st][lane * 4]);
+                    const uint32_t rw[4] = {raw.x << 16, raw.x & 0xFFFF0000u, raw.y << 16, raw.y & 0xFFFF0000u};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int row = lane * 4 + k;
-                    const float dk = row < len ? softplus_fast(__uint_as_float(dt_raw[k] << 16) + dtb) : 0.f;
-                    run += dk * Ah2;
-                    cl[k] = run;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {  // next piece's dt: predicated loads, consumed one piece later
-                    const int row = lane * 4 + k;
-                    dt_raw[k] = 0u;
-                    if (has_next && row < nlen) dt_raw[k] = __ldg(dt16 + (size_t)(nt0 + row) * p.H + hh);
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = lane * 4 + k;
+                        const float dk = row < len ? softplus_fast(__uint_as_float(rw[k]) + dtb) : 0.f;
+                        run += dk * Ah2;
+                        cl[k] = run;
+                    }
                 }
                 float incl = run;
 #pragma unroll
@@ -779,26 +850,41 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 const bool need_copy = !STATE_ONLY && !seg_end;
                 if (Cfg::kSepS || need_copy || nd > 0) {
 #pragma unroll 1
-                    for (int cs = c0; cs < c0 + kHalf; cs += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(tl + Cfg::kColH + cs, v);
+                    for (int cs = c0; cs < c0 + kHalf; cs += 32) {  // two 16-column groups per TMEM wait
+                        uint32_t v[2][16];
+                        tmem_ld16(tl + Cfg::kColH + cs, v[0]);
+                        tmem_ld16(tl + Cfg::kColH + cs + 16, v[1]);
                         if (Cfg::kSepS) {
-                            uint32_t sv[16];
-                            tmem_ld16(tl + Cfg::kColS + cs, sv);
+                            uint32_t sv[2][16];
+                            tmem_ld16(tl + Cfg::kColS + cs, sv[0]);
+                            tmem_ld16(tl + Cfg::kColS + cs + 16, sv[1]);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                v[k] = __float_as_uint(fmaf(decay, __uint_as_float(v[k]), __uint_as_float(sv[k])));
-                            tmem_st16(tl + Cfg::kColH + cs, v);
+                            for (int g2 = 0; g2 < 2; ++g2) {
+                                const uint64_t dec2 = f2(decay, decay);
+#pragma unroll
+                                for (int k = 0; k < 16; k += 2) {
+                                    float a, b;
+                                    f2_get(f2_fma(dec2, f2(__uint_as_float(v[g2][k]), __uint_as_float(v[g2][k + 1])),
+                                                  f2(__uint_as_float(sv[g2][k]), __uint_as_float(sv[g2][k + 1]))),
+                                           a, b);
+                                    v[g2][k] = __float_as_uint(a);
+                                    v[g2][k + 1] = __float_as_uint(b);
+                                }
+                                tmem_st16(tl + Cfg::kColH + cs + 16 * g2, v[g2]);
+                            }
                         } else {
                             tmem_ld_wait();
                         }
-                        for (int dd = 0; dd < nd; ++dd) {
-                            float *dst = dsts[dd] + ((size_t)hh * P + cs) * 128 + r;
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) dst[(size_t)k * 128] = __uint_as_float(v[k]);
+                        for (int g2 = 0; g2 < 2; ++g2) {
+                            for (int dd = 0; dd < nd; ++dd) {
+                                float *dst = dsts[dd] + ((size_t)hh * P + cs + 16 * g2) * 128 + r;
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) dst[(size_t)k * 128] = __uint_as_float(v[g2][k]);
+                            }
+                            if (need_copy) write_h_copy16<P>(s, r, cs + 16 * g2, v[g2]);
                         }
-                        if (need_copy) write_h_copy16<P>(s, r, cs, v);
                     }
                     if (Cfg::kSepS) tmem_st_wait();
                     if (need_copy) fence_async_smem();
@@ -810,14 +896,15 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     }
                 }
                 if (STATE_ONLY) {
-                    if (lane == 0) mbar_arrive(&s.empty_x[st]);
+                    if (!Cfg::kSepY && lane == 0) mbar_arrive(&s.empty_x[st]);
                 } else {
                     // ---- epilogue: y = (y_intra + exp(cs) y_inter) * silu(z), staged
                     // in this stage's x tile, then stored with coalesced 16-byte writes.
                     if (!wait_bar(&s.y_full[yb], par(pc / kNY), abort_flag, p.hdr)) { ok = false; break; }
+                    if (z_tile && !wait_bar(&s.full_z[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
                     const float ecs = fast_exp2(cs2);
-                    uint8_t *ys = s.x + st * Cfg::kXBytes;
+                    uint8_t *ys = Cfg::kSepY ? s.ystage : s.x + st * Cfg::kXBytes;
                     const uint8_t *zs = s.z + (Cfg::kZTile ? st * Cfg::kXBytes : 0);
                     const size_t yrow = ((size_t)(t0 + r) * p.H + hh) * P;
 #pragma unroll 1
@@ -839,15 +926,15 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                                 zw[0] = zq.x; zw[1] = zq.y; zw[2] = zq.z; zw[3] = zq.w;
                             }
                             uint32_t out[4];
+                            const uint64_t ecs2 = f2(ecs, ecs);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int k0 = c8 * 8 + 2 * e;
-                                float y0 = fmaf(ecs, __uint_as_float(ve[k0]), __uint_as_float(vi[k0]));
-                                float y1 = fmaf(ecs, __uint_as_float(ve[k0 + 1]), __uint_as_float(vi[k0 + 1]));
-                                if (zv) {
-                                    y0 *= silu_fast(bf16lo_to_f32(zw[e]));
-                                    y1 *= silu_fast(bf16hi_to_f32(zw[e]));
-                                }
+                                uint64_t y2 = f2_fma(ecs2, f2(__uint_as_float(ve[k0]), __uint_as_float(ve[k0 + 1])),
+                                                     f2(__uint_as_float(vi[k0]), __uint_as_float(vi[k0 + 1])));
+                                if (zv) y2 = f2_mul(y2, silu2(f2_bf16x2(zw[e])));
+                                float y0, y1;
+                                f2_get(y2, y0, y1);
                                 out[e] = pack_bf16x2(y0, y1);
                             }
                             *reinterpret_cast<uint4 *>(ys + off) = make_uint4(out[0], out[1], out[2], out[3]);
@@ -855,7 +942,10 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&s.y_empty[yb]);
+                    if (lane == 0) {
+                        mbar_arrive(&s.y_empty[yb]);
+                        if (z_tile) mbar_arrive(&s.empty_z[st]);
+                    }
                     // coalesced copy of this warp's half of its quadrant's 32 rows:
                     // lane l takes 16-byte chunk (l mod P/16) of row 32q + l / (P/16) + k (512 / P)
                     constexpr int kCh = P / 16;           // 16-byte chunks per half row
@@ -869,9 +959,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                             *reinterpret_cast<uint4 *>(yv + ((size_t)(t0 + rr) * p.H + hh) * P + ch * 8) = v;
                         }
                     }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s.empty_x[st]);
+                    if (!Cfg::kSepY) {
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&s.empty_x[st]);
+                    }
                 }
                 ++pc;
                 t0 = nt0;
@@ -879,6 +971,47 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 ae = nae;
                 have_piece = has_next;
             }
+        }
+    } else if (warp == kWarpBC) {
+        // ------------------------------------------------------------ B and C loader
+        if (lane == 0) {
+            prefetch_tmap(&maps.b);
+            if (!STATE_ONLY) prefetch_tmap(&maps.c);
+            const uint32_t bcbytes = kRows * 128 * 2 * (STATE_ONLY ? 1 : 2);
+            Cursor cur{blockIdx.x, Item{}, Pieces{}, false};
+            int t0 = 0, len = 0;
+            int64_t ae = 0;
+            uint32_t pc = 0;
+            while (cursor_next(cur, p, STATE_ONLY, Qi, n_work, t0, len, ae)) {
+                const int g = cur.it.head / (p.H / p.G);
+                if (pc >= 1 && !wait_bar(&s.empty_bc, par(pc - 1), abort_flag, p.hdr)) break;
+                mbar_arrive_expect_tx(&s.full_bc, bcbytes);
+                tma_load_3d(s.b, &maps.b, &s.full_bc, 0, g, t0);
+                tma_load_3d(s.b + 16384, &maps.b, &s.full_bc, 64, g, t0);
+                if (!STATE_ONLY) {
+                    tma_load_3d(s.c, &maps.c, &s.full_bc, 0, g, t0);
+                    tma_load_3d(s.c + 16384, &maps.c, &s.full_bc, 64, g, t0);
+                }
+                ++pc;
+            }
+            if (pc > 0) mbar_wait(&s.full_bc, par(pc - 1), kWaitNs);
+        }
+    } else {
+        // ------------------------------------------------------------ z loader
+        if (lane == 0 && z_tile) {
+            prefetch_tmap(&maps.z);
+            Cursor cur{blockIdx.x, Item{}, Pieces{}, false};
+            int t0 = 0, len = 0;
+            int64_t ae = 0;
+            uint32_t pc = 0;
+            while (cursor_next(cur, p, STATE_ONLY, Qi, n_work, t0, len, ae)) {
+                const int st = pc % kNS;
+                if (pc >= (uint32_t)kNS && !wait_bar(&s.empty_z[st], par(pc / kNS - 1), abort_flag, p.hdr)) break;
+                mbar_arrive_expect_tx(&s.full_z[st], Cfg::kXBytes);
+                tma_load_3d(s.z + st * Cfg::kXBytes, &maps.z, &s.full_z[st], 0, cur.it.head, t0);
+                ++pc;
+            }
+            if (pc > 0) mbar_wait(&s.full_z[(pc - 1) % kNS], par((pc - 1) / kNS), kWaitNs);
         }
     }
 
