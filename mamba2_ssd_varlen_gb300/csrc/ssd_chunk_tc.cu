@@ -27,13 +27,18 @@
 // bf16 hi + lo parts and their products issued twice into the fp32
 // accumulator.  CB, x, B and C are exact bf16 and go in once.
 //
-// Roles (576 threads, warp-specialised):
-//   warp 0  TMA producer: x (+ z) tiles into a double-buffered stage, B and C
-//           tiles into one stage released as soon as the state MMA has read them;
+// Roles (640 threads, warp-specialised):
+//   warp 0  producer: draws the work items (a ticket counter in the scan), the
+//           x tiles by TMA into a double-buffered stage (P = 64), and per piece
+//           dt' and the cumulative decay, computed once and published beside
+//           the x tile;
 //   warp 1  MMA issuer (one lane) and TMEM owner;
-//   G1      warps 2-9: decay scan, w x split tiles, causal mask;
-//   G2      warps 10-17: state bookkeeping, epilogue (y staged in the finished x
-//           tile and stored with coalesced writes), chunk/block/final states.
+//   G1      warps 2-9: w x split tiles, causal mask;
+//   G2      warps 10-17: state bookkeeping, epilogue (y staged in shared memory
+//           and stored with coalesced writes), chunk/block/final states;
+//   warp 18 B and C tiles by TMA, each reloaded as soon as its last MMA of the
+//           piece has read it (C after y_inter, B after the state update);
+//   warp 19 z tiles by TMA (P = 64).
 // Each of G1 and G2 has two warps per TMEM lane quadrant (thread r owns tile
 // row / TMEM lane r) that split the columns; many warps per role hide the
 // latency of TMEM and shared-memory traffic.
@@ -77,6 +82,10 @@ struct TcCfg {
     static constexpr bool kSepS = (P == 64);          // state update in its own columns
     static constexpr bool kZTile = (P == 64);         // z staged by TMA
     static constexpr bool kSepY = (P == 64);          // y staged in its own tile (else in the x tile)
+    // Slots of the per-piece decay values.  With y in its own tile G2 does not
+    // hold the x stage, so the values G2 reads get their own deeper ring (and
+    // barriers); otherwise they live and die with the x stage.
+    static constexpr int kNC = kSepY ? 4 : kNS;
     static constexpr int kXBytes = kRows * P * 2;
     // TMEM columns: CB/M [0,128), then kNY pairs (y_intra, y_inter), then h^T, then S.
     __host__ __device__ static constexpr uint32_t col_yi(int yb) { return 128 + yb * 2 * P; }
@@ -98,14 +107,17 @@ struct __align__(1024) TcSmem {
     uint8_t h_lo[128 * P * 2];
     uint8_t ystage[Cfg::kSepY ? Cfg::kXBytes : 0];           // y of the piece, for coalesced stores
     uint8_t z[Cfg::kZTile ? Cfg::kNS * Cfg::kXBytes : 16];  // last: a stub must not shift the tiles
-    uint16_t dt[2][kRows];               // raw bf16 dt of each x/z stage's piece (zero beyond its length)
-    float cs2[2][kRows];                 // per-piece cumulative decay (log2 units), by piece parity
-    float dtp[2][kRows];                 // per-piece dt'
-    uint64_t full_x[2], empty_x[2], full_z[2], empty_z[2], full_bc, empty_bc;
+    float cs2[Cfg::kNC][kRows];          // per slot: the piece's cumulative decay (log2 units)
+    float dtp[Cfg::kNC][kRows];          // per slot: dt' (zero beyond the piece's length)
+    float cslast[Cfg::kNC];              // per slot: the piece's total decay (log2 units)
+    uint64_t full_x[2], empty_x[2], full_z[2], empty_z[2];
+    uint64_t full_b, empty_b, full_c, empty_c;
+    uint64_t full_cs[4], empty_cs[4];    // decay-value ring (kSepY only)
     uint64_t cb_full, m_full, m_done;
     uint64_t y_full[2], y_empty[2];
     uint64_t xd_full, s_free, s_full, h_full;
-    uint64_t cs_ready[2];
+    int32_t item_ring[8];                // work items in the order the CTA processes them (-1: none left)
+    uint64_t item_full[8], item_empty[8];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -166,24 +178,19 @@ struct Pieces {
     }
 };
 
-// The CTA's pieces in order across its work items (used to look one piece ahead).
-struct Cursor {
-    uint32_t w;
-    Item it;
-    Pieces pcs;
-    bool in_item;
-};
-__device__ __forceinline__ bool cursor_next(Cursor &c, const FwdParams &p, bool state_only, int Qi, uint32_t n_work,
-                                            int &t0, int &len, int64_t &ae) {
-    while (true) {
-        if (c.in_item && c.pcs.next(t0, len, ae)) return true;
-        c.in_item = false;
-        if (c.w >= n_work) return false;
-        const uint32_t w = c.w;
-        c.w += gridDim.x;
-        if (!load_item(p, (int)w, state_only, c.it)) continue;
-        c.pcs = Pieces{c.it.abs0, c.it.abs0 + c.it.len, c.it.tok, Qi};
-        c.in_item = true;
+extern __shared__ __align__(1024) uint8_t tc_smem[];
+
+// Phase parity of a barrier's use-th completion.
+__device__ __forceinline__ uint32_t par(uint32_t use) { return use & 1u; }
+
+// The first wait of a launch to time out leaves where it was: header word
+// kHdrTimeoutAt = 1 + the waited barrier's byte offset in shared memory, the
+// next two words its block and thread.
+__device__ __noinline__ void record_timeout(int32_t *hdr, int site) {
+    atomicOr(hdr + kHdrErr, SSD_DEVERR_TIMEOUT);
+    if (atomicCAS(hdr + kHdrTimeoutAt, 0, 1 + site) == 0) {
+        hdr[kHdrTimeoutAt + 1] = (int32_t)blockIdx.x;
+        hdr[kHdrTimeoutAt + 2] = (int32_t)threadIdx.x;
     }
 }
 
@@ -191,7 +198,90 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     if (*abort_flag) return false;
     if (mbar_wait(bar, parity, kWaitNs)) return true;
     *abort_flag = 1;
-    atomicOr(hdr + kHdrErr, SSD_DEVERR_TIMEOUT);
+    record_timeout(hdr, (int)(smem_u32(bar) - smem_u32(tc_smem)));
+    return false;
+}
+
+// ---- work items -----------------------------------------------------------
+// Every role walks the same items in the same order.  The producer warp draws
+// them -- in the scan from a global ticket counter, so CTAs that run faster
+// take more items and neighbouring CTAs work on neighbouring (segment, head)
+// items; in the state pre-pass by striding over the grid -- and publishes each
+// through a ring in shared memory that the other roles read.
+constexpr int kItemRing = 8;
+
+// Producer: the next item index for this CTA (-1: none left), published.
+// Only items with pieces are published (the state pre-pass has none for a
+// request's last segment; an empty request's final state is written by
+// seg_pass_kernel), so every published item holds a piece and a ring of 8
+// covers the producer's look-ahead of two pieces: publishing item n waits for
+// item n - 8, which every role reaches with inputs already issued.
+template <bool STATE_ONLY, class Smem>
+__device__ __forceinline__ int publish_item(Smem &s, const FwdParams &p, uint32_t n_work, uint32_t &n,
+                                            uint32_t &drawn, volatile int *abort_flag) {
+    int item = -1;
+    while (true) {
+        const uint32_t w = STATE_ONLY ? blockIdx.x + drawn++ * gridDim.x : (uint32_t)atomicAdd(p.hdr + kHdrTicket, 1);
+        if (w >= n_work) break;
+        Item it;
+        if (load_item(p, (int)w, STATE_ONLY, it) && it.len > 0) {
+            item = (int)w;
+            break;
+        }
+    }
+    const int slot = n % kItemRing;
+    if (n >= (uint32_t)kItemRing && !wait_bar(&s.item_empty[slot], par(n / kItemRing - 1), abort_flag, p.hdr))
+        return -2;
+    s.item_ring[slot] = item;
+    mbar_arrive(&s.item_full[slot]);
+    ++n;
+    return item;
+}
+
+// Other roles (one lane): the next item (-1: none left, -2: aborted).
+template <class Smem>
+__device__ __forceinline__ int take_item(Smem &s, uint32_t &n, volatile int *abort_flag, int32_t *hdr) {
+    const int slot = n % kItemRing;
+    if (!wait_bar(&s.item_full[slot], par(n / kItemRing), abort_flag, hdr)) return -2;
+    const int item = s.item_ring[slot];
+    mbar_arrive(&s.item_empty[slot]);
+    ++n;
+    return item;
+}
+
+// The same for a whole warp (lane 0 takes, every lane gets it).
+template <class Smem>
+__device__ __forceinline__ int take_item_warp(Smem &s, uint32_t &n, volatile int *abort_flag, int32_t *hdr,
+                                              int lane) {
+    int item = 0;
+    if (lane == 0) item = take_item(s, n, abort_flag, hdr);
+    return __shfl_sync(0xffffffffu, item, 0);
+}
+
+// The CTA's pieces in order across its items (used to look ahead).  One lane
+// draws or takes the items; the piece fields are that lane's.
+struct Cursor {
+    uint32_t n, drawn;
+    Item it;
+    Pieces pcs;
+    bool in_item, done;
+};
+template <bool PUBLISH, bool STATE_ONLY, class Smem>
+__device__ __forceinline__ bool cursor_next(Cursor &c, Smem &s, const FwdParams &p, uint32_t n_work, int Qi,
+                                            volatile int *abort_flag, int &t0, int &len, int64_t &ae) {
+    while (!c.done) {
+        if (c.in_item && c.pcs.next(t0, len, ae)) return true;
+        c.in_item = false;
+        const int w = PUBLISH ? publish_item<STATE_ONLY>(s, p, n_work, c.n, c.drawn, abort_flag)
+                              : take_item(s, c.n, abort_flag, p.hdr);
+        if (w < 0) {
+            c.done = true;
+            break;
+        }
+        if (!load_item(p, w, STATE_ONLY, c.it)) continue;
+        c.pcs = Pieces{c.it.abs0, c.it.abs0 + c.it.len, c.it.tok, Qi};
+        c.in_item = true;
+    }
     return false;
 }
 
@@ -292,31 +382,31 @@ __device__ __forceinline__ void write_h_copy16(TcSmem<P> &s, int n, int pcol0, c
 }
 
 // Barrier phases.  Every barrier completes once per piece of the CTA's running
-// piece count pc, once per stage use (x/z stages, y accumulator pairs:
-// pc / depth), or once per two pieces (cs_ready, indexed by pc & 1).  No waiter
+// piece count pc, or once per use of a ring slot (x/z stages, decay-value
+// slots, y accumulator pairs: pc / depth; work items: per item).  No waiter
 // can fall two phases behind: each barrier's next phase needs an arrival that
 // comes after every waiter of the current one.
 //
-// Per piece the MMA warp issues CB = C B^T, y_inter = C h^T, the state update
-// B^T (w x) -- after which B and C are released to the producer -- and last
+// Per piece the MMA warp issues CB = C B^T, y_inter = C h^T (after which C is
+// reloaded), the state update B^T (w x) (after which B is reloaded) and last
 // y_intra = M x, which waits for the mask.  G2 reads the state out (which
 // frees the state columns and the h^T copy for the next piece) before it runs
 // the epilogue, so the state chain never waits for a mask or an epilogue.
-__device__ __forceinline__ uint32_t par(uint32_t use) { return use & 1u; }
 
 template <int P, bool STATE_ONLY>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int Qi) {
     using Cfg = TcCfg<P>;
     using Smem = TcSmem<P>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // The first kernel of a forward rewinds the scan's work ticket.
+    if (STATE_ONLY && blockIdx.x == 0 && threadIdx.x == 0) p.hdr[kHdrTicket] = 0;
     // The tiles need 1024-byte alignment (swizzle atoms); the dynamic shared
     // window starts there on this architecture.  Refuse to run otherwise.
-    if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if ((smem_u32(tc_smem) & 1023u) != 0) {
         if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
         return;
     }
-    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    Smem &s = *reinterpret_cast<Smem *>(tc_smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &s.abort_flag;
     constexpr int kNS = Cfg::kNS, kNY = Cfg::kNY;
@@ -327,16 +417,27 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.full_x[i], 2);  // TMA bytes + the producer warp's dt stores
-            // x is released by the MMA that last reads it, plus G2 when y is staged in it
+            // x is released by the MMA that last reads it, plus G2 when it stages y in
+            // the x tile (G2 then also reads the decay values of the stage)
             mbar_init(&s.empty_x[i], 1 + (Cfg::kSepY ? 0 : kMathPerRole));
             mbar_init(&s.full_z[i], 1);
             mbar_init(&s.empty_z[i], kMathPerRole);
             mbar_init(&s.y_full[i], 1);
             mbar_init(&s.y_empty[i], kMathPerRole);
-            mbar_init(&s.cs_ready[i], kMathPerRole);
         }
-        mbar_init(&s.full_bc, 1);
-        mbar_init(&s.empty_bc, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s.full_cs[i], 1);
+            mbar_init(&s.empty_cs[i], kMathPerRole);
+        }
+        for (int i = 0; i < kItemRing; ++i) {
+            mbar_init(&s.item_full[i], 1);
+            // every role but the producer takes each item: MMA, G1 and G2 warps, loaders
+            mbar_init(&s.item_empty[i], 2 + 2 * kMathPerRole + (z_tile ? 1 : 0));
+        }
+        mbar_init(&s.full_b, 1);
+        mbar_init(&s.empty_b, 1);
+        mbar_init(&s.full_c, 1);
+        mbar_init(&s.empty_c, 1);
         mbar_init(&s.cb_full, 1);
         mbar_init(&s.m_full, kMathPerRole);
         mbar_init(&s.m_done, 1);
@@ -359,30 +460,47 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // Lane 0 issues the TMA loads; the whole warp stages each piece's dt (128
-        // strided bf16 values) into shared memory, loaded into registers one
-        // piece ahead so the staging never waits on global memory.
+        // Draws the work items.  Per piece lane 0 issues the x TMA and the whole
+        // warp turns the piece's 128 dt values (strided in HBM, loaded into
+        // registers two pieces ahead) into dt' and the cumulative decay, which
+        // it publishes beside the x tile.
         const uint16_t *__restrict__ dt16 = static_cast<const uint16_t *>(p.dt);
-        if (lane == 0) {
-            prefetch_tmap(&maps.x);
-        }
+        if (lane == 0) prefetch_tmap(&maps.x);
+        struct Ahead {
+            bool have;
+            int t0, len, head;
+            float dtb, Ah2;
+            uint16_t d[4];
+        };
+        Cursor cur{0, 0, Item{}, Pieces{}, false, false};
+        auto next_piece = [&](Ahead &a) {
+            int t0 = 0, len = 0, head = 0;
+            int64_t ae = 0;
+            bool have = false;
+            if (lane == 0) {
+                have = cursor_next<true, STATE_ONLY>(cur, s, p, n_work, Qi, abort_flag, t0, len, ae);
+                head = cur.it.head;
+            }
+            a.have = __shfl_sync(0xffffffffu, have, 0);
+            a.t0 = __shfl_sync(0xffffffffu, t0, 0);
+            a.len = __shfl_sync(0xffffffffu, len, 0);
+            a.head = __shfl_sync(0xffffffffu, head, 0);
+            a.dtb = a.have ? p.dt_bias[a.head] : 0.f;
+            a.Ah2 = a.have ? p.A[a.head] * kLog2e : 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                a.d[k] = 0;
+                if (a.have && lane * 4 + k < a.len) a.d[k] = dt16[(size_t)(a.t0 + lane * 4 + k) * p.H + a.head];
+            }
+        };
+        Ahead a0, a1, a2;
+        next_piece(a0);
+        next_piece(a1);
         uint32_t pc = 0;
         bool ok = true;
         const uint32_t xbytes = Cfg::kXBytes;
-        Cursor cur{blockIdx.x, Item{}, Pieces{}, false};
-        int t0 = 0, len = 0;
-        int64_t ae = 0;
-        bool have = cursor_next(cur, p, STATE_ONLY, Qi, n_work, t0, len, ae);
-        int head = cur.it.head;
-        uint16_t dtr[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (have && lane * 4 + k < len) dtr[k] = dt16[(size_t)(t0 + lane * 4 + k) * p.H + head];
-        while (ok && have) {
-            int nt0 = 0, nlen = 0;
-            int64_t nae = 0;
-            const bool nhave = cursor_next(cur, p, STATE_ONLY, Qi, n_work, nt0, nlen, nae);
-            const int nhead = cur.it.head;
+        while (ok && a0.have) {
+            next_piece(a2);  // its dt loads stay in flight for two pieces
             const int st = pc % kNS;
             bool good = true;
             if (lane == 0 && pc >= (uint32_t)kNS) good = wait_bar(&s.empty_x[st], par(pc / kNS - 1), abort_flag, p.hdr);
@@ -390,23 +508,41 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             if (lane == 0) {
                 mbar_arrive_expect_tx(&s.full_x[st], xbytes);
                 uint8_t *xs = s.x + st * Cfg::kXBytes;
-                for (int q = 0; q < kPB; ++q) tma_load_3d(xs + q * 16384, &maps.x, &s.full_x[st], q * 64, head, t0);
+                for (int q = 0; q < kPB; ++q) tma_load_3d(xs + q * 16384, &maps.x, &s.full_x[st], q * 64, a0.head, a0.t0);
             }
-            *reinterpret_cast<uint2 *>(&s.dt[st][lane * 4]) =
-                make_uint2((uint32_t)dtr[0] | ((uint32_t)dtr[1] << 16), (uint32_t)dtr[2] | ((uint32_t)dtr[3] << 16));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.full_x[st]);
-            // the next piece's dt, consumed one iteration later
+            // dt' = softplus(dt + dt_bias) and its inclusive cumulative decay
+            // dt' A (log2 units) over the piece; lane l holds rows 4l .. 4l+3.
+            const int cslot = pc % Cfg::kNC;
+            if (Cfg::kSepY && pc >= (uint32_t)Cfg::kNC) {
+                bool free_ok = true;
+                if (lane == 0) free_ok = wait_bar(&s.empty_cs[cslot], par(pc / Cfg::kNC - 1), abort_flag, p.hdr);
+                if (!__shfl_sync(0xffffffffu, free_ok, 0)) { ok = false; break; }
+            }
+            float dl[4], cl[4], run = 0.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                dtr[k] = 0;
-                if (nhave && lane * 4 + k < nlen) dtr[k] = dt16[(size_t)(nt0 + lane * 4 + k) * p.H + nhead];
+                dl[k] = lane * 4 + k < a0.len ? softplus_fast(__uint_as_float((uint32_t)a0.d[k] << 16) + a0.dtb) : 0.f;
+                run += dl[k] * a0.Ah2;
+                cl[k] = run;
             }
-            t0 = nt0;
-            len = nlen;
-            ae = nae;
-            head = nhead;
-            have = nhave;
+            float incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const float excl = incl - run;
+            *reinterpret_cast<float4 *>(&s.cs2[cslot][lane * 4]) =
+                make_float4(cl[0] + excl, cl[1] + excl, cl[2] + excl, cl[3] + excl);
+            *reinterpret_cast<float4 *>(&s.dtp[cslot][lane * 4]) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            if (lane == 31) s.cslast[cslot] = incl;
+            __syncwarp();
+            if (lane == 0) {
+                if (Cfg::kSepY) mbar_arrive(&s.full_cs[cslot]);
+                mbar_arrive(&s.full_x[st]);
+            }
+            a0 = a1;
+            a1 = a2;
             ++pc;
         }
         // Never leave a copy in flight: wait for the last issued loads.
@@ -421,17 +557,21 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             constexpr uint32_t i_y = idesc_bf16_f32(128, P, false, true);      // K-major A x MN-major B
             constexpr uint32_t i_s = idesc_bf16_f32(128, P, true, true);       // B^T (MN-major) x wx (MN-major)
             const uint32_t colS = Cfg::kSepS ? Cfg::kColS : Cfg::kColH;
-            uint32_t pc = 0;
+            uint32_t pc = 0, nit = 0;
             bool ok = true;
-            for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+            while (ok) {
+                const int w = take_item(s, nit, abort_flag, p.hdr);
+                if (w == -2) ok = false;
+                if (w < 0) break;
                 Item it;
-                if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+                if (!load_item(p, w, STATE_ONLY, it)) continue;
                 Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
                 int t0, len;
                 int64_t ae;
                 while (pcs.next(t0, len, ae)) {
                     const int st = pc % kNS, yb = pc % kNY;
-                    if (!wait_bar(&s.full_bc, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                    if (!wait_bar(&s.full_b, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                    if (!STATE_ONLY && !wait_bar(&s.full_c, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                     if (!STATE_ONLY) {
                         // CB = C B^T, once the previous piece's y_intra has read M out of these columns.
                         if (pc > 0 && !wait_bar(&s.m_done, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
@@ -460,6 +600,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                                        sdesc_sw128(hb + kk * 2048, 16384, 1024), i_y, (part | kk) != 0);
                             }
                         }
+                        mma_commit(&s.empty_c);  // C has no further reader in this piece
                     }
                     // state update: S = B^T (w x)  (or h^T += ... in place)
                     if (!wait_bar(&s.xd_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
@@ -475,7 +616,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                                    Cfg::kSepS ? (uint32_t)((part | kk) != 0) : 1u);
                     }
                     mma_commit(&s.s_full);
-                    mma_commit(&s.empty_bc);  // B and C have no further reader in this piece
+                    mma_commit(&s.empty_b);  // B has no further reader in this piece
                     if (STATE_ONLY) {
                         mma_commit(&s.empty_x[st]);
                     } else {
@@ -509,21 +650,23 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             }
         }
     } else if (warp < 10) {
-        // ------------------------------------------------------------ G1: scan, w x, mask
+        // ------------------------------------------------------------ G1: w x, mask
         // Eight warps, two per TMEM lane quadrant q = warp % 4; the pair splits
         // the columns (hf).  Thread r of a pair owns tile row / TMEM lane r.
         const int q = warp & 3;
         const int hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
-        uint32_t pc = 0;
+        uint32_t pc = 0, nit = 0;
         bool ok = true;
-        for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+        while (ok) {
+            const int w = take_item_warp(s, nit, abort_flag, p.hdr, lane);
+            if (w == -2) ok = false;
+            if (w < 0) break;
             Item it;
-            if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+            if (!load_item(p, w, STATE_ONLY, it)) continue;
             if (it.len == 0) continue;
             const int hh = it.head;
-            const float dtb = p.dt_bias[hh], Ah2 = p.A[hh] * kLog2e;
             const float Dh = (!STATE_ONLY && p.D) ? p.D[hh] : 0.f;
             Pieces pcs{it.abs0, it.abs0 + it.len, it.tok, Qi};
             int t0, len;
@@ -534,56 +677,14 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 int nt0 = 0, nlen = 0;
                 int64_t nae = 0;
                 const bool has_next = pcs.next(nt0, nlen, nae);
-                // ---- dt' and the in-piece inclusive cumulative decay (log2 units),
-                // from the dt the producer staged with this piece's x tile.
-                // Every math warp scans all 128 rows itself: no cross-warp prefix.
+                // ---- this piece's decay values, published by the producer with its x tile
                 if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
-                float dl[4], cl[4];
-                float run = 0.f;
-                {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(&s.dt[st][lane * 4]);
-                    const uint32_t rw[4] = {raw.x << 16, raw.x & 0xFFFF0000u, raw.y << 16, raw.y & 0xFFFF0000u};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = lane * 4 + k;
-                        dl[k] = row < len ? softplus_fast(__uint_as_float(rw[k]) + dtb) : 0.f;
-                        run += dl[k] * Ah2;
-                        cl[k] = run;
-                    }
-                }
-                float incl = run;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                const float excl = incl - run;
-                const float cs2_last = __shfl_sync(0xffffffffu, incl, 31);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cl[k] += excl;
-                if (hf == 0 && (lane >> 3) == q) {  // publish this quadrant's 32 rows
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        s.cs2[pc & 1][lane * 4 + k] = cl[k];
-                        s.dtp[pc & 1][lane * 4 + k] = dl[k];
-                    }
-                }
-                // own row r = 32q + lane lives in lane 8q + lane/4, slot lane%4;
-                // the quadrant's reference row 32q - 1 in lane 8q - 1, slot 3.
-                const int src_lane = 8 * q + (lane >> 2);
-                float cs2 = 0.f, d = 0.f;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float cv = __shfl_sync(0xffffffffu, cl[k], src_lane);
-                    const float dv = __shfl_sync(0xffffffffu, dl[k], src_lane);
-                    if ((lane & 3) == k) {
-                        cs2 = cv;
-                        d = dv;
-                    }
-                }
-                const float cs2_ref = __shfl_sync(0xffffffffu, cl[3], (8 * q + 31) & 31);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.cs_ready[pc & 1]);
+                const int cslot = pc % Cfg::kNC;
+                const float *cs2v = s.cs2[cslot];
+                const float *dv = s.dtp[cslot];
+                const float cs2 = cs2v[r], d = dv[r], cs2_last = s.cslast[cslot];
+                // the quadrant's reference row 32q - 1 (used below the diagonal only, q > 0)
+                const float cs2_ref = cs2v[(32 * q + 127) & 127];
                 // ---- w x (hi, lo) tiles, this warp's half of the columns; the
                 // previous state MMA must have read the tiles
                 if (pc > 0 && !wait_bar(&s.s_full, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
@@ -614,11 +715,8 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     // the diagonal (j < q) exp(cs_r - cs_s) = u_r v_s with both factors
                     // <= 1 around the reference row 32q - 1; the diagonal block is
                     // evaluated directly.
-                    if (!wait_bar(&s.cs_ready[pc & 1], par(pc >> 1), abort_flag, p.hdr)) { ok = false; break; }
                     if (!wait_bar(&s.cb_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
-                    const float *cs2v = s.cs2[pc & 1];
-                    const float *dv = s.dtp[pc & 1];
                     const float u_r = fast_exp2(cs2 - cs2_ref);
                     // 16-column group g = 2j + hf of every 32-column block j: both warps of
                     // the pair get half of the diagonal block and half of the rest.
@@ -689,14 +787,18 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         const int c0 = hf * kHalf;                // first column of this warp
         const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
-        uint32_t pc = 0;
+        uint32_t pc = 0, nit = 0;
         bool ok = true;
-        for (uint32_t w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+        while (ok) {
+            const int w = take_item_warp(s, nit, abort_flag, p.hdr, lane);
+            if (w == -2) ok = false;
+            if (w < 0) break;
             Item it;
-            if (!load_item(p, (int)w, STATE_ONLY, it)) continue;
+            if (!load_item(p, w, STATE_ONLY, it)) continue;
             const int hh = it.head;
-            const float dtb = p.dt_bias[hh], Ah2 = p.A[hh] * kLog2e;
-            // ---- entering state: initial slot (first segment) or the chained state
+            // ---- entering state: initial slot (first segment) or the chained state;
+            // src points at this head's (P, N) block.
+            const size_t head_off = (size_t)hh * P * 128;
             const float *src = nullptr;
             if (!STATE_ONLY) {
                 if (it.first_seg) {
@@ -705,39 +807,19 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         if (slot >= p.num_slots) {
                             if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
                         } else if (slot >= 0) {
-                            src = p.pool + (size_t)slot * slot_elems;
+                            src = p.pool + (size_t)slot * slot_elems + head_off;
                         }
                     }
                 } else {
-                    src = p.seg_state + (size_t)(it.seg - 1) * slot_elems;
+                    src = p.seg_state + (size_t)(it.seg - 1) * slot_elems + head_off;
                 }
-            }
-            if (!STATE_ONLY && it.len == 0) {
-                // Empty request: its final state is its initial state.
-                float *fd = p.final_states ? p.final_states + (size_t)it.req * slot_elems : nullptr;
-                float *fs = nullptr;
-                if (p.final_slots) {
-                    const int fslot = p.final_slots[it.req];
-                    if (fslot >= p.num_slots) {
-                        if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
-                    } else if (fslot >= 0) {
-                        fs = p.pool + (size_t)fslot * slot_elems;
-                    }
-                }
-                for (int pp = c0; pp < c0 + kHalf; ++pp) {
-                    const size_t e = ((size_t)hh * P + pp) * 128 + r;
-                    const float v = src ? src[e] : 0.f;
-                    if (fd) fd[e] = v;
-                    if (fs) fs[e] = v;
-                }
-                continue;
             }
             // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
 #pragma unroll 1
             for (int cs = c0; cs < c0 + kHalf; cs += 16) {
                 uint32_t v[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = src ? __float_as_uint(src[((size_t)hh * P + cs + k) * 128 + r]) : 0u;
+                for (int k = 0; k < 16; ++k) v[k] = src ? __float_as_uint(src[(size_t)(cs + k) * 128 + r]) : 0u;
                 tmem_st16(tl + Cfg::kColH + cs, v);
                 if (!STATE_ONLY) write_h_copy16<P>(s, r, cs, v);
             }
@@ -760,34 +842,17 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 int nt0 = 0, nlen = 0;
                 int64_t nae = 0;
                 const bool has_next = pcs.next(nt0, nlen, nae);
-                // ---- this warp's own scan of the piece (same arithmetic as G1)
-                if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
-                float run = 0.f, cl[4];
-                {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(&s.dt[st][lane * 4]);
-                    const uint32_t rw[4] = {raw.x << 16, raw.x & 0xFFFF0000u, raw.y << 16, raw.y & 0xFFFF0000u};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = lane * 4 + k;
-                        const float dk = row < len ? softplus_fast(__uint_as_float(rw[k]) + dtb) : 0.f;
-                        run += dk * Ah2;
-                        cl[k] = run;
-                    }
+                // ---- this piece's decay values, published by the producer
+                const int cslot = pc % Cfg::kNC;
+                if (Cfg::kSepY) {
+                    if (!wait_bar(&s.full_cs[cslot], par(pc / Cfg::kNC), abort_flag, p.hdr)) { ok = false; break; }
+                } else {
+                    if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                 }
-                float incl = run;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                const float cs2_last = __shfl_sync(0xffffffffu, incl, 31);
-                const float excl = incl - run;
-                float cs2 = 0.f;
-                const int src_lane = 8 * q + (lane >> 2);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float cv = __shfl_sync(0xffffffffu, cl[k] + excl, src_lane);
-                    if ((lane & 3) == k) cs2 = cv;
+                const float cs2 = s.cs2[cslot][r], cs2_last = s.cslast[cslot];
+                if (Cfg::kSepY) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.empty_cs[cslot]);
                 }
                 const float decay = fast_exp2(cs2_last);
                 decay_sum2 += cs2_last;
@@ -817,7 +882,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 if (!STATE_ONLY) {
                     if (p.chunk_states && (ae % p.Q == 0 || req_end)) {
                         const int64_t row = (int64_t)p.req_first_chunk[it.req] + (ae - 1) / p.Q - it.req_s / p.Q;
-                        dsts[nd++] = p.chunk_states + (size_t)row * slot_elems;
+                        dsts[nd++] = p.chunk_states + (size_t)row * slot_elems + head_off;
                     }
                     if (p.block_table && p.block_size > 0 && ae % p.block_size == 0) {
                         const int64_t col = ae / p.block_size - 1;
@@ -828,23 +893,23 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                             if (bslot >= p.num_slots) {
                                 if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_BLOCK_SLOT);
                             } else if (bslot >= 0) {
-                                dsts[nd++] = p.pool + (size_t)bslot * slot_elems;
+                                dsts[nd++] = p.pool + (size_t)bslot * slot_elems + head_off;
                             }
                         }
                     }
                     if (req_end) {
-                        if (p.final_states) dsts[nd++] = p.final_states + (size_t)it.req * slot_elems;
+                        if (p.final_states) dsts[nd++] = p.final_states + (size_t)it.req * slot_elems + head_off;
                         if (p.final_slots) {
                             const int fslot = p.final_slots[it.req];
                             if (fslot >= p.num_slots) {
                                 if (r == 0 && hf == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
                             } else if (fslot >= 0) {
-                                dsts[nd++] = p.pool + (size_t)fslot * slot_elems;
+                                dsts[nd++] = p.pool + (size_t)fslot * slot_elems + head_off;
                             }
                         }
                     }
                 } else if (seg_end) {
-                    dsts[nd++] = p.seg_state + (size_t)it.seg * slot_elems;
+                    dsts[nd++] = p.seg_state + (size_t)it.seg * slot_elems + head_off;
                     if (r == 0 && hf == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = fast_exp2(decay_sum2);
                 }
                 const bool need_copy = !STATE_ONLY && !seg_end;
@@ -879,7 +944,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                         for (int g2 = 0; g2 < 2; ++g2) {
                             for (int dd = 0; dd < nd; ++dd) {
-                                float *dst = dsts[dd] + ((size_t)hh * P + cs + 16 * g2) * 128 + r;
+                                float *dst = dsts[dd] + (size_t)(cs + 16 * g2) * 128 + r;
 #pragma unroll
                                 for (int k = 0; k < 16; ++k) dst[(size_t)k * 128] = __uint_as_float(v[g2][k]);
                             }
@@ -977,34 +1042,41 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         if (lane == 0) {
             prefetch_tmap(&maps.b);
             if (!STATE_ONLY) prefetch_tmap(&maps.c);
-            const uint32_t bcbytes = kRows * 128 * 2 * (STATE_ONLY ? 1 : 2);
-            Cursor cur{blockIdx.x, Item{}, Pieces{}, false};
+            // C is released after y_inter, B after the state update: C first.
+            constexpr uint32_t tbytes = kRows * 128 * 2;
+            Cursor cur{0, 0, Item{}, Pieces{}, false, false};
             int t0 = 0, len = 0;
             int64_t ae = 0;
             uint32_t pc = 0;
-            while (cursor_next(cur, p, STATE_ONLY, Qi, n_work, t0, len, ae)) {
+            while (cursor_next<false, STATE_ONLY>(cur, s, p, n_work, Qi, abort_flag, t0, len, ae)) {
                 const int g = cur.it.head / (p.H / p.G);
-                if (pc >= 1 && !wait_bar(&s.empty_bc, par(pc - 1), abort_flag, p.hdr)) break;
-                mbar_arrive_expect_tx(&s.full_bc, bcbytes);
-                tma_load_3d(s.b, &maps.b, &s.full_bc, 0, g, t0);
-                tma_load_3d(s.b + 16384, &maps.b, &s.full_bc, 64, g, t0);
                 if (!STATE_ONLY) {
-                    tma_load_3d(s.c, &maps.c, &s.full_bc, 0, g, t0);
-                    tma_load_3d(s.c + 16384, &maps.c, &s.full_bc, 64, g, t0);
+                    if (pc >= 1 && !wait_bar(&s.empty_c, par(pc - 1), abort_flag, p.hdr)) break;
+                    mbar_arrive_expect_tx(&s.full_c, tbytes);
+                    tma_load_3d(s.c, &maps.c, &s.full_c, 0, g, t0);
+                    tma_load_3d(s.c + 16384, &maps.c, &s.full_c, 64, g, t0);
                 }
+                if (pc >= 1 && !wait_bar(&s.empty_b, par(pc - 1), abort_flag, p.hdr)) break;
+                mbar_arrive_expect_tx(&s.full_b, tbytes);
+                tma_load_3d(s.b, &maps.b, &s.full_b, 0, g, t0);
+                tma_load_3d(s.b + 16384, &maps.b, &s.full_b, 64, g, t0);
                 ++pc;
             }
-            if (pc > 0) mbar_wait(&s.full_bc, par(pc - 1), kWaitNs);
+            // Never leave a copy in flight.
+            if (pc > 0) {
+                mbar_wait(&s.full_b, par(pc - 1), kWaitNs);
+                if (!STATE_ONLY) mbar_wait(&s.full_c, par(pc - 1), kWaitNs);
+            }
         }
     } else {
         // ------------------------------------------------------------ z loader
         if (lane == 0 && z_tile) {
             prefetch_tmap(&maps.z);
-            Cursor cur{blockIdx.x, Item{}, Pieces{}, false};
+            Cursor cur{0, 0, Item{}, Pieces{}, false, false};
             int t0 = 0, len = 0;
             int64_t ae = 0;
             uint32_t pc = 0;
-            while (cursor_next(cur, p, STATE_ONLY, Qi, n_work, t0, len, ae)) {
+            while (cursor_next<false, STATE_ONLY>(cur, s, p, n_work, Qi, abort_flag, t0, len, ae)) {
                 const int st = pc % kNS;
                 if (pc >= (uint32_t)kNS && !wait_bar(&s.empty_z[st], par(pc / kNS - 1), abort_flag, p.hdr)) break;
                 mbar_arrive_expect_tx(&s.full_z[st], Cfg::kXBytes);
@@ -1023,21 +1095,43 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     }
 }
 
-// Chains the segment end states of each request:
+// Per (request, head): chains the segment end states of a long request,
 //   h <- initial state;  for every segment k but the last:
-//   h <- decay_k h + S_k  and store it in slot k (= entering state of segment k+1).
+//   h <- decay_k h + S_k  and store it in slot k (= entering state of segment k+1),
+// and writes an empty request's final state (its initial state).
 template <int P>
 __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
     const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     if (p.hdr[kHdrSegs] == 0 || i >= p.R) return;
     const int first = p.req_first_seg[i], cnt = p.req_first_seg[i + 1] - first;
-    if (cnt <= 1) return;
     const size_t pn = (size_t)P * 128, slot_elems = (size_t)p.H * pn;
     const float *init = nullptr;
     if (p.init_slots) {
         const int slot = p.init_slots[i];
         if (slot >= 0 && slot < p.num_slots) init = p.pool + (size_t)slot * slot_elems + hh * pn;
     }
+    if (p.segs[first].len == 0) {
+        // An empty request: its final state is its initial state.
+        if (threadIdx.x == 0 && p.init_slots && p.init_slots[i] >= p.num_slots)
+            atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
+        float *fd = p.final_states ? p.final_states + (size_t)i * slot_elems + hh * pn : nullptr;
+        float *fs = nullptr;
+        if (p.final_slots) {
+            const int fslot = p.final_slots[i];
+            if (fslot >= p.num_slots) {
+                if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
+            } else if (fslot >= 0) {
+                fs = p.pool + (size_t)fslot * slot_elems + hh * pn;
+            }
+        }
+        for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
+            const float4 v = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (fd) *reinterpret_cast<float4 *>(fd + e) = v;
+            if (fs) *reinterpret_cast<float4 *>(fs + e) = v;
+        }
+        return;
+    }
+    if (cnt <= 1) return;
     for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
         float4 h = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < cnt - 1; ++k) {

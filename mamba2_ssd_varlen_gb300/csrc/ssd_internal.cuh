@@ -15,7 +15,8 @@ constexpr int kHdrInts = 64;                             // header words at the 
 constexpr int kHdrErr = 0;       // device error bits (SSD_DEVERR_*)
 constexpr int kHdrChunks = 1;    // export rows of the batch
 constexpr int kHdrSegs = 2;      // work segments of the batch
-constexpr int kHdrTicket = 3;    // reserved for in-order work tickets
+constexpr int kHdrTicket = 3;    // next work item of the scan kernel (a ticket counter)
+constexpr int kHdrTimeoutAt = 4; // words 4-6: where the first timed-out wait of a launch was
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {

@@ -99,6 +99,7 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
         hdr[kHdrChunks] = bad ? 0 : carry_c;
         hdr[kHdrSegs] = bad ? 0 : carry_s;
         hdr[kHdrTicket] = 0;
+        hdr[kHdrTimeoutAt] = hdr[kHdrTimeoutAt + 1] = hdr[kHdrTimeoutAt + 2] = 0;
     }
     if (bad) return;  // forward kernels see zero segments and write nothing
     __syncthreads();

@@ -55,7 +55,8 @@ def run_full(prob, check_pool=True):
     pool_before = None if prob["state_pool"] is None else prob["state_pool"].clone()
     call = m.run(prob)
     torch.cuda.synchronize()
-    assert call.status() == 0
+    hdr = call.workspace[:32].view(torch.int32).cpu().tolist()
+    assert call.status() == 0, f"device error; header words 0-7: {hdr}"
     assert_close(host(call.y), ref["y"], "y")
     if call.final_states is not None:
         assert_close(host(call.final_states), ref["final_states"], "final_states")
@@ -97,6 +98,19 @@ def test_long_requests_span_several_segments(P):
                           export_chunks=True, block_size=1024)
     prob = workloads.make_problem(spec, seed=31, device="cuda", lengths=[5000, 4096, 3],
                                   num_computed=[1000, 0, 2047], canary=1.5)
+    run_full(prob)
+
+
+@pytest.mark.parametrize("P,Q", [(64, 64), (128, 128)])
+def test_more_items_than_sms(P, Q):
+    # More (segment, head) work items than SMs, so CTAs draw several items
+    # each from the work ticket; initial states, a resume offset, chunk exports
+    # and block checkpoints on every item.
+    spec = workloads.Spec("many", H=64, P=P, N=128, G=4, chunk_size=Q, dtype="bf16",
+                          has_D=True, has_z=True, init="all", pool_slots=32, final_slots=True,
+                          export_chunks=True, block_size=256)
+    prob = workloads.make_problem(spec, seed=41 + P, device="cuda", lengths=[1000, 900, 1100, 1001],
+                                  num_computed=[0, 64, 5, 1000], canary=2.5)
     run_full(prob)
 
 
