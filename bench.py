@@ -33,7 +33,10 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "uniform_8x2048"
 METRIC = "SSD varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
-KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc"]
+# The files the dominant (scan) kernel is compiled from; its DRAM-traffic figure in
+# profiles/traffic.txt is valid only for this exact source.
+KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
+                  "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh", "include/ssd_varlen.h"]
 
 
 def env_rank():
@@ -53,12 +56,9 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for d in KERNEL_SOURCES:
-        full = os.path.join(ROOT, d)
-        for name in sorted(os.listdir(full)):
-            if name.endswith((".cu", ".cuh")):
-                h.update(name.encode())
-                h.update(open(os.path.join(full, name), "rb").read())
+    for rel in KERNEL_SOURCES:
+        h.update(os.path.basename(rel).encode())
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
     return h.hexdigest()[:16]
 
 

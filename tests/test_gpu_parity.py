@@ -55,8 +55,8 @@ def run_full(prob, check_pool=True):
     pool_before = None if prob["state_pool"] is None else prob["state_pool"].clone()
     call = m.run(prob)
     torch.cuda.synchronize()
-    hdr = call.workspace[:32].view(torch.int32).cpu().tolist()
-    assert call.status() == 0, f"device error; header words 0-7: {hdr}"
+    hdr = call.workspace[:224].view(torch.int32).cpu().tolist()
+    assert call.status() == 0, f"device error; header words 0-55: {hdr}"
     assert_close(host(call.y), ref["y"], "y")
     if call.final_states is not None:
         assert_close(host(call.final_states), ref["final_states"], "final_states")
