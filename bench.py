@@ -33,10 +33,11 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "uniform_8x2048"
 METRIC = "SSD varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
+DECODE_METRIC = "SSD decode step tokens/s per layer (bf16, 1×GB300); % of roofline"
 # The files the dominant (scan) kernel is compiled from; its DRAM-traffic figure in
 # profiles/traffic.txt is valid only for this exact source.
 KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
-                  "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh", "include/ssd_varlen.h"]
+                  "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"]
 
 
 def env_rank():
@@ -213,10 +214,45 @@ def cpu_baseline(prob, max_seconds=30.0):
                       f"fp64 token-by-token recurrence, {dt:.2f} s"}
 
 
+def run_reference_decode(args, world):
+    """The oracle on the machine's host cores for a decode step: a bounded sample of
+    whole requests (all heads) per timed step."""
+    import oracle
+    import workloads
+    prob = workloads.make_decode_problem(args.config, device="cpu")
+    R, T, H = prob["R"], prob["T"], prob["H"]
+    n_req = max(1, min(R, 8))
+    sel = list(range(n_req))
+    o = workloads.to_oracle_decode(prob, requests=sel)
+    tok = int(sum(prob["windows"][i] for i in sel))
+    ncores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.decode(o, n_threads=ncores)
+    vals = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(o, n_threads=ncores)
+        vals.append(tok / (time.perf_counter() - t0))
+    value = sorted(vals)[len(vals) // 2]
+    sample = f"{n_req} of {R} requests ({tok} tokens, all {H} heads), fp64 token-by-token recurrence"
+    line = {"metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": T / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.config, "T": T, "R": R, "H": H, "P": prob["P"], "N": prob["N"],
+                       "G": prob["G"], "window": max(prob["windows"])},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     import workloads
     if rank != 0:
         return
+    if args.config in workloads.DECODE_CONFIGS:
+        return run_reference_decode(args, world)
     prob = workloads.make_problem(args.config, device="cpu")
     # Each step: a bounded sample (whole requests) sized so the run stays within minutes.
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
@@ -240,6 +276,107 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def decode_cost(prob):
+    """Bytes one decode step must move: the read anchors' states, the states written
+    to write anchors (fp32), and x, z, y, B, C, dt of the window tokens."""
+    T, H, P, N, G = prob["T"], prob["H"], prob["P"], prob["N"], prob["G"]
+    el = 4 if prob["dtype"] == "fp32" else 2
+    tok_bytes = el * (T * H * P * (2 + (prob["z"] is not None)) + 2 * T * G * N + T * H)
+    st = H * P * N * 4
+    win = prob["windows"]
+    reads = sum(1 for i, s in enumerate(prob["read_slots"].tolist()) if s >= 0 and win[i] > 0)
+    writes = int((prob["write_slots"] >= 0).sum().item())
+    return {"bytes": tok_bytes + st * (reads + writes), "token_bytes": tok_bytes,
+            "state_bytes": st * (reads + writes), "flops": T * H * P * N * 4}
+
+
+def run_decode_bench(args, rank, local_rank, world, dist):
+    """The decode / speculative-decode step (ssd_varlen_decode), timed like the forward."""
+    import torch
+    import mamba2_ssd_varlen_gb300 as m
+    import workloads
+    peaks = load_peaks()
+    prob = workloads.make_decode_problem(args.config, device="cuda")
+    call = m.DecodeCall(prob)
+    stream = torch.cuda.current_stream()
+    cost = decode_cost(prob)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert call.status() == 0, "device error during warm-up"
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert call.status() == 0, "device error during the timed region"
+    k_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    k_avg = sum(k_ms) / K
+    ms_per_step = total_ms / K
+    T = prob["T"]
+    # End to end: the step's inputs (tokens, anchors) host -> device and y back;
+    # the state pool stays resident in HBM (it is the cache the anchors index).
+    host_in = {k: prob[k].cpu().pin_memory() for k in ("x", "dt", "B", "C", "z", "cu_seqlens", "read_slots",
+                                                     "write_slots") if prob.get(k) is not None}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    y_host = torch.empty(call.y.shape, dtype=call.y.dtype, pin_memory=True)
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step():
+        for k_, t_ in host_in.items():
+            prob[k_].copy_(t_, non_blocking=True)
+        call()
+        y_host.copy_(call.y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.e2e_steps
+    achieved = cost["bytes"] / (k_avg / 1e3) / 1e9
+    line = {"metric": DECODE_METRIC, "value": T * world / (ms_per_step / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if prob["dtype"] == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": args.config, "T": T, "R": prob["R"], "H": prob["H"], "P": prob["P"],
+                       "N": prob["N"], "G": prob["G"], "window": max(prob["windows"]),
+                       "state_writes": int((prob["write_slots"] >= 0).sum().item()),
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "state traffic larger than L2 (no flush)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"], "algorithmic_bytes": cost["bytes"],
+                         "kernel": "ssd_varlen_decode", "kernel_ms_avg": round(k_avg, 5)},
+            "gpu_launches": K, "clocks": clocks,
+            "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -267,6 +404,11 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     m.load_library()
+    if args.config in workloads.DECODE_CONFIGS:
+        run_decode_bench(args, rank, local_rank, world, dist)
+        if dist:
+            dist.destroy_process_group()
+        return
     peaks = load_peaks()
     prob = workloads.make_problem(args.config, device="cuda")
     call = m.Call(prob)

@@ -202,6 +202,49 @@ int ssd_varlen_forward_static(const ssd_dims *dims, const int32_t *cu_seqlens, c
                               const ssd_inputs *in, const ssd_outputs *out, cudaStream_t stream,
                               ssd_plan *plan_out);
 
+/* ---- Decode and speculative-decode step with dual read/write anchors -----
+ * "Automatic prefix caching for GDN hybrid models (mamba_cache_mode=all) with
+ * MTP speculative decoding", Purpose (the Kernels/layers bullet): the decode
+ * kernels take dual read/write state anchors, so that a speculative-decode step
+ * reads the previous step's running state from one slot while writing the
+ * current step's states to others.  The same recurrence as the forward above,
+ * for short per-request windows:
+ *
+ *   Request i owns tokens [cu_seqlens[i], cu_seqlens[i+1]) of the packed batch:
+ *   one token for a plain decode step, 1 + the number of draft tokens for a
+ *   speculative step (0 tokens: nothing is read or written for it).  For every
+ *   head h its state starts from state_pool[read_slots[i]] (the read anchor;
+ *   read_slots[i] < 0 starts from zeros) and advances token by token; y of each
+ *   token is written, and the state after token t goes to
+ *   state_pool[write_slots[t]] when write_slots[t] >= 0 (the write anchors:
+ *   the state after every draft position can be kept, so the step after
+ *   verification reads the one after the last accepted token).
+ *
+ * dims: T, R, H, P, N, G, dtype, num_slots (>= 1) as above; chunk_size,
+ * block_size and block_table_width are not used.  P * N must be at most 16384
+ * and N a power of two in [16, 256] (SSD_ERR_UNSUPPORTED otherwise).  A write
+ * slot must not be a slot read in the same call.  Layouts as above; write_slots
+ * is (T) int32 and nullable (no state written), z and D are nullable.
+ * device_err (one int32 in device memory, required) receives SSD_DEVERR_* bits
+ * (CU_SEQLENS, INIT_SLOT for a read slot >= num_slots, FINAL_SLOT for a write
+ * slot >= num_slots); the caller clears it.  Launches one kernel on `stream`;
+ * allocates nothing. */
+typedef struct ssd_decode_io {
+    const void *x, *dt;         /* (T,H,P), (T,H) in dims.dtype */
+    const float *dt_bias, *A;   /* (H) */
+    const void *B, *C;          /* (T,G,N) in dims.dtype */
+    const float *D;             /* (H) or NULL */
+    const void *z;              /* (T,H,P) or NULL */
+    float *state_pool;          /* (num_slots,H,P,N) fp32, read and written */
+    const int32_t *read_slots;  /* (R) read anchor per request, < 0 = zero state */
+    const int32_t *write_slots; /* (T) write anchor per token, < 0 = none; or NULL */
+    void *y;                    /* (T,H,P) in dims.dtype */
+    int32_t *device_err;        /* one int32, OR-ed with SSD_DEVERR_* bits */
+} ssd_decode_io;
+
+int ssd_varlen_decode(const ssd_dims *dims, const int32_t *cu_seqlens, const ssd_decode_io *io,
+                      cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

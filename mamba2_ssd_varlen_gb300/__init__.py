@@ -13,6 +13,7 @@ The functions keep the C names:
   ssd_varlen_status(plan)                          -> device error bits
   ssd_varlen_strerror(code)                        -> text
   ssd_varlen_forward_static(...)   (C only: forward without a caller workspace)
+  ssd_varlen_decode(dims, cu_seqlens, io)        (decode / speculative-decode step)
 and ``run(...)`` wires a whole call from torch tensors (tests and bench use it).
 """
 from __future__ import annotations
@@ -36,7 +37,7 @@ STATUS = {
 }
 EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
             "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror",
-            "ssd_varlen_forward_static"]
+            "ssd_varlen_forward_static", "ssd_varlen_decode"]
 # Size of the library-owned scratch array used by ssd_varlen_forward_static.
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -65,6 +66,12 @@ class ssd_inputs(ctypes.Structure):
 class ssd_outputs(ctypes.Structure):
     _fields_ = [("y", c_vp), ("final_states", c_vp), ("final_slots", c_vp),
                 ("chunk_states", c_vp), ("block_table", c_vp)]
+
+
+class ssd_decode_io(ctypes.Structure):
+    _fields_ = [("x", c_vp), ("dt", c_vp), ("dt_bias", c_vp), ("A", c_vp), ("B", c_vp), ("C", c_vp),
+                ("D", c_vp), ("z", c_vp), ("state_pool", c_vp), ("read_slots", c_vp),
+                ("write_slots", c_vp), ("y", c_vp), ("device_err", c_vp)]
 
 
 class SsdError(RuntimeError):
@@ -103,6 +110,8 @@ def load_library():
                                               ctypes.POINTER(ssd_inputs), ctypes.POINTER(ssd_outputs),
                                               c_vp, ctypes.POINTER(ssd_plan)]
     lib.ssd_varlen_forward_static.restype = ctypes.c_int
+    lib.ssd_varlen_decode.argtypes = [ctypes.POINTER(ssd_dims), c_vp, ctypes.POINTER(ssd_decode_io), c_vp]
+    lib.ssd_varlen_decode.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -240,3 +249,48 @@ class Call:
 def run(prob: dict, **kw) -> Call:
     """Plan and run one call on the current stream; returns the Call (outputs on it)."""
     return Call(prob, **kw)()
+
+
+def ssd_varlen_decode(dims: ssd_dims, cu_seqlens, io: "ssd_decode_io", stream=None):
+    rc = load_library().ssd_varlen_decode(ctypes.byref(dims), _ptr(cu_seqlens), ctypes.byref(io),
+                                          _stream(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_decode")
+
+
+class DecodeCall:
+    """One decode / speculative-decode step over a problem from workloads.make_decode_problem:
+    the output y and the device error word, and the pre-built argument structs."""
+
+    def __init__(self, prob: dict, stream=None):
+        import torch
+        self.prob = prob
+        x = prob["x"]
+        T, H, P = x.shape
+        G, N = prob["B"].shape[1], prob["B"].shape[2]
+        R = prob["cu_seqlens"].shape[0] - 1
+        dtype = DTYPE_F32 if x.dtype == torch.float32 else DTYPE_BF16
+        pool = prob["state_pool"]
+        self.dims = make_dims(T, R, H, P, N, G, 0, dtype, num_slots=pool.shape[0])
+        self.y = torch.empty_like(x)
+        self.err = torch.zeros(4, dtype=torch.int32, device=x.device)
+        self.io = ssd_decode_io(_ptr(x), _ptr(prob["dt"]), _ptr(prob["dt_bias"]), _ptr(prob["A"]),
+                                _ptr(prob["B"]), _ptr(prob["C"]), _ptr(prob.get("D")), _ptr(prob.get("z")),
+                                _ptr(pool), _ptr(prob["read_slots"]), _ptr(prob.get("write_slots")),
+                                _ptr(self.y), _ptr(self.err))
+        self.stream = stream
+
+    def __call__(self):
+        ssd_varlen_decode(self.dims, self.prob["cu_seqlens"], self.io, self.stream)
+        return self
+
+    def status(self) -> int:
+        """Device error bits of the calls so far (synchronises), then clears them."""
+        v = int(self.err[0].item())
+        self.err.zero_()
+        return v
+
+
+def run_decode(prob: dict, **kw) -> DecodeCall:
+    """One decode step on the current stream; returns the DecodeCall (y on it, pool updated)."""
+    return DecodeCall(prob, **kw)()

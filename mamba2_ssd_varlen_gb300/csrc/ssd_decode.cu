@@ -1,0 +1,235 @@
+// ssd_decode.cu -- decode and speculative-decode step with dual read/write
+// state anchors ("Automatic prefix caching for GDN hybrid models
+// (mamba_cache_mode=all) with MTP speculative decoding", Purpose, the
+// Kernels/layers bullet: the decode kernels read the previous step's running
+// state from one slot while writing the current step's states to others).
+//
+// The same recurrence as the forward, for short per-request windows:
+//   h   <- state_pool[read_slots[i]]  (zeros when the slot is < 0)
+//   for each token t of request i:
+//       dt' = softplus(dt[t,h] + dt_bias[h])
+//       h   = exp(dt' A[h]) h + dt' x[t,h,:] (outer) B[t,g,:]
+//       y[t,h,:] = (h C[t,g,:] + D[h] x[t,h,:]) * silu(z[t,h,:])
+//       state_pool[write_slots[t]] <- h   when write_slots[t] >= 0
+//
+// One CTA of 256 threads per (request, head).  The (P, N) fp32 state lives in
+// registers: thread k owns KV consecutive elements of one state row p (KV
+// divides N, the N / KV threads of a row are adjacent lanes), so the state is
+// read once and each write anchor is one coalesced vector store; the row's
+// C.h dot product is a shuffle reduction over its lanes.  The step is bound by
+// the state traffic (4 P N bytes read, 4 P N per written anchor).
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kDecThreads = 256;
+
+struct DecParams {
+    int64_t T;
+    int32_t R, H, P, N, G, num_slots;
+    const int32_t *cu;
+    ssd_decode_io io;
+};
+
+template <typename T>
+__device__ __forceinline__ float ld_val(const void *base, size_t i) {
+    return to_f32(static_cast<const T *>(base)[i]);
+}
+
+// KV consecutive values of a bf16 or fp32 row, from 16-byte aligned storage
+// when KV allows, into fp32.
+template <typename T, int KV>
+__device__ __forceinline__ void load_vec(const T *src, float (&dst)[KV]) {
+    if constexpr (sizeof(T) == 2 && KV % 8 == 0) {
+#pragma unroll
+        for (int j = 0; j < KV; j += 8) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(src + j);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                dst[j + 2 * e] = __uint_as_float(w[e] << 16);
+                dst[j + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        }
+    } else if constexpr (sizeof(T) == 4 && KV % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < KV; j += 4) {
+            const float4 q = *reinterpret_cast<const float4 *>(src + j);
+            dst[j] = q.x;
+            dst[j + 1] = q.y;
+            dst[j + 2] = q.z;
+            dst[j + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < KV; ++j) dst[j] = to_f32(src[j]);
+    }
+}
+
+template <int KV>
+__device__ __forceinline__ void load_state(const float *src, float (&h)[KV]) {
+    if constexpr (KV % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < KV; j += 4) {
+            const float4 q = *reinterpret_cast<const float4 *>(src + j);
+            h[j] = q.x;
+            h[j + 1] = q.y;
+            h[j + 2] = q.z;
+            h[j + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < KV; ++j) h[j] = src[j];
+    }
+}
+
+template <int KV>
+__device__ __forceinline__ void store_state(float *dst, const float (&h)[KV]) {
+    if constexpr (KV % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < KV; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(h[j], h[j + 1], h[j + 2], h[j + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < KV; ++j) dst[j] = h[j];
+    }
+}
+
+template <typename T, int KV>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ DecParams p) {
+    const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
+    const int g = hh / (p.H / p.G);
+    const int rowlanes = p.N / KV;                   // threads per state row (power of 2, <= 32)
+    const int e0 = threadIdx.x * KV;                 // first state element of this thread
+    const bool active = e0 < p.P * p.N;
+    const int pr = active ? e0 / p.N : 0;            // state row p
+    const int n0 = e0 % p.N;                         // first column n
+    const size_t pn = (size_t)p.P * p.N, slot_elems = (size_t)p.H * pn;
+    const ssd_decode_io &io = p.io;
+
+    const int64_t a = p.cu[i], b = p.cu[i + 1];
+    if (b < a || a < 0 || b > p.T || (i == 0 && a != 0) || (i == p.R - 1 && b != p.T)) {
+        if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_CU_SEQLENS);
+        return;
+    }
+    if (b == a) return;  // an empty window reads and writes nothing
+
+    float h[KV];
+    const int rs = io.read_slots[i];
+    if (rs >= p.num_slots) {
+        if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_INIT_SLOT);
+    }
+    if (active && rs >= 0 && rs < p.num_slots) {
+        load_state<KV>(io.state_pool + (size_t)rs * slot_elems + hh * pn + e0, h);
+    } else {
+#pragma unroll
+        for (int j = 0; j < KV; ++j) h[j] = 0.f;
+    }
+    const float dtb = io.dt_bias[hh], Ah = io.A[hh];
+    const float Dh = io.D ? io.D[hh] : 0.f;
+    const T *Bv = static_cast<const T *>(io.B);
+    const T *Cv = static_cast<const T *>(io.C);
+    for (int64_t t = a; t < b; ++t) {
+        const float dtp = softplus_f32(ld_val<T>(io.dt, (size_t)t * p.H + hh) + dtb);
+        const float decay = expf(dtp * Ah);
+        const size_t xi = ((size_t)t * p.H + hh) * p.P + pr;
+        const float xv = active ? ld_val<T>(io.x, xi) : 0.f;
+        const float coef = dtp * xv;
+        float acc = 0.f;
+        if (active) {
+            float bv[KV], cv[KV];
+            const size_t bc = ((size_t)t * p.G + g) * p.N + n0;
+            load_vec<T, KV>(Bv + bc, bv);
+            load_vec<T, KV>(Cv + bc, cv);
+#pragma unroll
+            for (int j = 0; j < KV; ++j) {
+                h[j] = fmaf(decay, h[j], coef * bv[j]);
+                acc = fmaf(cv[j], h[j], acc);
+            }
+        }
+        // the row's C.h over its rowlanes adjacent lanes
+        for (int o = rowlanes >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (active && n0 == 0) {
+            float yv = fmaf(Dh, xv, acc);
+            if (io.z) yv *= silu_f32(ld_val<T>(io.z, xi));
+            static_cast<T *>(io.y)[xi] = from_f32<T>(yv);
+        }
+        const int ws = io.write_slots ? io.write_slots[t] : -1;
+        if (ws >= p.num_slots) {
+            if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_FINAL_SLOT);
+        } else if (ws >= 0 && active) {
+            store_state<KV>(io.state_pool + (size_t)ws * slot_elems + hh * pn + e0, h);
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_decode_t(const DecParams &p, int kv, cudaStream_t stream) {
+    const dim3 grid((unsigned)((int64_t)p.R * p.H)), block(kDecThreads);
+    switch (kv) {
+        case 1: decode_kernel<T, 1><<<grid, block, 0, stream>>>(p); break;
+        case 2: decode_kernel<T, 2><<<grid, block, 0, stream>>>(p); break;
+        case 4: decode_kernel<T, 4><<<grid, block, 0, stream>>>(p); break;
+        case 8: decode_kernel<T, 8><<<grid, block, 0, stream>>>(p); break;
+        case 16: decode_kernel<T, 16><<<grid, block, 0, stream>>>(p); break;
+        case 32: decode_kernel<T, 32><<<grid, block, 0, stream>>>(p); break;
+        case 64: decode_kernel<T, 64><<<grid, block, 0, stream>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// State elements per thread: the smallest power of two that spreads the (P, N)
+// state over the CTA with a row split over at most 32 adjacent lanes.
+int pick_kv(int P, int N) {
+    const int64_t elems = (int64_t)P * N;
+    for (int kv = 1; kv <= 64; kv <<= 1) {
+        if (N % kv != 0 || N / kv > 32) continue;
+        if (elems <= (int64_t)kDecThreads * kv) return kv;
+    }
+    return 0;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" int ssd_varlen_decode(const ssd_dims *d, const int32_t *cu_seqlens, const ssd_decode_io *io,
+                                 cudaStream_t stream) {
+    if (!d || !cu_seqlens || !io) return SSD_ERR_NULL;
+    if (d->reserved != 0) return SSD_ERR_DIMS;
+    if (d->T < 0 || d->T > 0x7fffffffLL || d->R < 1 || d->H < 1 || d->P < 1 || d->N < 1 || d->G < 1 ||
+        d->num_slots < 1 || d->H > 65535 || (int64_t)d->R * d->H > 0x7fffffffLL)
+        return SSD_ERR_DIMS;
+    if (d->H % d->G != 0) return SSD_ERR_GROUPS;
+    if (d->dtype != SSD_DTYPE_BF16 && d->dtype != SSD_DTYPE_F32) return SSD_ERR_DTYPE;
+    if ((d->N & (d->N - 1)) != 0 || d->N < 16 || d->N > 256) return SSD_ERR_UNSUPPORTED;
+    const int kv = pick_kv(d->P, d->N);
+    if (kv == 0) return SSD_ERR_UNSUPPORTED;
+    if (!io->x || !io->dt || !io->dt_bias || !io->A || !io->B || !io->C || !io->state_pool || !io->read_slots ||
+        !io->y || !io->device_err)
+        return SSD_ERR_NULL;
+    const void *big[] = {io->x, io->dt, io->B, io->C, io->z, io->y, io->state_pool};
+    for (const void *ptr : big)
+        if (ptr && !aligned16(ptr)) return SSD_ERR_ALIGN;
+    const void *small[] = {cu_seqlens, io->dt_bias, io->A, io->D, io->read_slots, io->write_slots, io->device_err};
+    for (const void *ptr : small)
+        if (ptr && !aligned4(ptr)) return SSD_ERR_ALIGN;
+    DecParams p{};
+    p.T = d->T;
+    p.R = d->R;
+    p.H = d->H;
+    p.P = d->P;
+    p.N = d->N;
+    p.G = d->G;
+    p.num_slots = d->num_slots;
+    p.cu = cu_seqlens;
+    p.io = *io;
+    const cudaError_t e = d->dtype == SSD_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, kv, stream)
+                                                     : launch_decode_t<float>(p, kv, stream);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}

@@ -186,3 +186,47 @@ def forward(prob: dict, n_threads: int = 0, requests=None, heads=None):
         out["state_pool"] = new_pool
     out["first_chunk"] = np.asarray(first_chunk, dtype=np.int64)
     return out
+
+
+def decode(prob: dict, n_threads: int = 0):
+    """The decode step's call semantics (ssd_varlen_decode), computed by the oracle.
+
+    "Automatic prefix caching for GDN hybrid models (mamba_cache_mode=all) with MTP
+    speculative decoding", Purpose (Kernels/layers): decode kernels with dual
+    read/write state anchors.  Each request's window of new tokens is a short
+    varlen sequence of the recurrence above: its state starts from
+    state_pool[read_slots[i]] (zeros when the slot is < 0) and the state after
+    token t is written to state_pool[write_slots[t]] when that slot is >= 0.
+
+    ``prob`` holds numpy arrays (upcast exactly to fp64): x, dt, dt_bias, A, B, C,
+    D|None, z|None, cu_seqlens (window boundaries), state_pool (indexable by slot,
+    (H,P,N) per slot), read_slots (R), write_slots (T) or None.
+
+    Returns {"y": (T,H,P), "writes": {slot: (H,P,N) state written there}}.
+    """
+    cu = np.asarray(prob["cu_seqlens"], dtype=np.int64)
+    R = cu.shape[0] - 1
+    x = prob["x"]
+    T, H, P = x.shape
+    N = prob["B"].shape[2]
+    pool = prob["state_pool"]
+    S = pool.shape[0]
+    read = np.asarray(prob["read_slots"], dtype=np.int64)
+    write = prob.get("write_slots")
+    write = np.full(T, -1, dtype=np.int64) if write is None else np.asarray(write, dtype=np.int64)
+    h0 = np.zeros((R, H, P, N), dtype=np.float64)
+    for i in range(R):
+        if 0 <= read[i] < S:
+            h0[i] = pool[int(read[i])]
+    rec_k = [[t - int(cu[i]) + 1 for t in range(int(cu[i]), int(cu[i + 1])) if 0 <= write[t] < S]
+             for i in range(R)]
+    y, _, rec = recurrence(cu, x, prob["dt"], prob["dt_bias"], prob["A"], prob["B"], prob["C"],
+                           prob.get("D"), prob.get("z"), h0, rec_k, None, n_threads)
+    writes = {}
+    row = 0
+    for i in range(R):
+        for t in range(int(cu[i]), int(cu[i + 1])):
+            if 0 <= write[t] < S:
+                writes[int(write[t])] = rec[row]
+                row += 1
+    return {"y": y, "writes": writes}

@@ -41,6 +41,7 @@ def test_struct_sizes_match_header(lib):
     assert ctypes.sizeof(m.ssd_dims) == 56
     assert ctypes.sizeof(m.ssd_inputs) == 10 * 8
     assert ctypes.sizeof(m.ssd_outputs) == 5 * 8
+    assert ctypes.sizeof(m.ssd_decode_io) == 13 * 8
 
 
 def _dims(**kw):
@@ -125,3 +126,38 @@ def test_count_chunks_matches_checkpoint_definition(lib, seed):
         assert m.ssd_varlen_count_chunks(cu, ncomp, Q) == first[-1]
         _, first0 = checkpoints.checkpoint_records(lens, None, Q)
         assert m.ssd_varlen_count_chunks(cu, None, Q) == first0[-1]
+
+
+# ---- decode step: host validation (no launch is reached) -------------------
+_FAKE = 0x100000  # an aligned address the host code never dereferences
+
+
+def _decode_io(**kw):
+    f = ctypes.c_void_p(_FAKE)
+    fields = dict(x=f, dt=f, dt_bias=f, A=f, B=f, C=f, D=None, z=None, state_pool=f,
+                  read_slots=f, write_slots=None, y=f, device_err=f)
+    fields.update(kw)
+    return m.ssd_decode_io(*[fields[n] for n, _ in m.ssd_decode_io._fields_])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(R=0), -2), (dict(num_slots=0), -2), (dict(G=3), -4), (dict(dtype=9), -6),
+    (dict(N=96), -11), (dict(N=8), -11), (dict(N=512), -11), (dict(P=256, N=128), -11),
+])
+def test_decode_rejects_bad_dims(lib, kw, code):
+    base = dict(T=8, R=2, H=4, P=64, N=128, G=1, chunk_size=0, dtype=m.DTYPE_BF16, num_slots=4)
+    base.update(kw)
+    d = m.make_dims(**base)
+    io = _decode_io()
+    assert lib.ssd_varlen_decode(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == code
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("x", None, -1), ("state_pool", None, -1), ("read_slots", None, -1), ("device_err", None, -1),
+    ("y", None, -1), ("x", ctypes.c_void_p(_FAKE + 4), -7), ("read_slots", ctypes.c_void_p(_FAKE + 2), -7),
+])
+def test_decode_rejects_bad_pointers(lib, field, value, code):
+    d = m.make_dims(8, 2, 4, 64, 128, 1, 0, m.DTYPE_BF16, num_slots=4)
+    io = _decode_io(**{field: value})
+    assert lib.ssd_varlen_decode(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == code
+    assert lib.ssd_varlen_decode(ctypes.byref(d), None, ctypes.byref(io), None) == -1

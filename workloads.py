@@ -275,3 +275,125 @@ class _SparsePool:
         c.shape = self.shape
         c.slots = {k: v.copy() for k, v in self.slots.items()}
         return c
+
+
+# ---- decode / speculative-decode steps --------------------------------------
+@dataclass
+class DecodeSpec:
+    """A decode step: R requests, each with a window of new tokens (1 for a plain
+    decode step, 1 + drafts for a speculative step), a read anchor per request and
+    a write anchor per token in one fp32 state pool."""
+    name: str
+    H: int
+    P: int
+    N: int
+    G: int
+    dtype: str
+    windows: list
+    has_D: bool = True
+    has_z: bool = True
+    read_zero_every: int = 0   # every k-th request starts from zeros (read slot -1); 0 = none
+    write_every: int = 1       # every k-th token of a window writes its state (the last always does)
+    init_std: float = 0.5
+
+
+DECODE_CONFIGS: dict[str, DecodeSpec] = {
+    "decode_tiny_fp32": DecodeSpec("decode_tiny_fp32", H=4, P=16, N=16, G=1, dtype="fp32",
+                                   windows=[1, 3, 0, 2], has_z=False, read_zero_every=3, write_every=2),
+    # the uniform prefill workload's layer shape, 256 requests with speculative
+    # windows of 1 verified + 3 draft tokens, every position keeping its state
+    "decode_spec_256x4": DecodeSpec("decode_spec_256x4", H=80, P=64, N=128, G=1, dtype="bf16",
+                                    windows=[4] * 256),
+}
+DECODE_SEED = {"decode_tiny_fp32": 100, "decode_spec_256x4": 101}
+
+
+def make_decode_problem(spec: DecodeSpec | str, seed: int | None = None, device="cpu", windows=None,
+                        canary: float | None = None):
+    """Draw one decode step.  Read slots are distinct, write slots distinct and
+    disjoint from them; the pool holds R + T slots (unused slots hold ``canary``)."""
+    if isinstance(spec, str):
+        spec = DECODE_CONFIGS[spec]
+    if seed is None:
+        seed = DECODE_SEED.get(spec.name, 0)
+    win = list(windows) if windows is not None else list(spec.windows)
+    R, T = len(win), int(sum(win))
+    H, P, N, G = spec.H, spec.P, spec.N, spec.G
+    dt_ = torch.float32 if spec.dtype == "fp32" else torch.bfloat16
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    rng = np.random.default_rng(seed + 1000)
+    cu = torch.zeros(R + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(win, dtype=torch.int64), 0).to(torch.int32)
+    prob = {"spec": spec.name, "windows": win, "T": T, "R": R, "H": H, "P": P, "N": N, "G": G,
+            "dtype": spec.dtype, "cu_seqlens": cu.to(dev)}
+    prob["x"] = _randn((T, H, P), gen, dev, dt_)
+    prob["dt"] = _randn((T, H), gen, dev, dt_)
+    prob["dt_bias"] = (torch.rand((H,), generator=gen, device=dev) * -1.0 - 1.0)
+    prob["A"] = -torch.exp(torch.rand((H,), generator=gen, device=dev) * math.log(16.0))
+    prob["B"] = _randn((T, G, N), gen, dev, dt_)
+    prob["C"] = _randn((T, G, N), gen, dev, dt_)
+    prob["D"] = _randn((H,), gen, dev, torch.float32) if spec.has_D else None
+    prob["z"] = _randn((T, H, P), gen, dev, dt_) if spec.has_z else None
+    S = R + T
+    perm = rng.permutation(S)
+    read = [int(v) for v in perm[:R]]
+    if spec.read_zero_every:
+        read = [-1 if i % spec.read_zero_every == spec.read_zero_every - 1 else s for i, s in enumerate(read)]
+    write = [-1] * T
+    k = R
+    for i in range(R):
+        a, L = int(cu[i]), win[i]
+        for j in range(L):
+            if j == L - 1 or j % spec.write_every == spec.write_every - 1:
+                write[a + j] = int(perm[k])
+                k += 1
+    pool = torch.full((S, H, P, N), 0.0 if canary is None else canary, dtype=torch.float32, device=dev)
+    for s in read:
+        if s >= 0:
+            pool[s] = _randn((H, P, N), gen, dev, torch.float32, spec.init_std)
+    prob["state_pool"] = pool
+    prob["read_slots"] = torch.tensor(read, dtype=torch.int32, device=dev)
+    prob["write_slots"] = torch.tensor(write, dtype=torch.int32, device=dev)
+    return prob
+
+
+def to_oracle_decode(prob: dict, requests=None, heads=None) -> dict:
+    """Host float64 copies of a decode step, in the form oracle.decode takes.  With
+    ``requests`` / ``heads`` only those are copied (requests repacked in order, each
+    selected head its own group); the pool is then a view of the read slots only."""
+    def f64(t):
+        return None if t is None else t.detach().to("cpu").to(torch.float64).numpy()
+
+    H, G = prob["H"], prob["G"]
+    hsel = list(range(H)) if heads is None else [int(h) for h in heads]
+    cu = prob["cu_seqlens"].detach().to("cpu").to(torch.int64).numpy()
+    sel = list(range(len(cu) - 1)) if requests is None else [int(i) for i in requests]
+    hidx = torch.tensor(hsel, dtype=torch.long)
+    gidx = torch.tensor([h // (H // G) for h in hsel] if heads is not None else list(range(G)),
+                        dtype=torch.long)
+    toks = torch.tensor([t for i in sel for t in range(int(cu[i]), int(cu[i + 1]))], dtype=torch.long)
+    new_cu = np.zeros(len(sel) + 1, dtype=np.int64)
+    new_cu[1:] = np.cumsum([int(cu[i + 1] - cu[i]) for i in sel])
+
+    def take(t, gdim=False):
+        if t is None:
+            return None
+        t = t.detach().to("cpu")[toks]
+        return f64(t.index_select(1, gidx if gdim else hidx))
+
+    read = prob["read_slots"].detach().to("cpu").numpy()
+    write = prob["write_slots"].detach().to("cpu").numpy() if prob.get("write_slots") is not None else None
+    out = {"cu_seqlens": new_cu, "x": take(prob["x"]), "dt": take(prob["dt"]),
+           "B": take(prob["B"], True), "C": take(prob["C"], True), "z": take(prob.get("z")),
+           "dt_bias": f64(prob["dt_bias"])[hsel], "A": f64(prob["A"])[hsel],
+           "D": None if prob.get("D") is None else f64(prob["D"])[hsel],
+           "read_slots": read[sel], "write_slots": None if write is None else write[toks.numpy()],
+           "requests": sel, "heads": hsel, "tokens": toks.numpy()}
+    pool = prob["state_pool"]
+    if requests is None and heads is None:
+        out["state_pool"] = f64(pool)
+    else:
+        out["state_pool"] = _SparsePool(pool, [int(s) for s in read[sel] if 0 <= s < pool.shape[0]], hidx)
+    return out
