@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 DEFAULT_CONFIG = "uniform_8x2048"
 METRIC = "SSD varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
 DECODE_METRIC = "SSD decode step tokens/s per layer (bf16, 1×GB300); % of roofline"
+CONV_METRIC = "varlen causal conv1d tokens/s per layer (bf16, 1×GB300); % of roofline"
 # The files the dominant (scan) kernel is compiled from; its DRAM-traffic figure in
 # profiles/traffic.txt is valid only for this exact source.
 KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
@@ -247,12 +248,40 @@ def run_reference_decode(args, world):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_conv(args, world):
+    """The conv1d oracle on the host cores: a bounded channel sample per timed step."""
+    from oracle.conv1d import conv1d
+    import workloads
+    prob = workloads.make_conv_problem(args.config, device="cpu")
+    T, D = prob["T"], prob["D"]
+    ch = list(range(0, D, max(1, D // 64)))[:64]
+    o = workloads.to_oracle_conv(prob, channels=ch)
+    for _ in range(args.warmup):
+        conv1d(o)
+    vals = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        conv1d(o)
+        vals.append(T * len(ch) / D / (time.perf_counter() - t0))
+    value = sorted(vals)[len(vals) // 2]
+    line = {"metric": CONV_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": T / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.config, "T": T, "R": prob["R"], "D": D, "W": prob["W"]},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{len(ch)} of {D} channels, all {T} tokens, scaled to all channels"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     import workloads
     if rank != 0:
         return
     if args.config in workloads.DECODE_CONFIGS:
         return run_reference_decode(args, world)
+    if args.config in workloads.CONV_CONFIGS:
+        return run_reference_conv(args, world)
     prob = workloads.make_problem(args.config, device="cpu")
     # Each step: a bounded sample (whole requests) sized so the run stays within minutes.
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
@@ -379,6 +408,89 @@ def run_decode_bench(args, rank, local_rank, world, dist):
         print(json.dumps(line), flush=True)
 
 
+def conv_cost(prob):
+    """Bytes one conv1d must move: x and y, the weights and bias, the conv states
+    read and written."""
+    T, D, W = prob["T"], prob["D"], prob["W"]
+    el = 4 if prob["dtype"] == "fp32" else 2
+    states = int((prob["read_slots"] >= 0).sum().item()) + int((prob["write_slots"] >= 0).sum().item())
+    return {"bytes": 2 * el * T * D + 4 * D * (W + 1) + el * D * (W - 1) * states, "flops": 2 * T * D * W}
+
+
+def run_conv_bench(args, rank, local_rank, world, dist):
+    """The varlen causal conv1d (ssd_varlen_conv1d), timed like the forward."""
+    import torch
+    import mamba2_ssd_varlen_gb300 as m
+    import workloads
+    peaks = load_peaks()
+    prob = workloads.make_conv_problem(args.config, device="cuda")
+    call = m.Conv1dCall(prob)
+    stream = torch.cuda.current_stream()
+    cost = conv_cost(prob)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert call.status() == 0, "device error during warm-up"
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    assert call.status() == 0, "device error during the timed region"
+    k_ms = [a.elapsed_time(b) for a, b in ev]
+    k_avg = sum(k_ms) / K
+    T = prob["T"]
+    host_x = prob["x"].cpu().pin_memory()
+    y_host = torch.empty(call.y.shape, dtype=call.y.dtype, pin_memory=True)
+
+    def e2e_step():
+        prob["x"].copy_(host_x, non_blocking=True)
+        call()
+        y_host.copy_(call.y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.e2e_steps
+    achieved = cost["bytes"] / (k_avg / 1e3) / 1e9
+    line = {"metric": CONV_METRIC, "value": T * world / (k_avg / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": k_avg, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob["dtype"] == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": args.config, "T": T, "R": prob["R"], "D": prob["D"], "W": prob["W"],
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "x and y each larger than L2 (no flush)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"], "algorithmic_bytes": cost["bytes"],
+                         "kernel": "ssd_varlen_conv1d", "kernel_ms_avg": round(k_avg, 5)},
+            "gpu_launches": K, "clocks": clocks,
+            "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": host_x.numel() * host_x.element_size(),
+                    "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,8 +516,9 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     m.load_library()
-    if args.config in workloads.DECODE_CONFIGS:
-        run_decode_bench(args, rank, local_rank, world, dist)
+    if args.config in workloads.DECODE_CONFIGS or args.config in workloads.CONV_CONFIGS:
+        bench_fn = run_decode_bench if args.config in workloads.DECODE_CONFIGS else run_conv_bench
+        bench_fn(args, rank, local_rank, world, dist)
         if dist:
             dist.destroy_process_group()
         return

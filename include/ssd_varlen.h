@@ -245,6 +245,69 @@ typedef struct ssd_decode_io {
 int ssd_varlen_decode(const ssd_dims *dims, const int32_t *cu_seqlens, const ssd_decode_io *io,
                       cudaStream_t stream);
 
+/* ---- Varlen causal depthwise conv1d with conv-state anchors ---------------
+ * The step before the SSD in a Mamba2 layer, over the same packed varlen batch
+ * ("[Model] Mamba2 varlen and metadata refactor", Purpose items 1-2; the
+ * causal_conv1d decode kernel with dual read/write state anchors of "Automatic
+ * prefix caching for GDN hybrid models (mamba_cache_mode=all) with MTP
+ * speculative decoding", Purpose, Kernels/layers).  Per request i (tokens
+ * [cu_seqlens[i], cu_seqlens[i+1])) and channel c, with the request's inputs
+ * preceded by its W-1 conv-state values (oldest first):
+ *     y[t,c] = act(bias[c] + sum_{k<W} weight[c,k] * xin[t - (W-1) + k, c])
+ * the conv state read from conv_pool[read_slots[i]] (zeros when the slot is < 0
+ * or read_slots is NULL) and the last W-1 inputs (the initial values included
+ * when the request is shorter) written to conv_pool[write_slots[i]] when that
+ * slot is >= 0; act is SiLU when dims.silu != 0, else the identity.
+ *
+ * Layouts: x, y (T,D) and conv_pool (num_slots,D,W-1) in dims.dtype (the state
+ * holds raw inputs, exact in that dtype); weight (D,W), bias (D) fp32.  W in
+ * [2, 4]; D a multiple of 8.  Read and write slots of one call are disjoint.
+ * device_err (one int32 in device memory, required) receives SSD_DEVERR_*
+ * bits (CU_SEQLENS, INIT_SLOT, FINAL_SLOT).  One launch on `stream`; allocates
+ * nothing. */
+typedef struct ssd_conv_dims {
+    int64_t T;          /* total tokens, >= 0 */
+    int32_t R;          /* requests, >= 1 */
+    int32_t D;          /* channels, a multiple of 8 */
+    int32_t W;          /* kernel width, 2..4 */
+    int32_t dtype;      /* enum ssd_dtype of x, y and conv_pool */
+    int32_t num_slots;  /* rows of conv_pool (0 when no slots are used) */
+    int32_t silu;       /* 1: SiLU activation, 0: none */
+} ssd_conv_dims;
+
+typedef struct ssd_conv_io {
+    const void *x;              /* (T,D) */
+    const float *weight;        /* (D,W) */
+    const float *bias;          /* (D) or NULL */
+    void *conv_pool;            /* (num_slots,D,W-1), or NULL when no slots are given */
+    const int32_t *read_slots;  /* (R) or NULL */
+    const int32_t *write_slots; /* (R) or NULL */
+    void *y;                    /* (T,D) */
+    int32_t *device_err;        /* one int32, OR-ed with SSD_DEVERR_* bits */
+} ssd_conv_io;
+
+int ssd_varlen_conv1d(const ssd_conv_dims *dims, const int32_t *cu_seqlens, const ssd_conv_io *io,
+                      cudaStream_t stream);
+
+/* ---- Block-aligned prefill bites (host only) --------------------------------
+ * "Automatic prefix caching for GDN hybrid models (mamba_cache_mode=all) with
+ * MTP speculative decoding", Purpose (engine core: kernel-chunk-aligned prefill
+ * clipping and block-aligned split in the scheduler) and the review note on
+ * that page about re-aligning a misaligned start in the final bite.
+ * A scheduler proposes to prefill positions [start, end) of a prompt that ends
+ * at `total`; the bite is clipped so that the next bite starts on the align
+ * grid (align = the block size, a multiple of chunk_size).  With
+ * last_aligned = total rounded down to a multiple of align:
+ *   - a start off the grid ends the bite at the next boundary, when that
+ *     boundary is at most last_aligned (also in the final bite);
+ *   - otherwise an end before last_aligned is rounded down to a boundary, which
+ *     is start itself when the budget is below one block: the request then
+ *     waits for a step with a larger budget;
+ *   - an aligned start reaching last_aligned may end anywhere (the tail).
+ * Returns the clipped end (start <= result <= end), or SSD_ERR_DIMS (< 0) when
+ * align < 1, start < 0, end <= start or end > total.  Pure host arithmetic. */
+int64_t ssd_varlen_align_bite(int64_t start, int64_t end, int64_t total, int32_t align);
+
 #ifdef __cplusplus
 }
 #endif

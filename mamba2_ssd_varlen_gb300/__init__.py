@@ -14,6 +14,8 @@ The functions keep the C names:
   ssd_varlen_strerror(code)                        -> text
   ssd_varlen_forward_static(...)   (C only: forward without a caller workspace)
   ssd_varlen_decode(dims, cu_seqlens, io)        (decode / speculative-decode step)
+  ssd_varlen_conv1d(dims, cu_seqlens, io)        (varlen causal conv1d with conv-state anchors)
+  ssd_varlen_align_bite(start, end, total, align) (block-aligned prefill bite, host)
 and ``run(...)`` wires a whole call from torch tensors (tests and bench use it).
 """
 from __future__ import annotations
@@ -37,7 +39,8 @@ STATUS = {
 }
 EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
             "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror",
-            "ssd_varlen_forward_static", "ssd_varlen_decode"]
+            "ssd_varlen_forward_static", "ssd_varlen_decode", "ssd_varlen_conv1d",
+            "ssd_varlen_align_bite"]
 # Size of the library-owned scratch array used by ssd_varlen_forward_static.
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -71,6 +74,16 @@ class ssd_outputs(ctypes.Structure):
 class ssd_decode_io(ctypes.Structure):
     _fields_ = [("x", c_vp), ("dt", c_vp), ("dt_bias", c_vp), ("A", c_vp), ("B", c_vp), ("C", c_vp),
                 ("D", c_vp), ("z", c_vp), ("state_pool", c_vp), ("read_slots", c_vp),
+                ("write_slots", c_vp), ("y", c_vp), ("device_err", c_vp)]
+
+
+class ssd_conv_dims(ctypes.Structure):
+    _fields_ = [("T", c_i64), ("R", c_i32), ("D", c_i32), ("W", c_i32), ("dtype", c_i32), ("num_slots", c_i32),
+                ("silu", c_i32)]
+
+
+class ssd_conv_io(ctypes.Structure):
+    _fields_ = [("x", c_vp), ("weight", c_vp), ("bias", c_vp), ("conv_pool", c_vp), ("read_slots", c_vp),
                 ("write_slots", c_vp), ("y", c_vp), ("device_err", c_vp)]
 
 
@@ -112,6 +125,10 @@ def load_library():
     lib.ssd_varlen_forward_static.restype = ctypes.c_int
     lib.ssd_varlen_decode.argtypes = [ctypes.POINTER(ssd_dims), c_vp, ctypes.POINTER(ssd_decode_io), c_vp]
     lib.ssd_varlen_decode.restype = ctypes.c_int
+    lib.ssd_varlen_conv1d.argtypes = [ctypes.POINTER(ssd_conv_dims), c_vp, ctypes.POINTER(ssd_conv_io), c_vp]
+    lib.ssd_varlen_conv1d.restype = ctypes.c_int
+    lib.ssd_varlen_align_bite.argtypes = [c_i64, c_i64, c_i64, c_i32]
+    lib.ssd_varlen_align_bite.restype = c_i64
     _lib = lib
     return lib
 
@@ -294,3 +311,54 @@ class DecodeCall:
 def run_decode(prob: dict, **kw) -> DecodeCall:
     """One decode step on the current stream; returns the DecodeCall (y on it, pool updated)."""
     return DecodeCall(prob, **kw)()
+
+
+
+def ssd_varlen_conv1d(dims: ssd_conv_dims, cu_seqlens, io: ssd_conv_io, stream=None):
+    rc = load_library().ssd_varlen_conv1d(ctypes.byref(dims), _ptr(cu_seqlens), ctypes.byref(io), _stream(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_conv1d")
+
+
+class Conv1dCall:
+    """One varlen causal conv1d over a problem from workloads.make_conv_problem: the
+    output y and the device error word, and the pre-built argument structs."""
+
+    def __init__(self, prob: dict, stream=None):
+        import torch
+        self.prob = prob
+        x = prob["x"]
+        T, D = x.shape
+        W = prob["weight"].shape[1]
+        R = prob["cu_seqlens"].shape[0] - 1
+        pool = prob.get("conv_pool")
+        self.dims = ssd_conv_dims(T, R, D, W, DTYPE_F32 if x.dtype == torch.float32 else DTYPE_BF16,
+                                  0 if pool is None else pool.shape[0], 1 if prob.get("silu") else 0)
+        self.y = torch.empty_like(x)
+        self.err = torch.zeros(4, dtype=torch.int32, device=x.device)
+        self.io = ssd_conv_io(_ptr(x), _ptr(prob["weight"]), _ptr(prob.get("bias")), _ptr(pool),
+                              _ptr(prob.get("read_slots")), _ptr(prob.get("write_slots")), _ptr(self.y),
+                              _ptr(self.err))
+        self.stream = stream
+
+    def __call__(self):
+        ssd_varlen_conv1d(self.dims, self.prob["cu_seqlens"], self.io, self.stream)
+        return self
+
+    def status(self) -> int:
+        v = int(self.err[0].item())
+        self.err.zero_()
+        return v
+
+
+def run_conv1d(prob: dict, **kw) -> Conv1dCall:
+    """One conv1d on the current stream; returns the Conv1dCall (y on it, conv states updated)."""
+    return Conv1dCall(prob, **kw)()
+
+
+def ssd_varlen_align_bite(start: int, end: int, total: int, align: int) -> int:
+    """Where a proposed prefill bite [start, end) of a prompt ending at ``total`` should end."""
+    r = int(load_library().ssd_varlen_align_bite(int(start), int(end), int(total), int(align)))
+    if r < 0:
+        raise SsdError(r, "ssd_varlen_align_bite")
+    return r

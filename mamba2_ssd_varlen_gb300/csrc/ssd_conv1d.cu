@@ -1,0 +1,314 @@
+// ssd_conv1d.cu -- varlen causal depthwise conv1d with conv-state anchors, the
+// step before the SSD in a Mamba2 layer ("[Model] Mamba2 varlen and metadata
+// refactor", Purpose items 1-2: packed varlen inputs; the causal_conv1d decode
+// kernel with dual read/write state anchors of "Automatic prefix caching for
+// GDN hybrid models (mamba_cache_mode=all) with MTP speculative decoding",
+// Purpose, Kernels/layers).
+//
+//   xin      = [conv state (W-1 inputs, oldest first), the request's inputs]
+//   y[t, c]  = act(bias[c] + sum_k weight[c, k] xin[t - (W-1) + k, c])
+//   new conv state = the last W-1 values of xin
+//
+// Streaming and HBM-bound: a warp takes a tile of kTile tokens and 32 x kN
+// channels; each thread owns one 16-byte vector of kN channels and slides a
+// W-deep register window down the tile, so every input and output row is one
+// coalesced vector access and every input is read once (plus a W-1 halo per
+// tile).  Request boundaries inside a tile restart the window from the next
+// request's conv state.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kConvThreads = 128;
+constexpr int kTile = 64;  // tokens per CTA
+
+struct ConvParams {
+    int64_t T;
+    int32_t R, D, W, num_slots, silu;
+    const int32_t *cu;
+    ssd_conv_io io;
+};
+
+template <typename T>
+struct Vec {  // one 16-byte vector of channels
+    static constexpr int kN = 16 / sizeof(T);
+    float v[kN];
+    __device__ __forceinline__ void load(const T *p) { set(*reinterpret_cast<const uint4 *>(p)); }
+    __device__ __forceinline__ void set(const uint4 q) {
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[2 * e] = __uint_as_float(w[e] << 16);
+                v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        } else {
+            v[0] = __uint_as_float(q.x);
+            v[1] = __uint_as_float(q.y);
+            v[2] = __uint_as_float(q.z);
+            v[3] = __uint_as_float(q.w);
+        }
+    }
+    __device__ __forceinline__ void store(T *p) const {
+        uint4 q;
+        if constexpr (sizeof(T) == 2) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            q = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            q = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+        }
+        *reinterpret_cast<uint4 *>(p) = q;
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int e = 0; e < kN; ++e) v[e] = 0.f;
+    }
+};
+
+// Conv state of kN channels c0.. of one slot: (W-1) values per channel, channel
+// major (kN * (W-1) consecutive elements); win[k+1] holds the k-th oldest input.
+template <typename T, int W>
+__device__ __forceinline__ void store_conv_state(T *slot, int c0, const Vec<T> (&win)[W]) {
+    constexpr int kN = Vec<T>::kN;
+    T *dst = slot + (size_t)c0 * (W - 1);
+#pragma unroll
+    for (int e = 0; e < kN; ++e)
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) dst[e * (W - 1) + k] = from_f32<T>(win[k + 1].v[e]);
+}
+
+// The request holding token t: the last i with cu[i] <= t < cu[i+1].
+__device__ __forceinline__ int request_of(const int32_t *cu, int R, int64_t t) {
+    int lo = 0, hi = R;  // invariant: cu[lo] <= t, answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// SiLU as v * 1/(1 + 2^(-v log2 e)) on the special-function unit's base-2
+// exponential and reciprocal (both good to about 2^-22 relative), far finer
+// than the storage rounding that follows.  Very negative v gives 2^(..) = inf,
+// a reciprocal of 0 and a (signed) zero, as SiLU tends to.
+__device__ __forceinline__ float silu_sfu(float v) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(v * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+    return v * r;
+}
+
+// 16-byte asynchronous global -> shared copy that bypasses L1 (the input is
+// streamed once), with commit / wait on the issuing thread's copy groups.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory"); }
+
+constexpr int kStages = 16;  // input rows in flight per thread
+constexpr int kUnroll = 6;   // a multiple of W-1 for every W, so the window shifts by renaming
+
+// One warp owns a work item: 32 consecutive 16-byte channel vectors (lane l the
+// vector g*32+l) over a tile of kTile tokens.  Items are numbered channel group
+// fastest, so the warps of a CTA read neighbouring parts of the same rows.
+// Each thread streams its inputs through a private kStages-deep ring in shared
+// memory filled by asynchronous copies, so the loads in flight cost no
+// registers; only the W-1 previous inputs stay in registers.
+template <typename T, int W, bool kSilu>
+__global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const __grid_constant__ ConvParams p) {
+    constexpr int kN = Vec<T>::kN;
+    __shared__ __align__(16) uint4 ring[kStages][kConvThreads];
+    const ssd_conv_io &io = p.io;
+    const int nvec = p.D / kN;
+    const int groups = (nvec + 31) / 32;
+    const int64_t item = (int64_t)blockIdx.x * (kConvThreads / 32) + (threadIdx.x >> 5);
+    const int g = (int)(item % groups);
+    const int64_t tile = item / groups;
+    const int c0 = (g * 32 + (threadIdx.x & 31)) * kN;  // first channel of this thread
+    const int64_t t0 = tile * kTile;
+    const T *__restrict__ xv = static_cast<const T *>(io.x);
+    T *__restrict__ yv = static_cast<T *>(io.y);
+    T *pool = static_cast<T *>(io.conv_pool);
+    const size_t slot_elems = (size_t)p.D * (W - 1);
+
+    // cu_seqlens must start at 0, not decrease and end at T (checked once).
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < p.R; i += kConvThreads)
+            if (p.cu[i + 1] < p.cu[i] || (i == 0 && p.cu[0] != 0) || (i == p.R - 1 && p.cu[p.R] != p.T))
+                atomicOr(io.device_err, SSD_DEVERR_CU_SEQLENS);
+    }
+    if (c0 >= p.D) return;
+
+    auto state_slot = [&](const int32_t *slots, int i, int bit) -> T * {
+        if (!slots || !pool) return nullptr;
+        const int s = slots[i];
+        if (s >= p.num_slots) {
+            if (c0 == 0) atomicOr(io.device_err, bit);
+            return nullptr;
+        }
+        return s >= 0 ? pool + (size_t)s * slot_elems : nullptr;
+    };
+
+    // An empty request's conv state passes through (the tile-0 items do it).
+    if (tile == 0) {
+        for (int i = 0; i < p.R; ++i) {
+            if (p.cu[i + 1] != p.cu[i]) continue;
+            T *dst = state_slot(io.write_slots, i, SSD_DEVERR_FINAL_SLOT);
+            if (!dst) continue;
+            const T *src = state_slot(io.read_slots, i, SSD_DEVERR_INIT_SLOT);
+            for (int e = 0; e < kN * (W - 1); ++e)
+                dst[(size_t)c0 * (W - 1) + e] = src ? src[(size_t)c0 * (W - 1) + e] : from_f32<T>(0.f);
+        }
+    }
+    if (t0 >= p.T) return;
+    const int n = (int)min(p.T - t0, (int64_t)kTile);  // tokens of this tile
+    const size_t row = (size_t)p.D;
+    const T *xt = xv + (size_t)t0 * row + c0;  // this thread's vector of token t0
+    T *yt = yv + (size_t)t0 * row + c0;
+    uint4 *mine = &ring[0][threadIdx.x];  // stage s at mine[s * kConvThreads]
+
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {  // one copy group per stage, empty past the tile
+        if (s < n) cp_async16(mine + s * kConvThreads, xt + (size_t)s * row);
+        cp_async_commit();
+    }
+
+    float wt[W][kN], bs[kN];
+#pragma unroll
+    for (int e = 0; e < kN; ++e) {
+        bs[e] = io.bias ? io.bias[c0 + e] : 0.f;
+#pragma unroll
+        for (int k = 0; k < W; ++k) wt[k][e] = io.weight[(size_t)(c0 + e) * W + k];
+    }
+
+    // window: win[0..W-2] the W-1 inputs before token t, win[W-1] token t
+    Vec<T> win[W];
+    int i = request_of(p.cu, p.R, t0);
+    int64_t rs = p.cu[i];
+    int rel_end = (int)min((int64_t)p.cu[i + 1] - t0, (int64_t)kTile + 1);  // request end, tile-relative
+    auto enter = [&](int64_t t) {  // fill win[0..W-2] with the inputs before t in its request
+        const T *src = nullptr;
+        if (t - rs < W - 1) src = state_slot(io.read_slots, i, SSD_DEVERR_INIT_SLOT);
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) {
+            const int64_t u = t - (W - 1) + k;
+            if (u >= rs && u >= 0) {
+                win[k].load(xv + (size_t)u * row + c0);
+            } else if (src) {
+                const int j = (int)(W - 1 - (rs - u));  // index in the conv state, oldest first
+#pragma unroll
+                for (int e = 0; e < kN; ++e) win[k].v[e] = to_f32(src[(size_t)(c0 + e) * (W - 1) + j]);
+            } else {
+                win[k].zero();
+            }
+        }
+    };
+    enter(t0);
+    for (int jb = 0; jb < n; jb += kUnroll) {
+        const int sb = jb % kStages;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = jb + u;
+            if (j >= n) break;
+            if (j == rel_end) {  // the next non-empty request starts here
+                const int64_t t = t0 + j;
+                while (i + 1 < p.R && p.cu[i + 1] <= t) ++i;
+                rs = p.cu[i];
+                rel_end = (int)min((int64_t)p.cu[i + 1] - t0, (int64_t)kTile + 1);
+                enter(t);
+            }
+            const int st = sb + u < kStages ? sb + u : sb + u - kStages;
+            cp_async_wait<kStages - 1>();  // token j's copy group has landed
+            win[W - 1].set(mine[st * kConvThreads]);
+            Vec<T> out;
+#pragma unroll
+            for (int e = 0; e < kN; ++e) {
+                float acc = bs[e];
+#pragma unroll
+                for (int k = 0; k < W; ++k) acc = fmaf(wt[k][e], win[k].v[e], acc);
+                out.v[e] = kSilu ? silu_sfu(acc) : acc;
+            }
+            out.store(yt + (size_t)j * row);
+            if (j + 1 == rel_end) {  // the request's last token: its conv state goes out
+                T *dst = state_slot(io.write_slots, i, SSD_DEVERR_FINAL_SLOT);
+                if (dst) store_conv_state<T, W>(dst, c0, win);
+            }
+            // refill the stage just read (its value is consumed above)
+            if (j + kStages < n) cp_async16(mine + st * kConvThreads, xt + (size_t)(j + kStages) * row);
+            cp_async_commit();
+#pragma unroll
+            for (int k = 0; k < W - 1; ++k) win[k] = win[k + 1];
+        }
+    }
+    cp_async_wait<0>();
+}
+
+template <typename T, int W>
+void launch_conv_w(const ConvParams &p, dim3 grid, cudaStream_t stream) {
+    if (p.silu) conv1d_kernel<T, W, true><<<grid, kConvThreads, 0, stream>>>(p);
+    else conv1d_kernel<T, W, false><<<grid, kConvThreads, 0, stream>>>(p);
+}
+
+template <typename T>
+cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t stream) {
+    constexpr int kN = 16 / sizeof(T);
+    const int64_t tiles = (p.T + kTile - 1) / kTile;
+    const int64_t groups = (p.D / kN + 31) / 32;
+    const int64_t items = (tiles > 0 ? tiles : 1) * groups;
+    const int64_t ctas = (items + kConvThreads / 32 - 1) / (kConvThreads / 32);
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)ctas);
+    switch (p.W) {
+        case 2: launch_conv_w<T, 2>(p, grid, stream); break;
+        case 3: launch_conv_w<T, 3>(p, grid, stream); break;
+        case 4: launch_conv_w<T, 4>(p, grid, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+bool aligned_to(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" int ssd_varlen_conv1d(const ssd_conv_dims *d, const int32_t *cu_seqlens, const ssd_conv_io *io,
+                                 cudaStream_t stream) {
+    if (!d || !cu_seqlens || !io) return SSD_ERR_NULL;
+    if (d->T < 0 || d->T > 0x7fffffffLL || d->R < 1 || d->D < 1 || d->num_slots < 0) return SSD_ERR_DIMS;
+    if (d->dtype != SSD_DTYPE_BF16 && d->dtype != SSD_DTYPE_F32) return SSD_ERR_DTYPE;
+    if (d->W < 2 || d->W > 4 || d->D % 8 != 0) return SSD_ERR_UNSUPPORTED;
+    if (!io->x || !io->weight || !io->y || !io->device_err) return SSD_ERR_NULL;
+    const bool uses_pool = io->read_slots || io->write_slots;
+    if (uses_pool && (!io->conv_pool || d->num_slots < 1)) return SSD_ERR_NULL;
+    const void *vec[] = {io->x, io->y, io->conv_pool};
+    for (const void *ptr : vec)
+        if (ptr && !aligned_to(ptr, 16)) return SSD_ERR_ALIGN;
+    const void *small[] = {cu_seqlens, io->weight, io->bias, io->read_slots, io->write_slots, io->device_err};
+    for (const void *ptr : small)
+        if (ptr && !aligned_to(ptr, 4)) return SSD_ERR_ALIGN;
+    ConvParams p{};
+    p.T = d->T;
+    p.R = d->R;
+    p.D = d->D;
+    p.W = d->W;
+    p.num_slots = d->num_slots;
+    p.silu = d->silu ? 1 : 0;
+    p.cu = cu_seqlens;
+    p.io = *io;
+    const cudaError_t e = d->dtype == SSD_DTYPE_BF16 ? launch_conv_t<__nv_bfloat16>(p, stream)
+                                                     : launch_conv_t<float>(p, stream);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}

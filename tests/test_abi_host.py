@@ -161,3 +161,37 @@ def test_decode_rejects_bad_pointers(lib, field, value, code):
     io = _decode_io(**{field: value})
     assert lib.ssd_varlen_decode(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == code
     assert lib.ssd_varlen_decode(ctypes.byref(d), None, ctypes.byref(io), None) == -1
+
+
+# ---- varlen causal conv1d: host validation ----------------------------------
+def _conv_io(**kw):
+    f = ctypes.c_void_p(_FAKE)
+    fields = dict(x=f, weight=f, bias=None, conv_pool=f, read_slots=f, write_slots=f, y=f, device_err=f)
+    fields.update(kw)
+    return m.ssd_conv_io(*[fields[n] for n, _ in m.ssd_conv_io._fields_])
+
+
+def test_conv_struct_sizes():
+    assert ctypes.sizeof(m.ssd_conv_dims) == 32
+    assert ctypes.sizeof(m.ssd_conv_io) == 8 * 8
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(R=0), -2), (dict(D=0), -2), (dict(T=-1), -2), (dict(dtype=4), -6), (dict(W=1), -11),
+    (dict(W=5), -11), (dict(D=12), -11),
+])
+def test_conv_rejects_bad_dims(lib, kw, code):
+    base = dict(T=8, R=2, D=64, W=4, dtype=m.DTYPE_BF16, num_slots=4, silu=1)
+    base.update(kw)
+    d = m.ssd_conv_dims(*[base[n] for n, _ in m.ssd_conv_dims._fields_])
+    assert lib.ssd_varlen_conv1d(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(_conv_io()), None) == code
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("x", None, -1), ("weight", None, -1), ("y", None, -1), ("device_err", None, -1), ("conv_pool", None, -1),
+    ("x", ctypes.c_void_p(_FAKE + 8), -7), ("weight", ctypes.c_void_p(_FAKE + 2), -7),
+])
+def test_conv_rejects_bad_pointers(lib, field, value, code):
+    d = m.ssd_conv_dims(8, 2, 64, 4, m.DTYPE_BF16, 4, 1)
+    io = _conv_io(**{field: value})
+    assert lib.ssd_varlen_conv1d(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == code

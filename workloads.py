@@ -305,7 +305,10 @@ DECODE_CONFIGS: dict[str, DecodeSpec] = {
     "decode_spec_256x4": DecodeSpec("decode_spec_256x4", H=80, P=64, N=128, G=1, dtype="bf16",
                                     windows=[4] * 256),
 }
-DECODE_SEED = {"decode_tiny_fp32": 100, "decode_spec_256x4": 101}
+# a quarter of it, for profiler captures that replay the kernel many times
+DECODE_CONFIGS["decode_spec_64x4"] = DecodeSpec("decode_spec_64x4", H=80, P=64, N=128, G=1, dtype="bf16",
+                                                windows=[4] * 64)
+DECODE_SEED = {"decode_tiny_fp32": 100, "decode_spec_256x4": 101, "decode_spec_64x4": 102}
 
 
 def make_decode_problem(spec: DecodeSpec | str, seed: int | None = None, device="cpu", windows=None,
@@ -397,3 +400,84 @@ def to_oracle_decode(prob: dict, requests=None, heads=None) -> dict:
     else:
         out["state_pool"] = _SparsePool(pool, [int(s) for s in read[sel] if 0 <= s < pool.shape[0]], hidx)
     return out
+
+
+# ---- varlen causal conv1d ----------------------------------------------------
+@dataclass
+class ConvSpec:
+    """A varlen causal depthwise conv1d over D channels with a W-wide kernel; every
+    request reads its conv state from one slot and writes it to another."""
+    name: str
+    D: int
+    W: int
+    dtype: str
+    lengths: list
+    silu: bool = True
+    has_bias: bool = True
+    read_zero_every: int = 0   # every k-th request starts from zeros (read slot -1)
+
+
+CONV_CONFIGS: dict[str, ConvSpec] = {
+    "conv_tiny_fp32": ConvSpec("conv_tiny_fp32", D=16, W=4, dtype="fp32", lengths=[5, 17, 0, 2, 42],
+                               read_zero_every=2),
+    # the conv of the uniform prefill workload's layer: x, B and C channels
+    # (H P + 2 G N = 80 * 64 + 2 * 128) of 8 requests x 2048 tokens
+    "conv_uniform_8x2048": ConvSpec("conv_uniform_8x2048", D=5376, W=4, dtype="bf16", lengths=[2048] * 8),
+}
+CONV_SEED = {"conv_tiny_fp32": 200, "conv_uniform_8x2048": 201}
+
+
+def make_conv_problem(spec: ConvSpec | str, seed: int | None = None, device="cpu", lengths=None,
+                      canary: float | None = None):
+    if isinstance(spec, str):
+        spec = CONV_CONFIGS[spec]
+    if seed is None:
+        seed = CONV_SEED.get(spec.name, 0)
+    lens = list(lengths) if lengths is not None else list(spec.lengths)
+    R, T = len(lens), int(sum(lens))
+    D, W = spec.D, spec.W
+    dt_ = torch.float32 if spec.dtype == "fp32" else torch.bfloat16
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    rng = np.random.default_rng(seed + 1000)
+    cu = torch.zeros(R + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    prob = {"spec": spec.name, "lengths": lens, "T": T, "R": R, "D": D, "W": W, "dtype": spec.dtype,
+            "cu_seqlens": cu.to(dev), "silu": spec.silu}
+    prob["x"] = _randn((T, D), gen, dev, dt_)
+    prob["weight"] = _randn((D, W), gen, dev, torch.float32, 0.5)
+    prob["bias"] = _randn((D,), gen, dev, torch.float32, 0.5) if spec.has_bias else None
+    S = 2 * R
+    perm = rng.permutation(S)
+    read = [int(v) for v in perm[:R]]
+    if spec.read_zero_every:
+        read = [-1 if i % spec.read_zero_every == spec.read_zero_every - 1 else s for i, s in enumerate(read)]
+    write = [int(v) for v in perm[R:]]
+    pool = torch.full((S, D, W - 1), 0.0 if canary is None else canary, dtype=dt_, device=dev)
+    for s in read:
+        if s >= 0:
+            pool[s] = _randn((D, W - 1), gen, dev, dt_)
+    prob["conv_pool"] = pool
+    prob["read_slots"] = torch.tensor(read, dtype=torch.int32, device=dev)
+    prob["write_slots"] = torch.tensor(write, dtype=torch.int32, device=dev)
+    return prob
+
+
+def to_oracle_conv(prob: dict, channels=None) -> dict:
+    """Host float64 copies of a conv1d problem for oracle.conv1d (optionally a channel subset)."""
+    def f64(t):
+        return None if t is None else t.detach().to("cpu").to(torch.float64).numpy()
+
+    cidx = None if channels is None else torch.tensor(list(channels), dtype=torch.long)
+
+    def cols(t, dim):
+        if t is None or cidx is None:
+            return f64(t)
+        return f64(t.detach().to("cpu").index_select(dim, cidx))
+
+    return {"x": cols(prob["x"], 1), "weight": cols(prob["weight"], 0), "bias": cols(prob.get("bias"), 0),
+            "cu_seqlens": prob["cu_seqlens"].detach().to("cpu").numpy().astype(np.int64),
+            "conv_pool": cols(prob["conv_pool"], 1),
+            "read_slots": prob["read_slots"].detach().to("cpu").numpy(),
+            "write_slots": prob["write_slots"].detach().to("cpu").numpy(), "silu": prob["silu"]}
