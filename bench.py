@@ -35,6 +35,7 @@ DEFAULT_CONFIG = "uniform_8x2048"
 METRIC = "SSD varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
 DECODE_METRIC = "SSD decode step tokens/s per layer (bf16, 1×GB300); % of roofline"
 CONV_METRIC = "varlen causal conv1d tokens/s per layer (bf16, 1×GB300); % of roofline"
+GDN_METRIC = "gated delta rule varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
 # The files the dominant (scan) kernel is compiled from; its DRAM-traffic figure in
 # profiles/traffic.txt is valid only for this exact source.
 KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
@@ -274,10 +275,50 @@ def run_reference_conv(args, world):
     print(json.dumps(line), flush=True)
 
 
+def gdn_oracle_sample(prob, max_seconds):
+    """The GDN oracle over whole requests of the workload, in order, until about
+    ``max_seconds`` have passed; returns (tokens/s, what was sampled)."""
+    from oracle.gdn import gdn_forward
+    import workloads
+    cu = prob["cu_seqlens"].cpu().numpy()
+    done, t0 = [], time.perf_counter()
+    for i in range(len(cu) - 1):
+        gdn_forward(workloads.to_oracle_gdn(prob, requests=[i]))
+        done.append(i)
+        if time.perf_counter() - t0 > max_seconds:
+            break
+    dt = time.perf_counter() - t0
+    toks = int(sum(cu[i + 1] - cu[i] for i in done))
+    return toks / dt, f"{len(done)} of {len(cu) - 1} requests ({toks} tokens, all heads), numpy fp64"
+
+
+def run_reference_gdn(args, world):
+    import workloads
+    prob = workloads.make_gdn_problem(args.config, device="cpu")
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        gdn_oracle_sample(prob, budget)
+    vals, sample = [], ""
+    for _ in range(args.steps):
+        v, sample = gdn_oracle_sample(prob, budget)
+        vals.append(v)
+    value = sorted(vals)[len(vals) // 2]
+    T = prob["T"]
+    line = {"metric": GDN_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": T / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": gdn_config(prob, args.config, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     import workloads
     if rank != 0:
         return
+    if args.config in workloads.GDN_CONFIGS:
+        return run_reference_gdn(args, world)
     if args.config in workloads.DECODE_CONFIGS:
         return run_reference_decode(args, world)
     if args.config in workloads.CONV_CONFIGS:
@@ -491,6 +532,106 @@ def run_conv_bench(args, rank, local_rank, world, dist):
         print(json.dumps(line), flush=True)
 
 
+def gdn_config(prob, name, world):
+    return {"workload": name, "T": prob["T"], "R": prob["R"], "Hk": prob["q"].shape[1], "Hv": prob["v"].shape[1],
+            "K": prob["q"].shape[2], "V": prob["v"].shape[2], "chunk": 64, "l2norm": bool(prob["l2norm"]),
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "q, k, v and o together larger than L2 (no flush)"}
+
+
+def gdn_cost(prob):
+    """Bytes one GDN prefill must move: q, k, v, o in their dtype, g and beta (fp32),
+    the initial states read and every state written (fp32); and its algorithmic
+    flops: per token and value head K*L (the two masked L x L products, half each)
+    + 3*K*V (K S0, Q S0, K^T U) + L*V/2 (P U), times 2, with L = 64."""
+    T, R = prob["T"], prob["R"]
+    Hk, K = prob["q"].shape[1], prob["q"].shape[2]
+    Hv, V = prob["v"].shape[1], prob["v"].shape[2]
+    el = prob["q"].element_size()
+    states = R if prob.get("final_dense", True) else 0
+    if prob.get("init_slots") is not None:
+        states += int((prob["init_slots"] >= 0).sum().item())
+    if prob.get("final_slots") is not None:
+        states += int((prob["final_slots"] >= 0).sum().item())
+    if prob.get("block_table") is not None:
+        states += int((prob["block_table"] >= 0).sum().item())
+    byt = T * (2 * Hk * K + 2 * Hv * V) * el + T * Hv * 8 + states * Hv * K * V * 4
+    flops = 2 * T * Hv * (K * 64 + 3 * K * V + 64 * V // 2)
+    return {"bytes": byt, "flops": flops}
+
+
+def run_gdn_bench(args, rank, local_rank, world, dist):
+    """The gated-delta-rule prefill (ssd_varlen_gdn_forward), timed like the forward."""
+    import torch
+    import mamba2_ssd_varlen_gb300 as m
+    import workloads
+    peaks = load_peaks()
+    prob = workloads.make_gdn_problem(args.config, device="cuda")
+    call = m.GdnCall(prob)
+    stream = torch.cuda.current_stream()
+    cost = gdn_cost(prob)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert call.status() == 0, "device error during warm-up"
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(K):
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    assert call.status() == 0, "device error during the timed region"
+    k_avg = sum(a.elapsed_time(b) for a, b in ev) / K
+    T = prob["T"]
+    hosts = {key: prob[key].cpu().pin_memory() for key in ("q", "k", "v", "g", "beta")}
+    o_host = torch.empty(call.o.shape, dtype=call.o.dtype, pin_memory=True)
+
+    def e2e_step():
+        for key, t in hosts.items():
+            prob[key].copy_(t, non_blocking=True)
+        call()
+        o_host.copy_(call.o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.e2e_steps
+    achieved = cost["bytes"] / (k_avg / 1e3) / 1e9
+    line = {"metric": GDN_METRIC, "value": T * world / (k_avg / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": k_avg, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": gdn_config(prob, args.config, world),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"], "algorithmic_bytes": cost["bytes"],
+                         "tensor_tflops": round(cost["flops"] / (k_avg / 1e3) / 1e12, 1),
+                         "kernel": "ssd_varlen_gdn_forward", "kernel_ms_avg": round(k_avg, 5)},
+            "gpu_launches": K, "clocks": clocks,
+            "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts.values()),
+                    "d2h_bytes_per_step": o_host.numel() * o_host.element_size()}}
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample = gdn_oracle_sample(workloads.make_gdn_problem(args.config, device="cpu"), 10.0)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,8 +657,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     m.load_library()
-    if args.config in workloads.DECODE_CONFIGS or args.config in workloads.CONV_CONFIGS:
-        bench_fn = run_decode_bench if args.config in workloads.DECODE_CONFIGS else run_conv_bench
+    if (args.config in workloads.DECODE_CONFIGS or args.config in workloads.CONV_CONFIGS
+            or args.config in workloads.GDN_CONFIGS):
+        bench_fn = (run_decode_bench if args.config in workloads.DECODE_CONFIGS else
+                    run_conv_bench if args.config in workloads.CONV_CONFIGS else run_gdn_bench)
         bench_fn(args, rank, local_rank, world, dist)
         if dist:
             dist.destroy_process_group()

@@ -289,6 +289,67 @@ typedef struct ssd_conv_io {
 int ssd_varlen_conv1d(const ssd_conv_dims *dims, const int32_t *cu_seqlens, const ssd_conv_io *io,
                       cudaStream_t stream);
 
+/* ---- Gated delta rule (GDN) chunked prefill with state export --------------
+ * "Automatic prefix caching for GDN hybrid models (mamba_cache_mode=all) with
+ * MTP speculative decoding", Purpose (Kernels/layers): the gated-delta-rule
+ * layers of GDN hybrid models run through a chunk kernel that exports per-chunk
+ * intermediate states, checkpointed by the same block-aligned scatter as the
+ * Mamba2 path.  The pages print no formula; this is the published gated delta
+ * rule ("Gated Delta Networks: Improving Mamba2 with Delta Rule"), state S a
+ * K x V matrix per value head h, key head h / (Hv/Hk), per token t in order:
+ *     q~, k~ = q_t, k_t   (or x / sqrt(|x|^2 + 1e-6) each, when dims.l2norm)
+ *     S  <- exp(g_t) S;   u = beta_t (v_t - S^T k~);   S <- S + k~ u^T
+ *     o_t = scale * S^T q~
+ * with S from state_pool[init_slots[i]] (zeros when < 0 or NULL).  Chunks are
+ * cut at absolute multiples of chunk_size (positions counted from
+ * num_computed[i]); state outputs follow the forward's rules: chunk_states row
+ * first_chunk[i] + j = the state after chunk j (rows as
+ * ssd_varlen_count_chunks with chunk_size), block checkpoints through
+ * block_table (state after absolute token kb-1 for every multiple kb of
+ * block_size in (s, s+L], entries < 0 skipped), final states to final_states[i]
+ * and state_pool[final_slots[i]].  An empty request's final state is its
+ * initial state.
+ *
+ * Supported: bf16 q, k, v, o; K = 128; V a multiple of 32 up to 256;
+ * chunk_size = 64; block_size a multiple of 64 (or 0 without a block table).
+ * g and beta fp32, g <= 0 expected (a decay).  Write slots must not alias read
+ * slots of the same call.  Host-visible violations return SSD_ERR_* before any
+ * launch; device_err (one int32, required) receives SSD_DEVERR_* bits
+ * (CU_SEQLENS, NUM_COMPUTED, INIT_SLOT, FINAL_SLOT, BLOCK_SLOT, BLOCK_TABLE),
+ * the offending writes skipped.  One launch on `stream`; allocates nothing. */
+typedef struct ssd_gdn_dims {
+    int64_t T;               /* total tokens, >= 0 */
+    int32_t R;               /* requests, >= 1 */
+    int32_t Hk, Hv;          /* key heads, value heads (a multiple of Hk) */
+    int32_t K, V;            /* key and value head dims */
+    int32_t chunk_size;      /* 64 */
+    int32_t block_size;      /* block-checkpoint granularity, or 0 */
+    int32_t block_table_width;
+    int32_t dtype;           /* enum ssd_dtype of q, k, v and o */
+    int32_t num_slots;       /* rows of state_pool (0 without a pool) */
+    int32_t l2norm;          /* 1: q and k l2-normalised per token inside the kernel */
+    float scale;             /* output scale; 0 means K^-1/2 */
+} ssd_gdn_dims;
+
+typedef struct ssd_gdn_io {
+    const void *q, *k;           /* (T,Hk,K) */
+    const void *v;               /* (T,Hv,V) */
+    const float *g;              /* (T,Hv) log decay per token and value head */
+    const float *beta;           /* (T,Hv) write strength */
+    const int32_t *num_computed; /* (R) tokens already in each request's state, or NULL */
+    float *state_pool;           /* (num_slots,Hv,K,V) fp32, or NULL */
+    const int32_t *init_slots;   /* (R) or NULL */
+    const int32_t *final_slots;  /* (R) or NULL */
+    const int32_t *block_table;  /* (R, block_table_width) or NULL */
+    void *o;                     /* (T,Hv,V) */
+    float *final_states;         /* (R,Hv,K,V) or NULL */
+    float *chunk_states;         /* (n_chunks,Hv,K,V) or NULL */
+    int32_t *device_err;         /* one int32, OR-ed with SSD_DEVERR_* bits */
+} ssd_gdn_io;
+
+int ssd_varlen_gdn_forward(const ssd_gdn_dims *dims, const int32_t *cu_seqlens, const ssd_gdn_io *io,
+                           cudaStream_t stream);
+
 /* ---- Block-aligned prefill bites (host only) --------------------------------
  * "Automatic prefix caching for GDN hybrid models (mamba_cache_mode=all) with
  * MTP speculative decoding", Purpose (engine core: kernel-chunk-aligned prefill

@@ -16,6 +16,7 @@ The functions keep the C names:
   ssd_varlen_decode(dims, cu_seqlens, io)        (decode / speculative-decode step)
   ssd_varlen_conv1d(dims, cu_seqlens, io)        (varlen causal conv1d with conv-state anchors)
   ssd_varlen_align_bite(start, end, total, align) (block-aligned prefill bite, host)
+  ssd_varlen_gdn_forward(dims, cu_seqlens, io)   (gated delta rule prefill by chunks)
 and ``run(...)`` wires a whole call from torch tensors (tests and bench use it).
 """
 from __future__ import annotations
@@ -40,7 +41,7 @@ STATUS = {
 EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
             "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror",
             "ssd_varlen_forward_static", "ssd_varlen_decode", "ssd_varlen_conv1d",
-            "ssd_varlen_align_bite"]
+            "ssd_varlen_align_bite", "ssd_varlen_gdn_forward"]
 # Size of the library-owned scratch array used by ssd_varlen_forward_static.
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -87,6 +88,18 @@ class ssd_conv_io(ctypes.Structure):
                 ("write_slots", c_vp), ("y", c_vp), ("device_err", c_vp)]
 
 
+class ssd_gdn_dims(ctypes.Structure):
+    _fields_ = [("T", c_i64), ("R", c_i32), ("Hk", c_i32), ("Hv", c_i32), ("K", c_i32), ("V", c_i32),
+                ("chunk_size", c_i32), ("block_size", c_i32), ("block_table_width", c_i32), ("dtype", c_i32),
+                ("num_slots", c_i32), ("l2norm", c_i32), ("scale", ctypes.c_float)]
+
+
+class ssd_gdn_io(ctypes.Structure):
+    _fields_ = [("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("beta", c_vp), ("num_computed", c_vp),
+                ("state_pool", c_vp), ("init_slots", c_vp), ("final_slots", c_vp), ("block_table", c_vp),
+                ("o", c_vp), ("final_states", c_vp), ("chunk_states", c_vp), ("device_err", c_vp)]
+
+
 class SsdError(RuntimeError):
     def __init__(self, code, what):
         super().__init__(f"{what}: {STATUS.get(code, code)} ({ssd_varlen_strerror(code)})")
@@ -129,6 +142,8 @@ def load_library():
     lib.ssd_varlen_conv1d.restype = ctypes.c_int
     lib.ssd_varlen_align_bite.argtypes = [c_i64, c_i64, c_i64, c_i32]
     lib.ssd_varlen_align_bite.restype = c_i64
+    lib.ssd_varlen_gdn_forward.argtypes = [ctypes.POINTER(ssd_gdn_dims), c_vp, ctypes.POINTER(ssd_gdn_io), c_vp]
+    lib.ssd_varlen_gdn_forward.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -362,3 +377,64 @@ def ssd_varlen_align_bite(start: int, end: int, total: int, align: int) -> int:
     if r < 0:
         raise SsdError(r, "ssd_varlen_align_bite")
     return r
+
+
+GDN_CHUNK = 64  # the chunk length of the GDN kernel
+
+
+def ssd_varlen_gdn_forward(dims: ssd_gdn_dims, cu_seqlens, io: ssd_gdn_io, stream=None):
+    rc = load_library().ssd_varlen_gdn_forward(ctypes.byref(dims), _ptr(cu_seqlens), ctypes.byref(io),
+                                                _stream(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_gdn_forward")
+
+
+class GdnCall:
+    """One GDN prefill over a problem from workloads.make_gdn_problem: outputs (o,
+    final_states, chunk_states when asked), the device error word, and the pre-built
+    argument structs (so a bench can call it repeatedly)."""
+
+    def __init__(self, prob: dict, stream=None):
+        import torch
+        self.prob = prob
+        q, v = prob["q"], prob["v"]
+        T, Hk, K = q.shape
+        Hv, V = v.shape[1], v.shape[2]
+        R = prob["cu_seqlens"].shape[0] - 1
+        pool = prob.get("state_pool")
+        bt = prob.get("block_table")
+        dev = q.device
+        self.final_states = (torch.empty((R, Hv, K, V), dtype=torch.float32, device=dev)
+                             if prob.get("final_dense", True) else None)
+        self.chunk_states = None
+        if prob.get("export_chunks"):
+            nc = prob.get("num_computed")
+            n = ssd_varlen_count_chunks(prob["cu_seqlens"].cpu().numpy(),
+                                        None if nc is None else nc.cpu().numpy(), GDN_CHUNK)
+            self.chunk_states = torch.empty((max(n, 1), Hv, K, V), dtype=torch.float32, device=dev)
+        self.o = torch.empty_like(v)
+        self.err = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.dims = ssd_gdn_dims(T, R, Hk, Hv, K, V, GDN_CHUNK, int(prob.get("block_size") or 0),
+                                 0 if bt is None else bt.shape[1],
+                                 DTYPE_F32 if q.dtype == torch.float32 else DTYPE_BF16,
+                                 0 if pool is None else pool.shape[0], 1 if prob.get("l2norm") else 0,
+                                 float(prob.get("scale") or 0.0))
+        self.io = ssd_gdn_io(_ptr(q), _ptr(prob["k"]), _ptr(v), _ptr(prob["g"]), _ptr(prob["beta"]),
+                             _ptr(prob.get("num_computed")), _ptr(pool), _ptr(prob.get("init_slots")),
+                             _ptr(prob.get("final_slots")), _ptr(bt), _ptr(self.o), _ptr(self.final_states),
+                             _ptr(self.chunk_states), _ptr(self.err))
+        self.stream = stream
+
+    def __call__(self):
+        ssd_varlen_gdn_forward(self.dims, self.prob["cu_seqlens"], self.io, self.stream)
+        return self
+
+    def status(self) -> int:
+        v = int(self.err[0].item())
+        self.err.zero_()
+        return v
+
+
+def run_gdn(prob: dict, **kw) -> GdnCall:
+    """One GDN prefill on the current stream; returns the GdnCall (outputs on it)."""
+    return GdnCall(prob, **kw)()

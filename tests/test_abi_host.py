@@ -195,3 +195,53 @@ def test_conv_rejects_bad_pointers(lib, field, value, code):
     d = m.ssd_conv_dims(8, 2, 64, 4, m.DTYPE_BF16, 4, 1)
     io = _conv_io(**{field: value})
     assert lib.ssd_varlen_conv1d(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == code
+
+
+# ---- gated delta rule prefill: host validation -------------------------------
+def _gdn_io(**kw):
+    f = ctypes.c_void_p(_FAKE)
+    fields = dict(q=f, k=f, v=f, g=f, beta=f, num_computed=None, state_pool=f, init_slots=f, final_slots=f,
+                  block_table=None, o=f, final_states=f, chunk_states=None, device_err=f)
+    fields.update(kw)
+    return m.ssd_gdn_io(*[fields[n] for n, _ in m.ssd_gdn_io._fields_])
+
+
+def _gdn_dims(**kw):
+    base = dict(T=64, R=2, Hk=2, Hv=4, K=128, V=64, chunk_size=64, block_size=0, block_table_width=0,
+                dtype=m.DTYPE_BF16, num_slots=8, l2norm=1, scale=0.0)
+    base.update(kw)
+    return m.ssd_gdn_dims(*[base[n] for n, _ in m.ssd_gdn_dims._fields_])
+
+
+def test_gdn_struct_sizes():
+    assert ctypes.sizeof(m.ssd_gdn_dims) == 8 + 12 * 4
+    assert ctypes.sizeof(m.ssd_gdn_io) == 14 * 8
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(R=0), -2), (dict(T=-1), -2), (dict(Hk=0), -2), (dict(num_slots=-1), -2), (dict(Hv=6, Hk=4), -4),
+    (dict(dtype=7), -6), (dict(dtype=m.DTYPE_F32), -11), (dict(K=64), -11), (dict(V=48), -11), (dict(V=512), -11),
+    (dict(chunk_size=128), -11),
+])
+def test_gdn_rejects_bad_dims(lib, kw, code):
+    d = _gdn_dims(**kw)
+    assert lib.ssd_varlen_gdn_forward(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(_gdn_io()), None) == code
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("q", None, -1), ("k", None, -1), ("v", None, -1), ("g", None, -1), ("beta", None, -1), ("o", None, -1),
+    ("device_err", None, -1), ("state_pool", None, -1),
+    ("q", ctypes.c_void_p(_FAKE + 8), -7), ("final_states", ctypes.c_void_p(_FAKE + 4), -7),
+    ("beta", ctypes.c_void_p(_FAKE + 2), -7),
+])
+def test_gdn_rejects_bad_pointers(lib, field, value, code):
+    io = _gdn_io(**{field: value})
+    assert lib.ssd_varlen_gdn_forward(ctypes.byref(_gdn_dims()), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == code
+    assert lib.ssd_varlen_gdn_forward(ctypes.byref(_gdn_dims()), None, ctypes.byref(io), None) == -1
+
+
+def test_gdn_block_table_needs_a_chunk_multiple_block_size(lib):
+    io = _gdn_io(block_table=ctypes.c_void_p(_FAKE))
+    for bs in (0, 96):
+        d = _gdn_dims(block_size=bs, block_table_width=4)
+        assert lib.ssd_varlen_gdn_forward(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == -5

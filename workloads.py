@@ -481,3 +481,133 @@ def to_oracle_conv(prob: dict, channels=None) -> dict:
             "conv_pool": cols(prob["conv_pool"], 1),
             "read_slots": prob["read_slots"].detach().to("cpu").numpy(),
             "write_slots": prob["write_slots"].detach().to("cpu").numpy(), "silu": prob["silu"]}
+
+
+# ---- gated delta rule (GDN) prefill ------------------------------------------
+# Value recipe: q, k, v ~ N(0, 1) (q and k are l2-normalised inside the method
+# when l2norm is set); per value head a decay rate a_h = exp(U(0, ln 16)) and
+# g = -a_h * softplus(N(0, 1) - 4) (log decays of about -0.005 to -1); beta =
+# sigmoid(N(0, 1)); initial states N(0, 0.5^2).  Layouts: q, k (T,Hk,K); v, o
+# (T,Hv,V); g, beta (T,Hv) fp32; states (..., Hv, K, V) fp32.
+
+@dataclass
+class GdnSpec:
+    name: str
+    Hk: int
+    Hv: int
+    K: int
+    V: int
+    lengths: list
+    dtype: str = "bf16"
+    l2norm: bool = True
+    init: str = "none"          # "none" or "all" (every request reads a slot)
+    final_slots: bool = False
+    export_chunks: bool = False
+    block_size: int = 0
+    final_dense: bool = True
+
+
+GDN_CONFIGS: dict[str, GdnSpec] = {
+    "gdn_small": GdnSpec("gdn_small", Hk=2, Hv=4, K=128, V=64, lengths=[37, 64, 1, 130, 0, 200],
+                         init="all", final_slots=True, export_chunks=True, block_size=128),
+    # the uniform 8 x 2048 token layout in a GDN layer shape: 16 key heads, 32 value
+    # heads, 128 x 128 state per value head
+    "gdn_uniform_8x2048": GdnSpec("gdn_uniform_8x2048", Hk=16, Hv=32, K=128, V=128, lengths=[2048] * 8),
+}
+GDN_SEED = {"gdn_small": 300, "gdn_uniform_8x2048": 301}
+
+
+def make_gdn_problem(spec: GdnSpec | str, seed: int | None = None, device="cpu", lengths=None,
+                     num_computed=None, canary: float | None = None):
+    """Draw one GDN prefill.  With init "all" every request reads a distinct slot;
+    final slots and block-table slots are distinct from them and from each other
+    (unused pool slots hold ``canary``)."""
+    if isinstance(spec, str):
+        spec = GDN_CONFIGS[spec]
+    if seed is None:
+        seed = GDN_SEED.get(spec.name, 0)
+    lens = list(lengths) if lengths is not None else list(spec.lengths)
+    R, T = len(lens), int(sum(lens))
+    Hk, Hv, K, V = spec.Hk, spec.Hv, spec.K, spec.V
+    dt_ = torch.float32 if spec.dtype == "fp32" else torch.bfloat16
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    rng = np.random.default_rng(seed + 1000)
+    cu = torch.zeros(R + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    prob = {"spec": spec.name, "lengths": lens, "T": T, "R": R, "cu_seqlens": cu.to(dev),
+            "block_size": spec.block_size, "export_chunks": spec.export_chunks, "l2norm": spec.l2norm,
+            "final_dense": spec.final_dense, "scale": None}
+    prob["q"] = _randn((T, Hk, K), gen, dev, dt_)
+    prob["k"] = _randn((T, Hk, K), gen, dev, dt_)
+    prob["v"] = _randn((T, Hv, V), gen, dev, dt_)
+    rate = torch.exp(torch.rand((Hv,), generator=gen, device=dev) * math.log(16.0))
+    prob["g"] = -rate * torch.nn.functional.softplus(_randn((T, Hv), gen, dev, torch.float32) - 4.0)
+    prob["beta"] = torch.sigmoid(_randn((T, Hv), gen, dev, torch.float32))
+    ncomp = list(num_computed) if num_computed is not None else [0] * R
+    prob["num_computed"] = (torch.tensor(ncomp, dtype=torch.int32, device=dev)
+                            if num_computed is not None else None)
+    init_slots = final_slots = block_table = pool = None
+    if spec.init == "all" or spec.final_slots or spec.block_size:
+        bs = spec.block_size
+        W = max(1, max((ncomp[i] + lens[i]) // bs for i in range(R))) if bs else 0
+        S = 2 * R + (R * W if bs else 0) + 4
+        perm = rng.permutation(S)
+        used = 0
+        if spec.init == "all":
+            init_slots = [int(v) for v in perm[:R]]
+            used = R
+        if spec.final_slots:
+            final_slots = [int(v) for v in perm[used:used + R]]
+            used += R
+        if bs:
+            block_table = np.full((R, W), -1, dtype=np.int32)
+            for i in range(R):
+                for j in range(ncomp[i] // bs, (ncomp[i] + lens[i]) // bs):
+                    block_table[i, j] = int(perm[used])
+                    used += 1
+        pool = torch.full((S, Hv, K, V), 0.0 if canary is None else canary, dtype=torch.float32, device=dev)
+        for s in (init_slots or []):
+            pool[s] = _randn((Hv, K, V), gen, dev, torch.float32, 0.5)
+    prob["state_pool"] = pool
+    prob["init_slots"] = None if init_slots is None else torch.tensor(init_slots, dtype=torch.int32, device=dev)
+    prob["final_slots"] = None if final_slots is None else torch.tensor(final_slots, dtype=torch.int32, device=dev)
+    prob["block_table"] = None if block_table is None else torch.from_numpy(block_table).to(dev)
+    return prob
+
+
+def to_oracle_gdn(prob: dict, requests=None, heads=None) -> dict:
+    """Host float64 copies of a GDN problem, in the form oracle.gdn.gdn_forward takes.
+    With ``requests`` / ``heads`` only those are copied (requests repacked in order;
+    each selected value head gets its own copy of its key head's q and k; slots,
+    num_computed and the block table follow the selected requests)."""
+    def f64(t):
+        return None if t is None else t.detach().to("cpu").to(torch.float64).numpy()
+
+    Hk, Hv = prob["q"].shape[1], prob["v"].shape[1]
+    cu = prob["cu_seqlens"].detach().to("cpu").to(torch.int64).numpy()
+    sel = list(range(len(cu) - 1)) if requests is None else [int(i) for i in requests]
+    toks = torch.tensor([t for i in sel for t in range(int(cu[i]), int(cu[i + 1]))], dtype=torch.long)
+    new_cu = np.zeros(len(sel) + 1, dtype=np.int64)
+    new_cu[1:] = np.cumsum([int(cu[i + 1] - cu[i]) for i in sel])
+    hsel = list(range(Hv)) if heads is None else [int(h) for h in heads]
+    kidx = torch.tensor([h // (Hv // Hk) for h in hsel] if heads is not None else list(range(Hk)), dtype=torch.long)
+    hidx = torch.tensor(hsel, dtype=torch.long)
+
+    def take(t, key=False):
+        return f64(t.detach().to("cpu")[toks].index_select(1, kidx if key else hidx))
+
+    def pick(t):
+        return None if t is None else t.detach().to("cpu").numpy()[sel]
+
+    pool = prob.get("state_pool")
+    out = {"q": take(prob["q"], True), "k": take(prob["k"], True), "v": take(prob["v"]),
+           "g": take(prob["g"]), "beta": take(prob["beta"]), "cu_seqlens": new_cu,
+           "num_computed": pick(prob.get("num_computed")), "chunk_size": 64,
+           "block_size": prob.get("block_size") or 0, "block_table": pick(prob.get("block_table")),
+           "state_pool": None if pool is None else f64(pool.detach().to("cpu").index_select(1, hidx)),
+           "init_slots": pick(prob.get("init_slots")), "final_slots": pick(prob.get("final_slots")),
+           "export_chunks": bool(prob.get("export_chunks")), "scale": prob.get("scale"),
+           "l2norm": bool(prob.get("l2norm")), "requests": sel, "heads": hsel, "tokens": toks.numpy()}
+    return out
