@@ -16,8 +16,9 @@
 // fp32 accumulation).  q, k, v are bf16 and enter exactly; the fp32 operands
 // (S0, P, U) are split into a bf16 high part and a bf16 remainder, and the
 // products that involve them are summed from hi*hi + hi*lo (+ lo*hi), which keeps
-// about 16 mantissa bits.  The unit-lower solve runs on the CUDA cores in fp32
-// (one lane per value column).
+// about 16 mantissa bits.  The unit-lower solve runs on the CUDA cores in fp32,
+// by 16-row blocks: each warp inverts one diagonal block, then every warp
+// substitutes block by block for its own value columns.
 //
 // A CTA owns one (request, value head, 32-column slice of V) and walks the
 // request's chunks in order, the state slice in registers (warp w holds rows
@@ -33,9 +34,12 @@ constexpr int kL = 64;        // chunk length
 constexpr int kK = 128;       // key head dim
 constexpr int kBV = 32;       // value columns per CTA
 constexpr int kThreads = 128; // four warps
-constexpr int kLdK = kK + 8;  // bf16 row stride of the K / Q tiles and of S0^T (272 bytes)
-constexpr int kLdA = kL + 4;  // fp32 row stride of A and of R^T / U^T
+constexpr int kLdK = kK + 8;  // bf16 row stride of the K / Q tiles (272 bytes)
+constexpr int kLdA = kL + 4;  // fp32 row stride of A
+constexpr int kLdU = kL + 1;  // fp32 row stride of R^T / U^T (a column per lane: conflict-free)
 constexpr int kLdP = kL + 8;  // bf16 row stride of P and of U^T (144 bytes)
+constexpr int kLdS = kBV + 8; // bf16 row stride of S0 [k][v] (80 bytes)
+constexpr int kLdT = 20;      // fp32 row stride of the inverted diagonal blocks
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct GdnParams {
@@ -52,11 +56,12 @@ struct GdnSmem {
     float a[kL * kLdA];           // A [s][r]; after the solve: U' hi/lo [v][s] (bf16)
     __nv_bfloat16 ph[kL * kLdP];  // P hi [t][s]
     __nv_bfloat16 pl[kL * kLdP];  // P lo
-    float ut[kBV * kLdA];         // R^T, solved in place into U^T [v][s]
+    float ut[kBV * kLdU];         // R^T, solved in place into U^T [v][s]
+    float tb[kL * kLdT];          // (I + A_bb)^-1 of the four 16 x 16 diagonal blocks, rows 16b..
     __nv_bfloat16 uh[kBV * kLdP]; // U^T hi [v][s]
     __nv_bfloat16 ul[kBV * kLdP]; // U^T lo
-    __nv_bfloat16 sh[kBV * kLdK]; // S0^T hi [v][k]
-    __nv_bfloat16 sl[kBV * kLdK]; // S0^T lo
+    __nv_bfloat16 sh[kK * kLdS];  // S0 hi [k][v]
+    __nv_bfloat16 sl[kK * kLdS];  // S0 lo
     float gl2[kL];                // G * log2 e, inclusive prefix sums
     float beta[kL];
     float rk[kL], rq[kL];         // per-row l2 scale factors of k and q (1 without l2norm)
@@ -93,10 +98,6 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
     hi = *reinterpret_cast<const uint32_t *>(&h);
     lo = *reinterpret_cast<const uint32_t *>(&l);
-}
-__device__ __forceinline__ void split1(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
 __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_constant__ GdnParams p) {
@@ -163,16 +164,19 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                     st[mt][nt][2 * hh + 1] = val.y;
                 }
     }
-    // S0^T hi/lo for the products of the next chunk
+    // S0 hi/lo for the products of the next chunk
     auto publish_state = [&]() {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kr = 32 * warp + 16 * mt + gq + 8 * (e >> 1), vc = 8 * nt + 2 * cq + (e & 1);
-                    split1(st[mt][nt][e], s.sh[vc * kLdK + kr], s.sl[vc * kLdK + kr]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int kr = 32 * warp + 16 * mt + gq + 8 * hh, vc = 8 * nt + 2 * cq;
+                    uint32_t hi, lo;
+                    split2(st[mt][nt][2 * hh], st[mt][nt][2 * hh + 1], hi, lo);
+                    *reinterpret_cast<uint32_t *>(s.sh + kr * kLdS + vc) = hi;
+                    *reinterpret_cast<uint32_t *>(s.sl + kr * kLdS + vc) = lo;
                 }
     };
     auto write_state = [&](float *dst) {
@@ -245,30 +249,27 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
             s.gl2[2 * lane] = excl + x0;
             s.gl2[2 * lane + 1] = incl;
         }
-#pragma unroll 1
-        for (int r = m0; r < m0 + 16; ++r) {
-            float rk = 1.f, rq = 1.f;
+        {  // one row per lane: lanes 0-15 the k rows m0.., lanes 16-31 the q rows
+            const int r = m0 + (lane & 15);
+            const __nv_bfloat16 *row = (lane < 16 ? s.k : s.q) + r * kLdK;
+            float f = 1.f;
             if (p.l2norm) {
-                const uint2 kv = *reinterpret_cast<const uint2 *>(s.k + r * kLdK + 4 * lane);
-                const uint2 qv = *reinterpret_cast<const uint2 *>(s.q + r * kLdK + 4 * lane);
-                const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kv.x));
-                const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kv.y));
-                const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qv.x));
-                const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qv.y));
-                float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
-                float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+                float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                for (int c = 0; c < kK; c += 8) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(row + c);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+                        ss0 = fmaf(lo, lo, ss0);
+                        ss1 = fmaf(hi, hi, ss1);
+                    }
                 }
-                rk = rsqrtf(sk + 1e-6f);
-                rq = rsqrtf(sq + 1e-6f);
+                f = rsqrtf(ss0 + ss1 + 1e-6f);
             }
-            if (lane == 0) {
-                s.rk[r] = rk;
-                s.rq[r] = rq;
-            }
+            if (lane < 16) s.rk[r] = f;
+            else s.rq[r] = f;
         }
         __syncthreads();
 
@@ -318,6 +319,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                     *reinterpret_cast<uint32_t *>(s.pl + row * kLdP + col) = lo;
                 }
             }
+            // (I + A_bb)^-1 of this warp's diagonal block (its own rows and columns of A):
+            // lane j < 16 solves for column j by forward substitution
+            __syncwarp();
+            if (lane < 16) {
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float *arow = s.a + (m0 + r) * kLdA + m0;
+                    float acc = r == lane ? 1.f : 0.f;
+#pragma unroll
+                    for (int c = 0; c < r; ++c) acc = fmaf(-arow[c], x[c], acc);
+                    x[r] = acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) s.tb[(m0 + r) * kLdT + lane] = x[r];
+            }
         }
 
         // ---- K S0 -> R = diag(beta)(V - diag(gamma rk) K S0) into R^T; Q S0 kept for O
@@ -336,9 +353,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
 #pragma unroll
                 for (int np = 0; np < 2; ++np) {
                     uint32_t bh[4], bl[4];
-                    const int off = (16 * np + (lane & 7) + ((lane >> 4) << 3)) * kLdK + kk * 16 + ((lane >> 3) & 1) * 8;
-                    ldsm_x4(bh, s.sh + off);
-                    ldsm_x4(bl, s.sl + off);
+                    const int mat = lane >> 3;
+                    const int off = (kk * 16 + (lane & 7) + ((mat & 1) << 3)) * kLdS + 16 * np + ((mat >> 1) << 3);
+                    ldsm_x4_t(bh, s.sh + off);
+                    ldsm_x4_t(bl, s.sl + off);
                     mma_bf16(acc_r[2 * np], fk, bh[0], bh[1]);
                     mma_bf16(acc_r[2 * np], fk, bl[0], bl[1]);
                     mma_bf16(acc_r[2 * np + 1], fk, bh[2], bh[3]);
@@ -356,43 +374,78 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                     const int row = m0 + gq + 8 * hh, col = 8 * nt + 2 * cq;
                     const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vraw[nt][hh]));
                     const float w = exp2f(s.gl2[row]) * s.rk[row], bt = s.beta[row];
-                    s.ut[col * kLdA + row] = bt * (vv.x - w * acc_r[nt][2 * hh]);
-                    s.ut[(col + 1) * kLdA + row] = bt * (vv.y - w * acc_r[nt][2 * hh + 1]);
+                    s.ut[col * kLdU + row] = bt * (vv.x - w * acc_r[nt][2 * hh]);
+                    s.ut[(col + 1) * kLdU + row] = bt * (vv.y - w * acc_r[nt][2 * hh + 1]);
                 }
         }
         __syncthreads();
 
-        // ---- unit-lower solve (I + A) U = R, one lane per value column (warp 0)
-        if (warp == 0) {
-            float u[kL];
-            const float *rcol = s.ut + lane * kLdA;
+        // ---- unit-lower solve (I + A) U = R by 16-row blocks b = 0..3:
+        //   U_b = (I + A_bb)^-1 (R_b - A_{b,<b} U_{<b})
+        // warp w owns value columns 8w..8w+7, four lanes per column, lane quarter q the
+        // rows 4q..4q+3 of each block; the columns are independent, so only the warp syncs.
+        {
+            const int vcol = 8 * warp + (lane >> 2), qr = 4 * (lane & 3);
+            float *ucol = s.ut + vcol * kLdU;
 #pragma unroll
-            for (int r = 0; r < kL; ++r) {
-                const float *arow = s.a + r * kLdA;
-                float acc0 = rcol[r], acc1 = 0.f;
+            for (int bk = 0; bk < kL / 16; ++bk) {
+                float rr[4];
 #pragma unroll
-                for (int c = 0; c < r; c += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + c);
-                    acc0 -= a4.x * u[c];
-                    if (c + 1 < r) acc1 -= a4.y * u[c + 1];
-                    if (c + 2 < r) acc0 -= a4.z * u[c + 2];
-                    if (c + 3 < r) acc1 -= a4.w * u[c + 3];
+                for (int e = 0; e < 4; ++e) {
+                    const int sr = 16 * bk + qr + e;
+                    const float *arow = s.a + sr * kLdA;
+                    float acc0 = ucol[sr], acc1 = 0.f;
+#pragma unroll
+                    for (int r = 0; r < 16 * bk; r += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(arow + r);
+                        acc0 = fmaf(-a4.x, ucol[r], acc0);
+                        acc1 = fmaf(-a4.y, ucol[r + 1], acc1);
+                        acc0 = fmaf(-a4.z, ucol[r + 2], acc0);
+                        acc1 = fmaf(-a4.w, ucol[r + 3], acc1);
+                    }
+                    rr[e] = acc0 + acc1;
                 }
-                u[r] = acc0 + acc1;
-            }
-            __syncwarp();  // every lane's reads of A are done before A's space is reused
-            const float gll = s.gl2[n - 1];
 #pragma unroll
-            for (int r = 0; r < kL; r += 2) {
+                for (int e = 0; e < 4; ++e) ucol[16 * bk + qr + e] = rr[e];
+                __syncwarp();
+                float uu[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float *trow = s.tb + (16 * bk + qr + e) * kLdT;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 16; c += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(trow + c);
+                        acc = fmaf(t4.x, ucol[16 * bk + c], acc);
+                        acc = fmaf(t4.y, ucol[16 * bk + c + 1], acc);
+                        acc = fmaf(t4.z, ucol[16 * bk + c + 2], acc);
+                        acc = fmaf(t4.w, ucol[16 * bk + c + 3], acc);
+                    }
+                    uu[e] = acc;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ucol[16 * bk + qr + e] = uu[e];
+                __syncwarp();
+            }
+        }
+        __syncthreads();  // U complete; A no longer read (its space takes U')
+
+        // ---- U and U' = diag(rk e^{G_L - G}) U as bf16 hi/lo, [v][s]
+        {
+            const float gll = s.gl2[n - 1];
+            for (int idx = tid; idx < kBV * (kL / 2); idx += kThreads) {
+                const int vc = idx / (kL / 2), r = (idx % (kL / 2)) * 2;
+                const float u0 = s.ut[vc * kLdU + r], u1 = s.ut[vc * kLdU + r + 1];
                 uint32_t hi, lo;
-                split2(u[r], u[r + 1], hi, lo);
-                *reinterpret_cast<uint32_t *>(s.uh + lane * kLdP + r) = hi;
-                *reinterpret_cast<uint32_t *>(s.ul + lane * kLdP + r) = lo;
+                split2(u0, u1, hi, lo);
+                *reinterpret_cast<uint32_t *>(s.uh + vc * kLdP + r) = hi;
+                *reinterpret_cast<uint32_t *>(s.ul + vc * kLdP + r) = lo;
                 const float w0 = s.rk[r] * exp2f(fminf(gll - s.gl2[r], 0.f));
                 const float w1 = s.rk[r + 1] * exp2f(fminf(gll - s.gl2[r + 1], 0.f));
-                split2(w0 * u[r], w1 * u[r + 1], hi, lo);
-                *reinterpret_cast<uint32_t *>(u2h + lane * kLdP + r) = hi;
-                *reinterpret_cast<uint32_t *>(u2l + lane * kLdP + r) = lo;
+                split2(w0 * u0, w1 * u1, hi, lo);
+                *reinterpret_cast<uint32_t *>(u2h + vc * kLdP + r) = hi;
+                *reinterpret_cast<uint32_t *>(u2l + vc * kLdP + r) = lo;
             }
         }
         __syncthreads();
