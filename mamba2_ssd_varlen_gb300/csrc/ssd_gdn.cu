@@ -36,7 +36,7 @@ constexpr int kBV = 32;       // value columns per CTA
 constexpr int kThreads = 128; // four warps
 constexpr int kLdK = kK + 8;  // bf16 row stride of the K / Q tiles (272 bytes)
 constexpr int kLdA = kL + 4;  // fp32 row stride of A
-constexpr int kLdU = kL + 1;  // fp32 row stride of R^T / U^T (a column per lane: conflict-free)
+constexpr int kLdU = kL + 4;  // fp32 row stride of R^T / U^T (eight columns x four rows: 32 banks)
 constexpr int kLdP = kL + 8;  // bf16 row stride of P and of U^T (144 bytes)
 constexpr int kLdS = kBV + 8; // bf16 row stride of S0 [k][v] (80 bytes)
 constexpr int kLdT = 20;      // fp32 row stride of the inverted diagonal blocks
@@ -383,16 +383,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
         // ---- unit-lower solve (I + A) U = R by 16-row blocks b = 0..3:
         //   U_b = (I + A_bb)^-1 (R_b - A_{b,<b} U_{<b})
         // warp w owns value columns 8w..8w+7, four lanes per column, lane quarter q the
-        // rows 4q..4q+3 of each block; the columns are independent, so only the warp syncs.
+        // rows q, q+4, q+8, q+12 of each block (neighbouring rows in one access: no
+        // bank conflicts); the columns are independent, so only the warp syncs.
         {
-            const int vcol = 8 * warp + (lane >> 2), qr = 4 * (lane & 3);
+            const int vcol = 8 * warp + (lane >> 2), qr = lane & 3;
             float *ucol = s.ut + vcol * kLdU;
 #pragma unroll
             for (int bk = 0; bk < kL / 16; ++bk) {
                 float rr[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int sr = 16 * bk + qr + e;
+                    const int sr = 16 * bk + 4 * e + qr;
                     const float *arow = s.a + sr * kLdA;
                     float acc0 = ucol[sr], acc1 = 0.f;
 #pragma unroll
@@ -406,12 +407,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                     rr[e] = acc0 + acc1;
                 }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ucol[16 * bk + qr + e] = rr[e];
+                for (int e = 0; e < 4; ++e) ucol[16 * bk + 4 * e + qr] = rr[e];
                 __syncwarp();
                 float uu[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float *trow = s.tb + (16 * bk + qr + e) * kLdT;
+                    const float *trow = s.tb + (16 * bk + 4 * e + qr) * kLdT;
                     float acc = 0.f;
 #pragma unroll
                     for (int c = 0; c < 16; c += 4) {
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                 }
                 __syncwarp();
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ucol[16 * bk + qr + e] = uu[e];
+                for (int e = 0; e < 4; ++e) ucol[16 * bk + 4 * e + qr] = uu[e];
                 __syncwarp();
             }
         }
