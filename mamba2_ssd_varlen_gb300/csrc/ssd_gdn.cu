@@ -65,6 +65,7 @@ struct GdnSmem {
     float gl2[kL];                // G * log2 e, inclusive prefix sums
     float beta[kL];
     float rk[kL], rq[kL];         // per-row l2 scale factors of k and q (1 without l2norm)
+    float wu[kL];                 // rk e^{G_L - G}: the row weights of U' in the state product
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -385,6 +386,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
         // warp w owns value columns 8w..8w+7, four lanes per column, lane quarter q the
         // rows q, q+4, q+8, q+12 of each block (neighbouring rows in one access: no
         // bank conflicts); the columns are independent, so only the warp syncs.
+        if (warp == 0) {
+            const float gll = s.gl2[n - 1];
+            s.wu[lane] = s.rk[lane] * exp2f(fminf(gll - s.gl2[lane], 0.f));
+            s.wu[lane + 32] = s.rk[lane + 32] * exp2f(fminf(gll - s.gl2[lane + 32], 0.f));
+        }
         {
             const int vcol = 8 * warp + (lane >> 2), qr = lane & 3;
             float *ucol = s.ut + vcol * kLdU;
@@ -434,7 +440,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
 
         // ---- U and U' = diag(rk e^{G_L - G}) U as bf16 hi/lo, [v][s]
         {
-            const float gll = s.gl2[n - 1];
             for (int idx = tid; idx < kBV * (kL / 2); idx += kThreads) {
                 const int vc = idx / (kL / 2), r = (idx % (kL / 2)) * 2;
                 const float u0 = s.ut[vc * kLdU + r], u1 = s.ut[vc * kLdU + r + 1];
@@ -442,9 +447,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                 split2(u0, u1, hi, lo);
                 *reinterpret_cast<uint32_t *>(s.uh + vc * kLdP + r) = hi;
                 *reinterpret_cast<uint32_t *>(s.ul + vc * kLdP + r) = lo;
-                const float w0 = s.rk[r] * exp2f(fminf(gll - s.gl2[r], 0.f));
-                const float w1 = s.rk[r + 1] * exp2f(fminf(gll - s.gl2[r + 1], 0.f));
-                split2(w0 * u0, w1 * u1, hi, lo);
+                split2(s.wu[r] * u0, s.wu[r + 1] * u1, hi, lo);
                 *reinterpret_cast<uint32_t *>(u2h + vc * kLdP + r) = hi;
                 *reinterpret_cast<uint32_t *>(u2l + vc * kLdP + r) = lo;
             }
