@@ -57,9 +57,17 @@ def load_peaks():
             "source": "fallback"}
 
 
-def kernel_source_hash():
+# The same for the kernels of the other rows (each bench line reports its own).
+ROW_KERNEL_SOURCES = {
+    "conv": ["mamba2_ssd_varlen_gb300/csrc/ssd_conv1d.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
+    "decode": ["mamba2_ssd_varlen_gb300/csrc/ssd_decode.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
+    "gdn": ["mamba2_ssd_varlen_gb300/csrc/ssd_gdn.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
+}
+
+
+def kernel_source_hash(files=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (KERNEL_SOURCES if files is None else files):
         h.update(os.path.basename(rel).encode())
         h.update(open(os.path.join(ROOT, rel), "rb").read())
     return h.hexdigest()[:16]
@@ -177,16 +185,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(loaded)}
 
 
-def read_traffic(kernel_hash):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
-    or None when the summary is absent or the kernel source changed since."""
+def read_traffic(kernel_hash, config=None):
+    """DRAM bytes per launch of a kernel from the committed ncu summaries, or None
+    when the figure is absent or the kernel source changed since.  Lines of the
+    other rows carry the workload they were measured (or scaled) for."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and parts[0] == "dram_bytes_per_launch":
-            if parts[2] == kernel_hash:
+            if parts[2] == kernel_hash and (config is None or (len(parts) >= 4 and parts[3] == config)):
                 return float(parts[1])
     return None
 
@@ -439,7 +448,7 @@ def run_decode_bench(args, rank, local_rank, world, dist):
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "l2": "state traffic larger than L2 (no flush)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": read_traffic(kernel_source_hash(ROW_KERNEL_SOURCES["decode"]), args.config),
                          "peak_source": peaks["source"], "algorithmic_bytes": cost["bytes"],
                          "kernel": "ssd_varlen_decode", "kernel_ms_avg": round(k_avg, 5)},
             "gpu_launches": K, "clocks": clocks,
@@ -521,7 +530,7 @@ def run_conv_bench(args, rank, local_rank, world, dist):
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "l2": "x and y each larger than L2 (no flush)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": read_traffic(kernel_source_hash(ROW_KERNEL_SOURCES["conv"]), args.config),
                          "peak_source": peaks["source"], "algorithmic_bytes": cost["bytes"],
                          "kernel": "ssd_varlen_conv1d", "kernel_ms_avg": round(k_avg, 5)},
             "gpu_launches": K, "clocks": clocks,
@@ -617,7 +626,7 @@ def run_gdn_bench(args, rank, local_rank, world, dist):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": gdn_config(prob, args.config, world),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": read_traffic(kernel_source_hash(ROW_KERNEL_SOURCES["gdn"]), args.config),
                          "peak_source": peaks["source"], "algorithmic_bytes": cost["bytes"],
                          "tensor_tflops": round(cost["flops"] / (k_avg / 1e3) / 1e12, 1),
                          "kernel": "ssd_varlen_gdn_forward", "kernel_ms_avg": round(k_avg, 5)},
