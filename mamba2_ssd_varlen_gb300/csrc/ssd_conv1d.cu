@@ -94,15 +94,46 @@ __device__ __forceinline__ int request_of(const int32_t *cu, int R, int64_t t) {
     return lo;
 }
 
-// SiLU as v * 1/(1 + 2^(-v log2 e)) on the special-function unit's base-2
-// exponential and reciprocal (both good to about 2^-22 relative), far finer
-// than the storage rounding that follows.  Very negative v gives 2^(..) = inf,
-// a reciprocal of 0 and a (signed) zero, as SiLU tends to.
-__device__ __forceinline__ float silu_sfu(float v) {
-    float e, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(v * -1.4426950408889634f));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
-    return v * r;
+// Packed fp32 pairs (one 64-bit register pair) for the f32x2 instructions: two
+// channels per fused multiply-add.
+__device__ __forceinline__ uint64_t pair(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ void unpair(uint64_t d, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// SiLU of a pair, v * 1/(1 + 2^(-v log2 e)): the scaling, the 1 + e and the
+// final product packed; the base-2 exponential and the reciprocal per value on
+// the special-function unit (both good to about 2^-22 relative, far finer than
+// the storage rounding that follows).  Very negative v gives 2^(..) = inf, a
+// reciprocal of 0 and a (signed) zero, as SiLU tends to.
+__device__ __forceinline__ uint64_t silu_pair(uint64_t v) {
+    float a, b;
+    unpair(mul2(v, pair(-1.4426950408889634f, -1.4426950408889634f)), a, b);
+    float ea, eb;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(a));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(b));
+    unpair(add2(pair(ea, eb), pair(1.f, 1.f)), a, b);
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(a));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(b));
+    return mul2(v, pair(ea, eb));
 }
 
 // 16-byte asynchronous global -> shared copy that bypasses L1 (the input is
@@ -232,11 +263,13 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const __grid_const
             win[W - 1].set(mine[st * kConvThreads]);
             Vec<T> out;
 #pragma unroll
-            for (int e = 0; e < kN; ++e) {
-                float acc = bs[e];
+            for (int e = 0; e < kN; e += 2) {  // two channels per packed instruction
+                uint64_t acc = pair(bs[e], bs[e + 1]);
 #pragma unroll
-                for (int k = 0; k < W; ++k) acc = fmaf(wt[k][e], win[k].v[e], acc);
-                out.v[e] = kSilu ? silu_sfu(acc) : acc;
+                for (int k = 0; k < W; ++k)
+                    acc = fma2(pair(wt[k][e], wt[k][e + 1]), pair(win[k].v[e], win[k].v[e + 1]), acc);
+                if (kSilu) acc = silu_pair(acc);
+                unpair(acc, out.v[e], out.v[e + 1]);
             }
             out.store(yt + (size_t)j * row);
             if (j + 1 == rel_end) {  // the request's last token: its conv state goes out
