@@ -92,6 +92,23 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// Packed fp32 pairs (one 64-bit register pair) for the f32x2 instructions.
+__device__ __forceinline__ uint64_t pair(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float pair_sum(uint64_t d) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+    return a + b;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // fp32 pair -> (bf16x2 high parts, bf16x2 remainders)
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -298,20 +315,30 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                     mma_bf16(acc_p[2 * np + 1], fq, fb[2], fb[3]);
                 }
             }
+            float wa_row[2], wp_row[2], g_row[2];  // this thread's two rows
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = m0 + gq + 8 * hh;
+                wa_row[hh] = s.beta[row] * s.rk[row];
+                wp_row[hh] = p.scale * s.rq[row];
+                g_row[hh] = s.gl2[row];
+            }
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 if (nt > 2 * warp + 1) break;
+                const int col = 8 * nt + 2 * cq;
+                const float2 gc = *reinterpret_cast<const float2 *>(s.gl2 + col);
+                const float2 kc = *reinterpret_cast<const float2 *>(s.rk + col);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int row = m0 + gq + 8 * hh, col = 8 * nt + 2 * cq;
+                    const int row = m0 + gq + 8 * hh;
                     float pa[2], pp[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int c = col + e;
-                        const float decay = exp2f(fminf(s.gl2[row] - s.gl2[c], 0.f));
-                        const float base = s.rk[c] * decay;
-                        pa[e] = c < row ? s.beta[row] * s.rk[row] * base * acc_a[nt][2 * hh + e] : 0.f;
-                        pp[e] = c <= row ? p.scale * s.rq[row] * base * acc_p[nt][2 * hh + e] : 0.f;
+                        const float base = (e ? kc.y : kc.x) * exp2f(fminf(g_row[hh] - (e ? gc.y : gc.x), 0.f));
+                        pa[e] = c < row ? wa_row[hh] * base * acc_a[nt][2 * hh + e] : 0.f;
+                        pp[e] = c <= row ? wp_row[hh] * base * acc_p[nt][2 * hh + e] : 0.f;
                     }
                     *reinterpret_cast<float2 *>(s.a + row * kLdA + col) = make_float2(pa[0], pa[1]);
                     uint32_t hi, lo;
@@ -401,16 +428,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
                 for (int e = 0; e < 4; ++e) {
                     const int sr = 16 * bk + 4 * e + qr;
                     const float *arow = s.a + sr * kLdA;
-                    float acc0 = ucol[sr], acc1 = 0.f;
+                    // A r-pairs times U r-pairs, two terms per packed instruction
+                    uint64_t acc0 = pair(ucol[sr], 0.f), acc1 = pair(0.f, 0.f);
 #pragma unroll
                     for (int r = 0; r < 16 * bk; r += 4) {
                         const float4 a4 = *reinterpret_cast<const float4 *>(arow + r);
-                        acc0 = fmaf(-a4.x, ucol[r], acc0);
-                        acc1 = fmaf(-a4.y, ucol[r + 1], acc1);
-                        acc0 = fmaf(-a4.z, ucol[r + 2], acc0);
-                        acc1 = fmaf(-a4.w, ucol[r + 3], acc1);
+                        const float2 u01 = *reinterpret_cast<const float2 *>(ucol + r);
+                        const float2 u23 = *reinterpret_cast<const float2 *>(ucol + r + 2);
+                        acc0 = fma2(pair(-a4.x, -a4.y), pair(u01.x, u01.y), acc0);
+                        acc1 = fma2(pair(-a4.z, -a4.w), pair(u23.x, u23.y), acc1);
                     }
-                    rr[e] = acc0 + acc1;
+                    rr[e] = pair_sum(acc0) + pair_sum(acc1);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ucol[16 * bk + 4 * e + qr] = rr[e];
@@ -419,16 +447,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_chunk_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float *trow = s.tb + (16 * bk + 4 * e + qr) * kLdT;
-                    float acc = 0.f;
+                    uint64_t acc0 = pair(0.f, 0.f), acc1 = pair(0.f, 0.f);
 #pragma unroll
                     for (int c = 0; c < 16; c += 4) {
                         const float4 t4 = *reinterpret_cast<const float4 *>(trow + c);
-                        acc = fmaf(t4.x, ucol[16 * bk + c], acc);
-                        acc = fmaf(t4.y, ucol[16 * bk + c + 1], acc);
-                        acc = fmaf(t4.z, ucol[16 * bk + c + 2], acc);
-                        acc = fmaf(t4.w, ucol[16 * bk + c + 3], acc);
+                        const float2 u01 = *reinterpret_cast<const float2 *>(ucol + 16 * bk + c);
+                        const float2 u23 = *reinterpret_cast<const float2 *>(ucol + 16 * bk + c + 2);
+                        acc0 = fma2(pair(t4.x, t4.y), pair(u01.x, u01.y), acc0);
+                        acc1 = fma2(pair(t4.z, t4.w), pair(u23.x, u23.y), acc1);
                     }
-                    uu[e] = acc;
+                    uu[e] = pair_sum(acc0) + pair_sum(acc1);
                 }
                 __syncwarp();
 #pragma unroll
