@@ -312,7 +312,8 @@ int ssd_varlen_conv1d(const ssd_conv_dims *dims, const int32_t *cu_seqlens, cons
  *
  * Supported: bf16 q, k, v, o; K = 128; V a multiple of 32 up to 256;
  * chunk_size = 64; block_size a multiple of 64 (or 0 without a block table).
- * g and beta fp32, g <= 0 expected (a decay).  Write slots must not alias read
+ * g and beta fp32, g <= 0 expected (a decay).  With T = 0 (every request empty)
+ * the token buffers may be NULL.  Write slots must not alias read
  * slots of the same call.  Host-visible violations return SSD_ERR_* before any
  * launch; device_err (one int32, required) receives SSD_DEVERR_* bits
  * (CU_SEQLENS, NUM_COMPUTED, INIT_SLOT, FINAL_SLOT, BLOCK_SLOT, BLOCK_TABLE),

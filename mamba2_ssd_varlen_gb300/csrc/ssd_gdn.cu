@@ -611,7 +611,8 @@ extern "C" int ssd_varlen_gdn_forward(const ssd_gdn_dims *d, const int32_t *cu_s
     if (d->chunk_size != kL) return SSD_ERR_UNSUPPORTED;
     if (io->block_table && (d->block_size <= 0 || d->block_size % kL != 0 || d->block_table_width < 1))
         return SSD_ERR_BLOCK_SIZE;
-    if (!io->q || !io->k || !io->v || !io->g || !io->beta || !io->o || !io->device_err) return SSD_ERR_NULL;
+    if (!io->device_err) return SSD_ERR_NULL;
+    if (d->T > 0 && (!io->q || !io->k || !io->v || !io->g || !io->beta || !io->o)) return SSD_ERR_NULL;
     if ((io->init_slots || io->final_slots || io->block_table) && (!io->state_pool || d->num_slots < 1))
         return SSD_ERR_NULL;
     const void *vec[] = {io->q, io->k, io->v, io->o, io->state_pool, io->final_states, io->chunk_states};

@@ -158,3 +158,12 @@ def test_full_uniform_8x2048_sampled():
     toks = torch.tensor(o["tokens"], device="cuda")
     assert_close(host(call.o.index_select(0, toks).index_select(1, hidx)), ref["o"], "o")
     assert_close(host(call.final_states[reqs].index_select(1, hidx)), ref["final_states"], "final_states")
+
+
+def test_all_requests_empty():
+    # T = 0: no chunk runs; every request's final state is its initial state
+    # (zeros where the read slot is -1), in the dense output and the final slots.
+    spec = _spec(lengths=[0, 0, 0], export_chunks=False, block_size=0)
+    prob = workloads.make_gdn_problem(spec, seed=21, device="cuda", canary=0.75)
+    prob["init_slots"][1] = -1
+    run_full(prob)
