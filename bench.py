@@ -47,6 +47,22 @@ def env_rank():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(value, dist, device="cuda"):
+    """The largest of every rank's value (the slowest rank's time), or the value
+    itself on one rank."""
+    if not dist:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, world, ms):
+    """Whole-job units per second when every rank processes units_per_rank in ms."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -404,10 +420,7 @@ def run_decode_bench(args, rank, local_rank, world, dist):
         dist.barrier()
     clocks = sampler.stop()
     total_ms = t0.elapsed_time(t1)
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     assert call.status() == 0, "device error during the timed region"
     k_ms = sorted(a.elapsed_time(b) for a, b in ev)
     k_avg = sum(k_ms) / K
@@ -437,6 +450,7 @@ def run_decode_bench(args, rank, local_rank, world, dist):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / args.e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     achieved = cost["bytes"] / (k_avg / 1e3) / 1e9
     line = {"metric": DECODE_METRIC, "value": T * world / (ms_per_step / 1e3), "unit": "tokens/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -502,6 +516,7 @@ def run_conv_bench(args, rank, local_rank, world, dist):
     assert call.status() == 0, "device error during the timed region"
     k_ms = [a.elapsed_time(b) for a, b in ev]
     k_avg = sum(k_ms) / K
+    k_avg = max_over_ranks(k_avg, dist)
     T = prob["T"]
     host_x = prob["x"].cpu().pin_memory()
     y_host = torch.empty(call.y.shape, dtype=call.y.dtype, pin_memory=True)
@@ -521,6 +536,7 @@ def run_conv_bench(args, rank, local_rank, world, dist):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / args.e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     achieved = cost["bytes"] / (k_avg / 1e3) / 1e9
     line = {"metric": CONV_METRIC, "value": T * world / (k_avg / 1e3), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": k_avg, "higher_is_better": True,
@@ -600,6 +616,7 @@ def run_gdn_bench(args, rank, local_rank, world, dist):
     clocks = sampler.stop()
     assert call.status() == 0, "device error during the timed region"
     k_avg = sum(a.elapsed_time(b) for a, b in ev) / K
+    k_avg = max_over_ranks(k_avg, dist)
     T = prob["T"]
     hosts = {key: prob[key].cpu().pin_memory() for key in ("q", "k", "v", "g", "beta")}
     o_host = torch.empty(call.o.shape, dtype=call.o.dtype, pin_memory=True)
@@ -620,6 +637,7 @@ def run_gdn_bench(args, rank, local_rank, world, dist):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / args.e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     achieved = cost["bytes"] / (k_avg / 1e3) / 1e9
     line = {"metric": GDN_METRIC, "value": T * world / (k_avg / 1e3), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": k_avg, "higher_is_better": True,
@@ -721,10 +739,7 @@ def main():
     fwd_ms = sorted(e1.elapsed_time(e2) for _, e1, e2 in ev)
     plan_ms = sorted(e0.elapsed_time(e1) for e0, e1, _ in ev)
     fwd_avg = sum(fwd_ms) / K
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     assert call.status() == 0, "device error during the timed region"
     ms_per_step = total_ms / K
     T = prob["T"]
@@ -764,10 +779,7 @@ def main():
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / KE
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
 
     khash = kernel_source_hash()
     achieved = cost["bytes"] / (fwd_avg / 1e3) / 1e9
