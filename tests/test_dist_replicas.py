@@ -35,7 +35,7 @@ def _rank_main(rank, world, port, times, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world, port = 2, _free_port()
     times = [0.40, 0.55]
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, times, out), nprocs=world, join=True)
         res = dict(out)
