@@ -245,3 +245,14 @@ def test_gdn_block_table_needs_a_chunk_multiple_block_size(lib):
     for bs in (0, 96):
         d = _gdn_dims(block_size=bs, block_table_width=4)
         assert lib.ssd_varlen_gdn_forward(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == -5
+
+
+def test_gdn_empty_batch_accepts_null_token_buffers(lib):
+    # T = 0: q, k, v, g, beta and o may be NULL; validation passes and the call
+    # goes on to the launch (which reports SSD_ERR_CUDA on a host without a GPU).
+    d = _gdn_dims(T=0)
+    io = _gdn_io(q=None, k=None, v=None, g=None, beta=None, o=None)
+    rc = lib.ssd_varlen_gdn_forward(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None)
+    assert rc not in (-1, -2, -7)
+    io = _gdn_io(device_err=None)
+    assert lib.ssd_varlen_gdn_forward(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == -1
