@@ -85,6 +85,7 @@ enum ssd_status {
 #define SSD_DEVERR_BLOCK_TABLE 0x20  /* a boundary needs a column >= block_table_width */
 #define SSD_DEVERR_TIMEOUT 0x40      /* a bounded wait inside a kernel gave up (work skipped) */
 #define SSD_DEVERR_INTERNAL 0x80     /* a kernel could not start (shared-memory alignment) */
+#define SSD_DEVERR_ALIAS 0x100       /* ssd_varlen_check_slots: a written slot is read or written twice */
 
 /* Problem sizes.  Filled by the caller, copied into the plan. */
 typedef struct ssd_dims {
@@ -350,6 +351,24 @@ typedef struct ssd_gdn_io {
 
 int ssd_varlen_gdn_forward(const ssd_gdn_dims *dims, const int32_t *cu_seqlens, const ssd_gdn_io *io,
                            cudaStream_t stream);
+
+/* ---- Slot aliasing check (for debug runs) ------------------------------------
+ * The calls above require that no pool slot written in a call is also read in
+ * it, and that no slot is written twice (the caller's responsibility: checking
+ * it on every call would cost a pass over the slot tables).  This entry point
+ * checks it on the device, for debug runs: with R = dims->R requests,
+ *   read slots  = init_slots[i] >= 0
+ *   write slots = final_slots[i] >= 0 and block_table[i][j] >= 0
+ *                 (j < dims->block_table_width)
+ * it ORs SSD_DEVERR_ALIAS into *device_err when a write slot equals a read slot
+ * or another write slot (the decode step's anchors: pass read_slots as
+ * init_slots and its per-token write_slots as final_slots with R = T).  Any of
+ * the three tables may be NULL.  O((R + R W)^2) comparisons on the device: meant
+ * for tests and debug builds, not for every step.  One launch on `stream`;
+ * allocates nothing.  Returns SSD_ERR_NULL without device_err, SSD_ERR_DIMS for
+ * R < 1 or a negative width. */
+int ssd_varlen_check_slots(const ssd_dims *dims, const int32_t *init_slots, const int32_t *final_slots,
+                           const int32_t *block_table, int32_t *device_err, cudaStream_t stream);
 
 /* ---- Block-aligned prefill bites (host only) --------------------------------
  * "Automatic prefix caching for GDN hybrid models (mamba_cache_mode=all) with

@@ -17,6 +17,7 @@ The functions keep the C names:
   ssd_varlen_conv1d(dims, cu_seqlens, io)        (varlen causal conv1d with conv-state anchors)
   ssd_varlen_align_bite(start, end, total, align) (block-aligned prefill bite, host)
   ssd_varlen_gdn_forward(dims, cu_seqlens, io)   (gated delta rule prefill by chunks)
+  ssd_varlen_check_slots(dims, init, final, block_table, err)  (slot-aliasing check, debug)
 and ``run(...)`` wires a whole call from torch tensors (tests and bench use it).
 """
 from __future__ import annotations
@@ -32,7 +33,7 @@ DTYPE_F32 = 1
 
 DEVERR = {
     "CU_SEQLENS": 0x1, "NUM_COMPUTED": 0x2, "INIT_SLOT": 0x4, "FINAL_SLOT": 0x8,
-    "BLOCK_SLOT": 0x10, "BLOCK_TABLE": 0x20, "TIMEOUT": 0x40, "INTERNAL": 0x80,
+    "BLOCK_SLOT": 0x10, "BLOCK_TABLE": 0x20, "TIMEOUT": 0x40, "INTERNAL": 0x80, "ALIAS": 0x100,
 }
 STATUS = {
     0: "OK", -1: "NULL", -2: "DIMS", -3: "CHUNK_SIZE", -4: "GROUPS", -5: "BLOCK_SIZE",
@@ -41,7 +42,7 @@ STATUS = {
 EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
             "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror",
             "ssd_varlen_forward_static", "ssd_varlen_decode", "ssd_varlen_conv1d",
-            "ssd_varlen_align_bite", "ssd_varlen_gdn_forward"]
+            "ssd_varlen_align_bite", "ssd_varlen_gdn_forward", "ssd_varlen_check_slots"]
 # Size of the library-owned scratch array used by ssd_varlen_forward_static.
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -144,6 +145,8 @@ def load_library():
     lib.ssd_varlen_align_bite.restype = c_i64
     lib.ssd_varlen_gdn_forward.argtypes = [ctypes.POINTER(ssd_gdn_dims), c_vp, ctypes.POINTER(ssd_gdn_io), c_vp]
     lib.ssd_varlen_gdn_forward.restype = ctypes.c_int
+    lib.ssd_varlen_check_slots.argtypes = [ctypes.POINTER(ssd_dims), c_vp, c_vp, c_vp, c_vp, c_vp]
+    lib.ssd_varlen_check_slots.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -438,3 +441,19 @@ class GdnCall:
 def run_gdn(prob: dict, **kw) -> GdnCall:
     """One GDN prefill on the current stream; returns the GdnCall (outputs on it)."""
     return GdnCall(prob, **kw)()
+
+
+def ssd_varlen_check_slots(R, init_slots=None, final_slots=None, block_table=None, stream=None) -> int:
+    """Device check that no written slot is read or written twice; returns the
+    device error bits (SSD_DEVERR_ALIAS when it finds one).  Synchronises."""
+    import torch
+    dev = next(t.device for t in (init_slots, final_slots, block_table) if t is not None)
+    err = torch.zeros(4, dtype=torch.int32, device=dev)
+    width = 0 if block_table is None else int(block_table.shape[1])
+    dims = make_dims(0, R, 1, 1, 1, 1, 16, DTYPE_BF16, block_table_width=width)
+    rc = load_library().ssd_varlen_check_slots(ctypes.byref(dims), _ptr(init_slots), _ptr(final_slots),
+                                               _ptr(block_table), _ptr(err), _stream(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_check_slots")
+    torch.cuda.synchronize(dev)
+    return int(err[0].item())

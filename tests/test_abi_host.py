@@ -256,3 +256,12 @@ def test_gdn_empty_batch_accepts_null_token_buffers(lib):
     assert rc not in (-1, -2, -7)
     io = _gdn_io(device_err=None)
     assert lib.ssd_varlen_gdn_forward(ctypes.byref(d), ctypes.c_void_p(_FAKE), ctypes.byref(io), None) == -1
+
+
+def test_check_slots_host_validation(lib):
+    d = m.make_dims(8, 2, 4, 64, 128, 1, 64, m.DTYPE_BF16, num_slots=4)
+    f = ctypes.c_void_p(_FAKE)
+    assert lib.ssd_varlen_check_slots(ctypes.byref(d), f, f, None, None, None) == -1
+    assert lib.ssd_varlen_check_slots(None, f, f, None, f, None) == -1
+    bad = m.make_dims(8, 0, 4, 64, 128, 1, 64, m.DTYPE_BF16, num_slots=4)
+    assert lib.ssd_varlen_check_slots(ctypes.byref(bad), f, f, None, f, None) == -2
