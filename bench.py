@@ -236,9 +236,16 @@ def cpu_baseline(prob, max_seconds=30.0):
     t0 = time.perf_counter()
     oracle.forward(o, n_threads=ncores)
     dt = time.perf_counter() - t0
+    # the same recurrence on one core, over the first request only
+    o1 = workloads.to_oracle(prob, requests=sel[:1])
+    t1 = time.perf_counter()
+    oracle.forward(o1, n_threads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": tok / dt, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
             "sample": f"{len(sel)} of {len(lens)} requests ({tok} tokens, all {prob['H']} heads), "
-                      f"fp64 token-by-token recurrence, {dt:.2f} s"}
+                      f"fp64 token-by-token recurrence, {dt:.2f} s",
+            "value_one_core": lens[sel[0]] / dt1,
+            "sample_one_core": f"request {sel[0]} ({lens[sel[0]]} tokens, all heads) on one core, {dt1:.2f} s"}
 
 
 def run_reference_decode(args, world):
