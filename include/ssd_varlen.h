@@ -118,6 +118,9 @@ typedef struct ssd_plan {
     cudaStream_t stream;       /* the stream the plan was built on */
 } ssd_plan;
 
+/* Inputs and outputs of a forward.  With T = 0 (every request empty) the token
+ * buffers (x, dt, B, C, z, y) may be NULL; the forward then writes each
+ * request's final state (its initial state, or zeros) where asked. */
 typedef struct ssd_inputs {
     const void *x;             /* (T,H,P) */
     const void *dt;            /* (T,H) */
@@ -228,8 +231,9 @@ int ssd_varlen_forward_static(const ssd_dims *dims, const int32_t *cu_seqlens, c
  * is (T) int32 and nullable (no state written), z and D are nullable.
  * device_err (one int32 in device memory, required) receives SSD_DEVERR_* bits
  * (CU_SEQLENS, INIT_SLOT for a read slot >= num_slots, FINAL_SLOT for a write
- * slot >= num_slots); the caller clears it.  Launches one kernel on `stream`;
- * allocates nothing. */
+ * slot >= num_slots); the caller clears it.  With T = 0 the token buffers (x,
+ * dt, B, C, z, y) may be NULL.  Launches one kernel on `stream`; allocates
+ * nothing. */
 typedef struct ssd_decode_io {
     const void *x, *dt;         /* (T,H,P), (T,H) in dims.dtype */
     const float *dt_bias, *A;   /* (H) */
@@ -264,8 +268,8 @@ int ssd_varlen_decode(const ssd_dims *dims, const int32_t *cu_seqlens, const ssd
  * holds raw inputs, exact in that dtype); weight (D,W), bias (D) fp32.  W in
  * [2, 4]; D a multiple of 8.  Read and write slots of one call are disjoint.
  * device_err (one int32 in device memory, required) receives SSD_DEVERR_*
- * bits (CU_SEQLENS, INIT_SLOT, FINAL_SLOT).  One launch on `stream`; allocates
- * nothing. */
+ * bits (CU_SEQLENS, INIT_SLOT, FINAL_SLOT).  With T = 0, x and y may be NULL.
+ * One launch on `stream`; allocates nothing. */
 typedef struct ssd_conv_dims {
     int64_t T;          /* total tokens, >= 0 */
     int32_t R;          /* requests, >= 1 */

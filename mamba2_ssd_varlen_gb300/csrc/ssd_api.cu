@@ -124,7 +124,9 @@ int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_out
     const ssd_dims *d = &plan->dims;
     int rc = check_dims(d);
     if (rc != SSD_OK) return rc;
-    if (!in->x || !in->dt || !in->dt_bias || !in->A || !in->B || !in->C || !out->y) return SSD_ERR_NULL;
+    if (!in->dt_bias || !in->A) return SSD_ERR_NULL;
+    // with no tokens (every request empty) the token buffers may be NULL
+    if (d->T > 0 && (!in->x || !in->dt || !in->B || !in->C || !out->y)) return SSD_ERR_NULL;
     const void *big[] = {in->x, in->dt, in->B, in->C, in->z, out->y, in->state_pool,
                          out->final_states, out->chunk_states};
     for (const void *ptr : big)
@@ -175,8 +177,10 @@ int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_out
     p.chunk_states = out->chunk_states;
     p.block_table = out->block_table;
     if (d->T == 0 && !out->final_states && !out->final_slots) return SSD_OK;
-    cudaError_t e = chunk_tc_supported(p, d->dtype) ? launch_chunk_tc(p, plan->max_segs, stream)
-                                                    : launch_recurrent(p, d->dtype, stream);
+    // an empty batch (final = initial state for every request) takes the general
+    // path, which needs no tensor maps over the absent token buffers
+    cudaError_t e = (d->T > 0 && chunk_tc_supported(p, d->dtype)) ? launch_chunk_tc(p, plan->max_segs, stream)
+                                                                  : launch_recurrent(p, d->dtype, stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -323,7 +323,8 @@ extern "C" int ssd_varlen_conv1d(const ssd_conv_dims *d, const int32_t *cu_seqle
     if (d->T < 0 || d->T > 0x7fffffffLL || d->R < 1 || d->D < 1 || d->num_slots < 0) return SSD_ERR_DIMS;
     if (d->dtype != SSD_DTYPE_BF16 && d->dtype != SSD_DTYPE_F32) return SSD_ERR_DTYPE;
     if (d->W < 2 || d->W > 4 || d->D % 8 != 0) return SSD_ERR_UNSUPPORTED;
-    if (!io->x || !io->weight || !io->y || !io->device_err) return SSD_ERR_NULL;
+    if (!io->weight || !io->device_err) return SSD_ERR_NULL;
+    if (d->T > 0 && (!io->x || !io->y)) return SSD_ERR_NULL;  // optional with no tokens
     const bool uses_pool = io->read_slots || io->write_slots;
     if (uses_pool && (!io->conv_pool || d->num_slots < 1)) return SSD_ERR_NULL;
     const void *vec[] = {io->x, io->y, io->conv_pool};

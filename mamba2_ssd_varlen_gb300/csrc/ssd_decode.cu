@@ -210,9 +210,9 @@ extern "C" int ssd_varlen_decode(const ssd_dims *d, const int32_t *cu_seqlens, c
     if ((d->N & (d->N - 1)) != 0 || d->N < 16 || d->N > 256) return SSD_ERR_UNSUPPORTED;
     const int kv = pick_kv(d->P, d->N);
     if (kv == 0) return SSD_ERR_UNSUPPORTED;
-    if (!io->x || !io->dt || !io->dt_bias || !io->A || !io->B || !io->C || !io->state_pool || !io->read_slots ||
-        !io->y || !io->device_err)
-        return SSD_ERR_NULL;
+    if (!io->dt_bias || !io->A || !io->state_pool || !io->read_slots || !io->device_err) return SSD_ERR_NULL;
+    // with no tokens (every window empty) the token buffers may be NULL
+    if (d->T > 0 && (!io->x || !io->dt || !io->B || !io->C || !io->y)) return SSD_ERR_NULL;
     const void *big[] = {io->x, io->dt, io->B, io->C, io->z, io->y, io->state_pool};
     for (const void *ptr : big)
         if (ptr && !aligned16(ptr)) return SSD_ERR_ALIGN;

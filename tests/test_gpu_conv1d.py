@@ -135,3 +135,8 @@ def test_full_size_sampled_channels():
     assert_close(call.y.index_select(1, idx).float().cpu().numpy(), ref["y"], "y")
     for s, v in ref["writes"].items():
         np.testing.assert_array_equal(prob["conv_pool"][s].index_select(0, idx).double().cpu().numpy(), v)
+
+
+def test_all_requests_empty():
+    # T = 0: every request passes its conv state (or zeros) to its write slot.
+    run_and_check(workloads.make_conv_problem(_spec(lengths=[0, 0, 0]), seed=14, device="cuda", canary=0.25))

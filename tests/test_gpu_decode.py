@@ -144,3 +144,9 @@ def test_full_size_spec_decode_sampled():
     assert_close(call.y.index_select(0, toks).index_select(1, hidx).float().cpu().numpy(), ref["y"], "y")
     for s, v in ref["writes"].items():
         assert_close(prob["state_pool"][s].index_select(0, hidx).cpu().numpy(), v, f"state_pool[{s}]")
+
+
+def test_all_windows_empty():
+    # T = 0: nothing is read or written; y is empty and the pool keeps its values.
+    spec = _spec(windows=[0, 0, 0])
+    run_and_check(workloads.make_decode_problem(spec, seed=19, device="cuda", canary=0.5))

@@ -290,3 +290,13 @@ def test_full_block_checkpointed_varlen():
     order = np.argsort(lens)
     reqs = sorted({int(order[-1]), int(order[0]), 17, 64})
     _sampled_check(prob, reqs, [0, 35, 63])
+
+
+def test_all_requests_empty():
+    # T = 0: no token buffers; every request's final state (dense and in its final
+    # slot) is its initial state, zeros where it has no initial slot.
+    spec = workloads.Spec("empty", H=4, P=64, N=128, G=2, chunk_size=64, dtype="bf16", has_D=True, has_z=True,
+                          init="all", pool_slots=16, final_slots=True)
+    prob = workloads.make_problem(spec, seed=23, device="cuda", lengths=[0, 0, 0], canary=-4.0)
+    prob["init_slots"][1] = -1
+    run_full(prob)
