@@ -73,7 +73,7 @@ enum ssd_status {
     SSD_ERR_WORKSPACE = -8,     /* workspace too small or misaligned */
     SSD_ERR_PLAN = -9,          /* plan not built, or built for other dims */
     SSD_ERR_CUDA = -10,         /* a CUDA runtime call failed */
-    SSD_ERR_UNSUPPORTED = -11   /* a combination this build does not handle */
+    SSD_ERR_UNSUPPORTED = -11   /* a combination this library does not handle */
 };
 
 /* Bits of the device error word (ssd_varlen_status). */

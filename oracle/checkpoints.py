@@ -17,7 +17,7 @@ Definitions (readings of the pages where they are silent):
   absolute chunks every block boundary is a chunk end, so nothing is skipped.)
 * The exported state of a chunk is the state AFTER the chunk's last token
   (the FLA-style ``h`` export named on the prefix-caching page, Kernels/layers;
-  its exact semantics are pinned there by tests this build does not have).
+  its exact semantics are pinned there by tests the page only names).
   Chunk j of request i is row first_chunk[i] + j of the export buffer;
   first_chunk is the exclusive prefix sum of the per-request chunk counts.
 * Block checkpoints: for every absolute block boundary kb (a multiple of
