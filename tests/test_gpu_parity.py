@@ -300,3 +300,14 @@ def test_all_requests_empty():
     prob = workloads.make_problem(spec, seed=23, device="cuda", lengths=[0, 0, 0], canary=-4.0)
     prob["init_slots"][1] = -1
     run_full(prob)
+
+
+@pytest.mark.parametrize("P,N", [(64, 64), (32, 128), (96, 256), (8, 16)])
+def test_bf16_shapes_on_the_general_path(P, N):
+    # bf16 shapes the tensor-core kernel does not take (P not 64/128 or N != 128)
+    # run on the token-serial path: every output against the oracle.
+    spec = workloads.Spec("gen", H=3, P=P, N=N, G=3, chunk_size=32, dtype="bf16", has_D=True, has_z=True,
+                          init="all", pool_slots=40, final_slots=True, export_chunks=True, block_size=64)
+    prob = workloads.make_problem(spec, seed=P + N, device="cuda", lengths=[90, 0, 200, 1],
+                                  num_computed=[3, 0, 64, 10], canary=0.5)
+    run_full(prob)
