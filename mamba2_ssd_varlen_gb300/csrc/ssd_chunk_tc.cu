@@ -1178,17 +1178,19 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t
         !make_map(&maps.c, p.C, 128, p.G, p.T) || !make_map(&maps.z, p.z ? p.z : p.x, P, p.H, p.T))
         return cudaErrorInvalidValue;
     const int smem = (int)sizeof(TcSmem<P>);
-    static bool attr_done = false;
-    if (!attr_done) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    // the shared-memory attribute is per device: set once on each device this process uses
+    static bool attr_done[64] = {};
+    const bool known = dev >= 0 && dev < 64;
+    if (!known || !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        if (known) attr_done[dev] = true;
     }
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_items));
     ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
