@@ -851,7 +851,7 @@ def main():
     achieved = cost["bytes"] / (fwd_avg / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": read_traffic(khash), "peak_source": peaks["source"],
+                "traffic": read_traffic(khash, args.config), "peak_source": peaks["source"],
                 "algorithmic_bytes": cost["bytes"], "algorithmic_flops": cost["flops"],
                 "kernel": "ssd_varlen_forward", "kernel_ms_avg": round(fwd_avg, 5),
                 "tensor_frac_of_peak": round(cost["flops"] / (fwd_avg / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}

@@ -557,6 +557,14 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             constexpr uint32_t i_y = idesc_bf16_f32(128, P, false, true);      // K-major A x MN-major B
             constexpr uint32_t i_s = idesc_bf16_f32(128, P, true, true);       // B^T (MN-major) x wx (MN-major)
             const uint32_t colS = Cfg::kSepS ? Cfg::kColS : Cfg::kColH;
+            // Descriptors are built once: the start-address field is (address >> 4) in
+            // the low 14 bits and shared memory ends below 256 KB, so the descriptor
+            // of (tile + offset) is the tile's descriptor + offset / 16.
+            const uint64_t dC = sdesc_sw128(sc, 16, 1024), dBk = sdesc_sw128(sb, 16, 1024);
+            const uint64_t dBm = sdesc_sw128(sb, 16384, 1024);
+            const uint64_t dHh = sdesc_sw128(shh, 16384, 1024), dHl = sdesc_sw128(shl, 16384, 1024);
+            const uint64_t dXh = sdesc_sw128(sxh, 16384, 1024), dXl = sdesc_sw128(sxl, 16384, 1024);
+            const uint64_t dX0 = sdesc_sw128(smem_u32(s.x), 16384, 1024);
             uint32_t pc = 0, nit = 0;
             bool ok = true;
             while (ok) {
@@ -579,7 +587,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tbase, sdesc_sw128(sc + ko, 16, 1024), sdesc_sw128(sb + ko, 16, 1024), i_cb, kk > 0);
+                            mma_ss(tbase, dC + (ko >> 4), dBk + (ko >> 4), i_cb, kk > 0);
                         }
                         mma_commit(&s.cb_full);
                         // y_inter = C h^T (h in hi + lo) into accumulator pair yb,
@@ -592,12 +600,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         tc_fence_after();
 #pragma unroll
                         for (int part = 0; part < 2; ++part) {
-                            const uint32_t hb = part ? shl : shh;
+                            const uint64_t dH = part ? dHl : dHh;
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                mma_ss(tbase + Cfg::col_ye(yb), sdesc_sw128(sc + ko, 16, 1024),
-                                       sdesc_sw128(hb + kk * 2048, 16384, 1024), i_y, (part | kk) != 0);
+                                mma_ss(tbase + Cfg::col_ye(yb), dC + (ko >> 4), dH + kk * 128, i_y, (part | kk) != 0);
                             }
                         }
                         mma_commit(&s.empty_c);  // C has no further reader in this piece
@@ -608,11 +615,10 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     tc_fence_after();
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t xb = part ? sxl : sxh;
+                        const uint64_t dXd = part ? dXl : dXh;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_ss(tbase + colS, sdesc_sw128(sb + kk * 2048, 16384, 1024),
-                                   sdesc_sw128(xb + kk * 2048, 16384, 1024), i_s,
+                            mma_ss(tbase + colS, dBm + kk * 128, dXd + kk * 128, i_s,
                                    Cfg::kSepS ? (uint32_t)((part | kk) != 0) : 1u);
                     }
                     mma_commit(&s.s_full);
@@ -626,14 +632,13 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         if (!wait_bar(&s.m_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
                         if (!wait_bar(&s.full_x[st], par(pc / kNS), abort_flag, p.hdr)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t sx = smem_u32(s.x + st * Cfg::kXBytes);
+                        const uint64_t dX = dX0 + (uint32_t)(st * Cfg::kXBytes >> 4);
 #pragma unroll
                         for (int part = 0; part < 2; ++part) {
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t acol = kk * 16 + part * 8;
-                                mma_ts(tbase + Cfg::col_yi(yb), tbase + acol, sdesc_sw128(sx + kk * 2048, 16384, 1024),
-                                       i_y, (part | kk) != 0);
+                                mma_ts(tbase + Cfg::col_yi(yb), tbase + acol, dX + kk * 128, i_y, (part | kk) != 0);
                             }
                         }
                         mma_commit(&s.empty_x[st]);
