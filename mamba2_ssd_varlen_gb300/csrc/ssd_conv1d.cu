@@ -9,11 +9,11 @@
 //   y[t, c]  = act(bias[c] + sum_k weight[c, k] xin[t - (W-1) + k, c])
 //   new conv state = the last W-1 values of xin
 //
-// Streaming and HBM-bound: a warp takes a tile of kTile tokens and 32 x kN
+// Streaming and HBM-bound: a warp takes a strip of consecutive tokens over 32 x kN
 // channels; each thread owns one 16-byte vector of kN channels and slides a
-// W-deep register window down the tile, so every input and output row is one
+// W-deep register window down the strip, so every input and output row is one
 // coalesced vector access and every input is read once (plus a W-1 halo per
-// tile).  Request boundaries inside a tile restart the window from the next
+// strip).  Request boundaries inside a strip restart the window from the next
 // request's conv state.
 #include "ssd_internal.cuh"
 
@@ -21,7 +21,8 @@ namespace ssd {
 namespace {
 
 constexpr int kConvThreads = 128;
-constexpr int kTile = 64;  // tokens per CTA
+constexpr int kMinStrip = 64;  // tokens per warp at least, when the grid need not fill the GPU
+constexpr int kMaxDevices = 64;
 
 struct ConvParams {
     int64_t T;
@@ -149,12 +150,15 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 constexpr int kStages = 16;  // input rows in flight per thread
 constexpr int kUnroll = 6;   // a multiple of W-1 for every W, so the window shifts by renaming
 
-// One warp owns a work item: 32 consecutive 16-byte channel vectors (lane l the
-// vector g*32+l) over a tile of kTile tokens.  Items are numbered channel group
-// fastest, so the warps of a CTA read neighbouring parts of the same rows.
-// Each thread streams its inputs through a private kStages-deep ring in shared
-// memory filled by asynchronous copies, so the loads in flight cost no
-// registers; only the W-1 previous inputs stay in registers.
+// Work units are (channel group g, token t), g major; channel group g is the 32
+// consecutive 16-byte channel vectors g*32 .. g*32+31 (lane l the vector g*32+l).
+// The grid is what stays resident on the GPU at once, and its warps split the
+// units evenly in order: every warp streams one strip (two where its strip
+// crosses into the next channel group), so there is no tail wave and each warp
+// fills its input ring once per strip.  Each thread streams its inputs through a
+// private kStages-deep ring in shared memory filled by asynchronous copies, so
+// the loads in flight cost no registers; only the W-1 previous inputs stay in
+// registers.
 template <typename T, int W, bool kSilu>
 __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const __grid_constant__ ConvParams p) {
     constexpr int kN = Vec<T>::kN;
@@ -162,15 +166,16 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const __grid_const
     const ssd_conv_io &io = p.io;
     const int nvec = p.D / kN;
     const int groups = (nvec + 31) / 32;
-    const int64_t item = (int64_t)blockIdx.x * (kConvThreads / 32) + (threadIdx.x >> 5);
-    const int g = (int)(item % groups);
-    const int64_t tile = item / groups;
-    const int c0 = (g * 32 + (threadIdx.x & 31)) * kN;  // first channel of this thread
-    const int64_t t0 = tile * kTile;
+    const int64_t t_units = p.T > 0 ? p.T : 1;  // one unit per group when T = 0 (empty requests)
+    const int64_t units = (int64_t)groups * t_units;
+    const int64_t nwarps = (int64_t)gridDim.x * (kConvThreads / 32);
+    const int64_t wid = (int64_t)blockIdx.x * (kConvThreads / 32) + (threadIdx.x >> 5);
     const T *__restrict__ xv = static_cast<const T *>(io.x);
     T *__restrict__ yv = static_cast<T *>(io.y);
     T *pool = static_cast<T *>(io.conv_pool);
     const size_t slot_elems = (size_t)p.D * (W - 1);
+    const size_t row = (size_t)p.D;
+    uint4 *mine = &ring[0][threadIdx.x];  // stage s at mine[s * kConvThreads]
 
     // cu_seqlens must start at 0, not decrease and end at T (checked once).
     if (blockIdx.x == 0) {
@@ -178,136 +183,172 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const __grid_const
             if (p.cu[i + 1] < p.cu[i] || (i == 0 && p.cu[0] != 0) || (i == p.R - 1 && p.cu[p.R] != p.T))
                 atomicOr(io.device_err, SSD_DEVERR_CU_SEQLENS);
     }
-    if (c0 >= p.D) return;
 
-    auto state_slot = [&](const int32_t *slots, int i, int bit) -> T * {
-        if (!slots || !pool) return nullptr;
-        const int s = slots[i];
-        if (s >= p.num_slots) {
-            if (c0 == 0) atomicOr(io.device_err, bit);
-            return nullptr;
-        }
-        return s >= 0 ? pool + (size_t)s * slot_elems : nullptr;
-    };
+    int64_t u = wid * units / nwarps;
+    const int64_t u_end = (wid + 1) * units / nwarps;
+    while (u < u_end) {
+        const int g = (int)(u / t_units);
+        const int64_t t0 = u % t_units;
+        const int n_units = (int)min(u_end - u, t_units - t0);
+        u += n_units;
+        const int c0 = (g * 32 + (threadIdx.x & 31)) * kN;  // first channel of this thread
+        if (c0 >= p.D) continue;
 
-    // An empty request's conv state passes through (the tile-0 items do it).
-    if (tile == 0) {
-        for (int i = 0; i < p.R; ++i) {
-            if (p.cu[i + 1] != p.cu[i]) continue;
-            T *dst = state_slot(io.write_slots, i, SSD_DEVERR_FINAL_SLOT);
-            if (!dst) continue;
-            const T *src = state_slot(io.read_slots, i, SSD_DEVERR_INIT_SLOT);
-            for (int e = 0; e < kN * (W - 1); ++e)
-                dst[(size_t)c0 * (W - 1) + e] = src ? src[(size_t)c0 * (W - 1) + e] : from_f32<T>(0.f);
-        }
-    }
-    if (t0 >= p.T) return;
-    const int n = (int)min(p.T - t0, (int64_t)kTile);  // tokens of this tile
-    const size_t row = (size_t)p.D;
-    const T *xt = xv + (size_t)t0 * row + c0;  // this thread's vector of token t0
-    T *yt = yv + (size_t)t0 * row + c0;
-    uint4 *mine = &ring[0][threadIdx.x];  // stage s at mine[s * kConvThreads]
-
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) {  // one copy group per stage, empty past the tile
-        if (s < n) cp_async16(mine + s * kConvThreads, xt + (size_t)s * row);
-        cp_async_commit();
-    }
-
-    float wt[W][kN], bs[kN];
-#pragma unroll
-    for (int e = 0; e < kN; ++e) {
-        bs[e] = io.bias ? io.bias[c0 + e] : 0.f;
-#pragma unroll
-        for (int k = 0; k < W; ++k) wt[k][e] = io.weight[(size_t)(c0 + e) * W + k];
-    }
-
-    // window: win[0..W-2] the W-1 inputs before token t, win[W-1] token t
-    Vec<T> win[W];
-    int i = request_of(p.cu, p.R, t0);
-    int64_t rs = p.cu[i];
-    int rel_end = (int)min((int64_t)p.cu[i + 1] - t0, (int64_t)kTile + 1);  // request end, tile-relative
-    auto enter = [&](int64_t t) {  // fill win[0..W-2] with the inputs before t in its request
-        const T *src = nullptr;
-        if (t - rs < W - 1) src = state_slot(io.read_slots, i, SSD_DEVERR_INIT_SLOT);
-#pragma unroll
-        for (int k = 0; k < W - 1; ++k) {
-            const int64_t u = t - (W - 1) + k;
-            if (u >= rs && u >= 0) {
-                win[k].load(xv + (size_t)u * row + c0);
-            } else if (src) {
-                const int j = (int)(W - 1 - (rs - u));  // index in the conv state, oldest first
-#pragma unroll
-                for (int e = 0; e < kN; ++e) win[k].v[e] = to_f32(src[(size_t)(c0 + e) * (W - 1) + j]);
-            } else {
-                win[k].zero();
+        auto state_slot = [&](const int32_t *slots, int i, int bit) -> T * {
+            if (!slots || !pool) return nullptr;
+            const int s = slots[i];
+            if (s >= p.num_slots) {
+                if (c0 == 0) atomicOr(io.device_err, bit);
+                return nullptr;
             }
-        }
-    };
-    enter(t0);
-    for (int jb = 0; jb < n; jb += kUnroll) {
-        const int sb = jb % kStages;
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int j = jb + u;
-            if (j >= n) break;
-            if (j == rel_end) {  // the next non-empty request starts here
-                const int64_t t = t0 + j;
-                while (i + 1 < p.R && p.cu[i + 1] <= t) ++i;
-                rs = p.cu[i];
-                rel_end = (int)min((int64_t)p.cu[i + 1] - t0, (int64_t)kTile + 1);
-                enter(t);
-            }
-            const int st = sb + u < kStages ? sb + u : sb + u - kStages;
-            cp_async_wait<kStages - 1>();  // token j's copy group has landed
-            win[W - 1].set(mine[st * kConvThreads]);
-            Vec<T> out;
-#pragma unroll
-            for (int e = 0; e < kN; e += 2) {  // two channels per packed instruction
-                uint64_t acc = pair(bs[e], bs[e + 1]);
-#pragma unroll
-                for (int k = 0; k < W; ++k)
-                    acc = fma2(pair(wt[k][e], wt[k][e + 1]), pair(win[k].v[e], win[k].v[e + 1]), acc);
-                if (kSilu) acc = silu_pair(acc);
-                unpair(acc, out.v[e], out.v[e + 1]);
-            }
-            out.store(yt + (size_t)j * row);
-            if (j + 1 == rel_end) {  // the request's last token: its conv state goes out
+            return s >= 0 ? pool + (size_t)s * slot_elems : nullptr;
+        };
+
+        // An empty request's conv state passes through (the strip holding token 0 does it).
+        if (t0 == 0) {
+            for (int i = 0; i < p.R; ++i) {
+                if (p.cu[i + 1] != p.cu[i]) continue;
                 T *dst = state_slot(io.write_slots, i, SSD_DEVERR_FINAL_SLOT);
-                if (dst) store_conv_state<T, W>(dst, c0, win);
+                if (!dst) continue;
+                const T *src = state_slot(io.read_slots, i, SSD_DEVERR_INIT_SLOT);
+                for (int e = 0; e < kN * (W - 1); ++e)
+                    dst[(size_t)c0 * (W - 1) + e] = src ? src[(size_t)c0 * (W - 1) + e] : from_f32<T>(0.f);
             }
-            // refill the stage just read (its value is consumed above)
-            if (j + kStages < n) cp_async16(mine + st * kConvThreads, xt + (size_t)(j + kStages) * row);
-            cp_async_commit();
-#pragma unroll
-            for (int k = 0; k < W - 1; ++k) win[k] = win[k + 1];
         }
+        if (t0 >= p.T) continue;
+        const int n = n_units;  // tokens of this strip
+        const T *xt = xv + (size_t)t0 * row + c0;  // this thread's vector of token t0
+        T *yt = yv + (size_t)t0 * row + c0;
+
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {  // one copy group per stage, empty past the strip
+            if (s < n) cp_async16(mine + s * kConvThreads, xt + (size_t)s * row);
+            cp_async_commit();
+        }
+
+        float wt[W][kN], bs[kN];
+#pragma unroll
+        for (int e = 0; e < kN; ++e) {
+            bs[e] = io.bias ? io.bias[c0 + e] : 0.f;
+#pragma unroll
+            for (int k = 0; k < W; ++k) wt[k][e] = io.weight[(size_t)(c0 + e) * W + k];
+        }
+
+        // window: win[0..W-2] the W-1 inputs before token t, win[W-1] token t
+        Vec<T> win[W];
+        int i = request_of(p.cu, p.R, t0);
+        int64_t rs = p.cu[i];
+        int rel_end = (int)min((int64_t)p.cu[i + 1] - t0, (int64_t)n + 1);  // request end, strip-relative
+        auto enter = [&](int64_t t) {  // fill win[0..W-2] with the inputs before t in its request
+            const T *src = nullptr;
+            if (t - rs < W - 1) src = state_slot(io.read_slots, i, SSD_DEVERR_INIT_SLOT);
+#pragma unroll
+            for (int k = 0; k < W - 1; ++k) {
+                const int64_t v = t - (W - 1) + k;
+                if (v >= rs && v >= 0) {
+                    win[k].load(xv + (size_t)v * row + c0);
+                } else if (src) {
+                    const int j = (int)(W - 1 - (rs - v));  // index in the conv state, oldest first
+#pragma unroll
+                    for (int e = 0; e < kN; ++e) win[k].v[e] = to_f32(src[(size_t)(c0 + e) * (W - 1) + j]);
+                } else {
+                    win[k].zero();
+                }
+            }
+        };
+        enter(t0);
+        for (int jb = 0; jb < n; jb += kUnroll) {
+            const int sb = jb % kStages;
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) {
+                const int j = jb + q;
+                if (j >= n) break;
+                if (j == rel_end) {  // the next non-empty request starts here
+                    const int64_t t = t0 + j;
+                    while (i + 1 < p.R && p.cu[i + 1] <= t) ++i;
+                    rs = p.cu[i];
+                    rel_end = (int)min((int64_t)p.cu[i + 1] - t0, (int64_t)n + 1);
+                    enter(t);
+                }
+                const int st = sb + q < kStages ? sb + q : sb + q - kStages;
+                cp_async_wait<kStages - 1>();  // token j's copy group has landed
+                win[W - 1].set(mine[st * kConvThreads]);
+                Vec<T> out;
+#pragma unroll
+                for (int e = 0; e < kN; e += 2) {  // two channels per packed instruction
+                    uint64_t acc = pair(bs[e], bs[e + 1]);
+#pragma unroll
+                    for (int k = 0; k < W; ++k)
+                        acc = fma2(pair(wt[k][e], wt[k][e + 1]), pair(win[k].v[e], win[k].v[e + 1]), acc);
+                    if (kSilu) acc = silu_pair(acc);
+                    unpair(acc, out.v[e], out.v[e + 1]);
+                }
+                out.store(yt + (size_t)j * row);
+                if (j + 1 == rel_end) {  // the request's last token: its conv state goes out
+                    T *dst = state_slot(io.write_slots, i, SSD_DEVERR_FINAL_SLOT);
+                    if (dst) store_conv_state<T, W>(dst, c0, win);
+                }
+                // refill the stage just read (its value is consumed above)
+                if (j + kStages < n) cp_async16(mine + st * kConvThreads, xt + (size_t)(j + kStages) * row);
+                cp_async_commit();
+#pragma unroll
+                for (int k = 0; k < W - 1; ++k) win[k] = win[k + 1];
+            }
+        }
+        cp_async_wait<0>();  // the ring is free for the next strip
     }
-    cp_async_wait<0>();
+}
+
+// CTAs of one conv kernel that fit on the current device at once (queried once
+// per device).
+template <typename T, int W, bool kSilu>
+cudaError_t conv_resident_ctas(int64_t &out) {
+    static int64_t cached[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (cached[dev] == 0) {
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv1d_kernel<T, W, kSilu>, kConvThreads, 0);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+        cached[dev] = (int64_t)per_sm * sms;
+    }
+    out = cached[dev];
+    return cudaSuccess;
+}
+
+// The grid: every resident CTA, or fewer when the strips would fall below
+// kMinStrip units a warp.
+template <typename T, int W, bool kSilu>
+cudaError_t launch_conv_k(const ConvParams &p, int64_t units, cudaStream_t stream) {
+    int64_t resident = 0;
+    const cudaError_t e = conv_resident_ctas<T, W, kSilu>(resident);
+    if (e != cudaSuccess) return e;
+    const int64_t warps = (units + kMinStrip - 1) / kMinStrip;
+    const int64_t ctas = std::max<int64_t>(1, std::min(resident, (warps + kConvThreads / 32 - 1) / (kConvThreads / 32)));
+    conv1d_kernel<T, W, kSilu><<<dim3((unsigned)ctas), kConvThreads, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 template <typename T, int W>
-void launch_conv_w(const ConvParams &p, dim3 grid, cudaStream_t stream) {
-    if (p.silu) conv1d_kernel<T, W, true><<<grid, kConvThreads, 0, stream>>>(p);
-    else conv1d_kernel<T, W, false><<<grid, kConvThreads, 0, stream>>>(p);
+cudaError_t launch_conv_w(const ConvParams &p, int64_t units, cudaStream_t stream) {
+    return p.silu ? launch_conv_k<T, W, true>(p, units, stream) : launch_conv_k<T, W, false>(p, units, stream);
 }
 
 template <typename T>
 cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t stream) {
     constexpr int kN = 16 / sizeof(T);
-    const int64_t tiles = (p.T + kTile - 1) / kTile;
     const int64_t groups = (p.D / kN + 31) / 32;
-    const int64_t items = (tiles > 0 ? tiles : 1) * groups;
-    const int64_t ctas = (items + kConvThreads / 32 - 1) / (kConvThreads / 32);
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)ctas);
+    const int64_t units = groups * (p.T > 0 ? p.T : 1);  // as the kernel counts them
     switch (p.W) {
-        case 2: launch_conv_w<T, 2>(p, grid, stream); break;
-        case 3: launch_conv_w<T, 3>(p, grid, stream); break;
-        case 4: launch_conv_w<T, 4>(p, grid, stream); break;
+        case 2: return launch_conv_w<T, 2>(p, units, stream);
+        case 3: return launch_conv_w<T, 3>(p, units, stream);
+        case 4: return launch_conv_w<T, 4>(p, units, stream);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 bool aligned_to(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }

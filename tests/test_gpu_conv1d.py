@@ -69,6 +69,15 @@ def test_tiles_across_request_boundaries(dtype, W):
     run_and_check(workloads.make_conv_problem(_spec(W=W, dtype=dtype), seed=W, device="cuda", canary=2.0))
 
 
+@pytest.mark.parametrize("lengths", [[331], [100, 0, 231], [7, 300, 24]])
+def test_strips_across_channel_groups(lengths):
+    # warps take even strips of the (channel group, token) units: with three
+    # channel groups (D = 520 bf16: 65 vectors, the last group one lane wide) and
+    # 331 tokens, strips start inside requests and one crosses into the next group
+    spec = _spec(D=520, lengths=lengths)
+    run_and_check(workloads.make_conv_problem(spec, seed=len(lengths), device="cuda", canary=1.25))
+
+
 def test_no_activation_no_bias_many_channels():
     spec = _spec(D=2056, silu=False, has_bias=False, lengths=[200, 1, 1, 77])
     run_and_check(workloads.make_conv_problem(spec, seed=8, device="cuda", canary=0.5))
