@@ -16,14 +16,32 @@
 // registers: thread k owns KV consecutive elements of one state row p (KV
 // divides N, the N / KV threads of a row are adjacent lanes), so the state is
 // read once and each write anchor is one coalesced vector store; the row's
-// C.h dot product is a shuffle reduction over its lanes.  The step is bound by
-// the state traffic (4 P N bytes read, 4 P N per written anchor).
+// C.h dot product is a shuffle reduction over its lanes.  The window's B and C
+// rows, the head's x row, dt', the decay and the write slot of up to
+// kStageTok tokens are staged in shared memory by the whole CTA, so the P
+// state rows that read the same values do so from shared memory and the
+// global load path carries each value once.  The step is bound by the state
+// traffic (4 P N bytes read, 4 P N per written anchor).
 #include "ssd_internal.cuh"
 
 namespace ssd {
 namespace {
 
 constexpr int kDecThreads = 256;
+constexpr int kStageTok = 8;  // window tokens staged in shared memory at a time
+
+// Shared-memory layout of one stage (bytes): B rows, C rows, x rows of the head,
+// then dt', the decay and the write slot of each token.
+struct DecStage {
+    int off_c, off_x, off_f, bytes;
+    __host__ __device__ DecStage(int N, int P, int esize) {
+        const int nb = N * esize;  // a multiple of 32 (N a power of two >= 16)
+        off_c = kStageTok * nb;
+        off_x = 2 * kStageTok * nb;
+        off_f = off_x + (kStageTok * P * esize + 15) / 16 * 16;
+        bytes = off_f + 3 * kStageTok * 4;
+    }
+};
 
 struct DecParams {
     int64_t T;
@@ -96,7 +114,9 @@ __device__ __forceinline__ void store_state(float *dst, const float (&h)[KV]) {
 }
 
 template <typename T, int KV>
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ DecParams p) {
+// Four CTAs per SM up to KV = 32 (64 registers a thread: the bf16 instance fits,
+// the fp32 one spills 12 bytes); KV = 64 keeps all the registers it needs.
+__global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(const __grid_constant__ DecParams p) {
     const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     const int g = hh / (p.H / p.G);
     const int rowlanes = p.N / KV;                   // threads per state row (power of 2, <= 32)
@@ -129,51 +149,85 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     const float Dh = io.D ? io.D[hh] : 0.f;
     const T *Bv = static_cast<const T *>(io.B);
     const T *Cv = static_cast<const T *>(io.C);
-    for (int64_t t = a; t < b; ++t) {
-        const float dtp = softplus_f32(ld_val<T>(io.dt, (size_t)t * p.H + hh) + dtb);
-        const float decay = expf(dtp * Ah);
-        const size_t xi = ((size_t)t * p.H + hh) * p.P + pr;
-        const float xv = active ? ld_val<T>(io.x, xi) : 0.f;
-        const float coef = dtp * xv;
-        float acc = 0.f;
-        if (active) {
-            float bv[KV], cv[KV];
-            const size_t bc = ((size_t)t * p.G + g) * p.N + n0;
-            load_vec<T, KV>(Bv + bc, bv);
-            load_vec<T, KV>(Cv + bc, cv);
+    const T *Xv = static_cast<const T *>(io.x);
+    extern __shared__ __align__(16) uint8_t dec_smem[];
+    const DecStage L(p.N, p.P, (int)sizeof(T));
+    const T *sB = reinterpret_cast<const T *>(dec_smem);
+    const T *sC = reinterpret_cast<const T *>(dec_smem + L.off_c);
+    T *sX = reinterpret_cast<T *>(dec_smem + L.off_x);
+    float *sDtp = reinterpret_cast<float *>(dec_smem + L.off_f);
+    float *sDec = sDtp + kStageTok;
+    int *sWs = reinterpret_cast<int *>(sDec + kStageTok);
+    const int vrow = p.N * (int)sizeof(T) / 16;  // 16-byte vectors per B or C row
+    for (int64_t tc = a; tc < b; tc += kStageTok) {
+        const int nt = (int)min((int64_t)kStageTok, b - tc);
+        // ---- stage tokens tc .. tc+nt-1 (every thread, active or not)
+        for (int v = threadIdx.x; v < 2 * nt * vrow; v += kDecThreads) {
+            const int cmat = v / (nt * vrow), rem = v % (nt * vrow);
+            const int tt = rem / vrow, c = rem % vrow;
+            const T *src = (cmat ? Cv : Bv) + ((size_t)(tc + tt) * p.G + g) * p.N;
+            reinterpret_cast<uint4 *>(dec_smem + (cmat ? L.off_c : 0) + (size_t)tt * p.N * sizeof(T))[c] =
+                reinterpret_cast<const uint4 *>(src)[c];
+        }
+        for (int v = threadIdx.x; v < nt * p.P; v += kDecThreads) {
+            const int tt = v / p.P, c = v % p.P;
+            sX[v] = Xv[((size_t)(tc + tt) * p.H + hh) * p.P + c];
+        }
+        if (threadIdx.x < nt) {
+            const int64_t t = tc + threadIdx.x;
+            const float dtp = softplus_f32(ld_val<T>(io.dt, (size_t)t * p.H + hh) + dtb);
+            sDtp[threadIdx.x] = dtp;
+            sDec[threadIdx.x] = expf(dtp * Ah);
+            sWs[threadIdx.x] = io.write_slots ? io.write_slots[t] : -1;
+        }
+        __syncthreads();
+        for (int tt = 0; tt < nt; ++tt) {
+            const int64_t t = tc + tt;
+            const float dtp = sDtp[tt], decay = sDec[tt];
+            const size_t xi = ((size_t)t * p.H + hh) * p.P + pr;
+            const float xv = active ? to_f32(sX[tt * p.P + pr]) : 0.f;
+            const float coef = dtp * xv;
+            float acc = 0.f;
+            if (active) {
+                float bv[KV], cv[KV];
+                load_vec<T, KV>(sB + (size_t)tt * p.N + n0, bv);
+                load_vec<T, KV>(sC + (size_t)tt * p.N + n0, cv);
 #pragma unroll
-            for (int j = 0; j < KV; ++j) {
-                h[j] = fmaf(decay, h[j], coef * bv[j]);
-                acc = fmaf(cv[j], h[j], acc);
+                for (int j = 0; j < KV; ++j) {
+                    h[j] = fmaf(decay, h[j], coef * bv[j]);
+                    acc = fmaf(cv[j], h[j], acc);
+                }
+            }
+            // the row's C.h over its rowlanes adjacent lanes
+            for (int o = rowlanes >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (active && n0 == 0) {
+                float yv = fmaf(Dh, xv, acc);
+                if (io.z) yv *= silu_f32(ld_val<T>(io.z, xi));
+                static_cast<T *>(io.y)[xi] = from_f32<T>(yv);
+            }
+            const int ws = sWs[tt];
+            if (ws >= p.num_slots) {
+                if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_FINAL_SLOT);
+            } else if (ws >= 0 && active) {
+                store_state<KV>(io.state_pool + (size_t)ws * slot_elems + hh * pn + e0, h);
             }
         }
-        // the row's C.h over its rowlanes adjacent lanes
-        for (int o = rowlanes >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (active && n0 == 0) {
-            float yv = fmaf(Dh, xv, acc);
-            if (io.z) yv *= silu_f32(ld_val<T>(io.z, xi));
-            static_cast<T *>(io.y)[xi] = from_f32<T>(yv);
-        }
-        const int ws = io.write_slots ? io.write_slots[t] : -1;
-        if (ws >= p.num_slots) {
-            if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_FINAL_SLOT);
-        } else if (ws >= 0 && active) {
-            store_state<KV>(io.state_pool + (size_t)ws * slot_elems + hh * pn + e0, h);
-        }
+        __syncthreads();  // the stage is rewritten by the next tokens
     }
 }
 
 template <typename T>
 cudaError_t launch_decode_t(const DecParams &p, int kv, cudaStream_t stream) {
     const dim3 grid((unsigned)((int64_t)p.R * p.H)), block(kDecThreads);
+    const size_t smem = (size_t)DecStage(p.N, p.P, (int)sizeof(T)).bytes;
     switch (kv) {
-        case 1: decode_kernel<T, 1><<<grid, block, 0, stream>>>(p); break;
-        case 2: decode_kernel<T, 2><<<grid, block, 0, stream>>>(p); break;
-        case 4: decode_kernel<T, 4><<<grid, block, 0, stream>>>(p); break;
-        case 8: decode_kernel<T, 8><<<grid, block, 0, stream>>>(p); break;
-        case 16: decode_kernel<T, 16><<<grid, block, 0, stream>>>(p); break;
-        case 32: decode_kernel<T, 32><<<grid, block, 0, stream>>>(p); break;
-        case 64: decode_kernel<T, 64><<<grid, block, 0, stream>>>(p); break;
+        case 1: decode_kernel<T, 1><<<grid, block, smem, stream>>>(p); break;
+        case 2: decode_kernel<T, 2><<<grid, block, smem, stream>>>(p); break;
+        case 4: decode_kernel<T, 4><<<grid, block, smem, stream>>>(p); break;
+        case 8: decode_kernel<T, 8><<<grid, block, smem, stream>>>(p); break;
+        case 16: decode_kernel<T, 16><<<grid, block, smem, stream>>>(p); break;
+        case 32: decode_kernel<T, 32><<<grid, block, smem, stream>>>(p); break;
+        case 64: decode_kernel<T, 64><<<grid, block, smem, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
