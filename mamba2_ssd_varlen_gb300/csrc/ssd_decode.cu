@@ -13,9 +13,10 @@
 //       state_pool[write_slots[t]] <- h   when write_slots[t] >= 0
 //
 // One CTA of 256 threads per (request, head).  The (P, N) fp32 state lives in
-// registers: thread k owns KV consecutive elements of one state row p (KV
-// divides N, the N / KV threads of a row are adjacent lanes), so the state is
-// read once and each write anchor is one coalesced vector store; the row's
+// registers: thread k owns KV elements of one state row p (KV divides N, the
+// N / KV threads of a row are adjacent lanes), in chunks of 4 columns
+// interleaved with the row's other threads, so the state is read once and each
+// write anchor is a run of 16-byte stores that fill whole sectors; the row's
 // C.h dot product is a shuffle reduction over its lanes.  The window's B and C
 // rows, the head's x row, dt', the decay and the write slot of up to
 // kStageTok tokens are staged in shared memory by the whole CTA, so the P
@@ -55,61 +56,74 @@ __device__ __forceinline__ float ld_val(const void *base, size_t i) {
     return to_f32(static_cast<const T *>(base)[i]);
 }
 
-// KV consecutive values of a bf16 or fp32 row, from 16-byte aligned storage
-// when KV allows, into fp32.
+// A thread's KV state elements of row p are KV / CW chunks of CW = min(KV, 4)
+// consecutive columns, chunk m at column CW (l + lanes m) for the thread's index l
+// among the row's `lanes` threads: one 16-byte store instruction of a warp then
+// writes lanes x 16 consecutive bytes of each row (whole 32-byte sectors)
+// instead of 16 bytes every 4 KV.
+template <int KV>
+struct Chunks {
+    static constexpr int CW = KV < 4 ? KV : 4;
+    static constexpr int NC = KV / CW;
+};
+
+template <int KV>
+__device__ __forceinline__ void load_row_chunks(const float *row, int col0, int stride, float (&h)[KV]) {
+    constexpr int CW = Chunks<KV>::CW;
+#pragma unroll
+    for (int m = 0; m < Chunks<KV>::NC; ++m) {
+        const float *src = row + col0 + m * stride;
+        if constexpr (CW == 4) {
+            const float4 q = *reinterpret_cast<const float4 *>(src);
+            h[4 * m] = q.x;
+            h[4 * m + 1] = q.y;
+            h[4 * m + 2] = q.z;
+            h[4 * m + 3] = q.w;
+        } else {
+#pragma unroll
+            for (int c = 0; c < CW; ++c) h[CW * m + c] = src[c];
+        }
+    }
+}
+
+template <int KV>
+__device__ __forceinline__ void store_row_chunks(float *row, int col0, int stride, const float (&h)[KV]) {
+    constexpr int CW = Chunks<KV>::CW;
+#pragma unroll
+    for (int m = 0; m < Chunks<KV>::NC; ++m) {
+        float *dst = row + col0 + m * stride;
+        if constexpr (CW == 4) {
+            *reinterpret_cast<float4 *>(dst) = make_float4(h[4 * m], h[4 * m + 1], h[4 * m + 2], h[4 * m + 3]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CW; ++c) dst[c] = h[CW * m + c];
+        }
+    }
+}
+
+// The same chunks of a staged bf16 or fp32 B or C row, into fp32.
 template <typename T, int KV>
-__device__ __forceinline__ void load_vec(const T *src, float (&dst)[KV]) {
-    if constexpr (sizeof(T) == 2 && KV % 8 == 0) {
+__device__ __forceinline__ void load_vec_chunks(const T *row, int col0, int stride, float (&dst)[KV]) {
+    constexpr int CW = Chunks<KV>::CW;
 #pragma unroll
-        for (int j = 0; j < KV; j += 8) {
-            const uint4 q = *reinterpret_cast<const uint4 *>(src + j);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int m = 0; m < Chunks<KV>::NC; ++m) {
+        const T *src = row + col0 + m * stride;
+        if constexpr (CW == 4 && sizeof(T) == 2) {
+            const uint2 q = *reinterpret_cast<const uint2 *>(src);
+            dst[4 * m] = __uint_as_float(q.x << 16);
+            dst[4 * m + 1] = __uint_as_float(q.x & 0xFFFF0000u);
+            dst[4 * m + 2] = __uint_as_float(q.y << 16);
+            dst[4 * m + 3] = __uint_as_float(q.y & 0xFFFF0000u);
+        } else if constexpr (CW == 4) {
+            const float4 q = *reinterpret_cast<const float4 *>(src);
+            dst[4 * m] = q.x;
+            dst[4 * m + 1] = q.y;
+            dst[4 * m + 2] = q.z;
+            dst[4 * m + 3] = q.w;
+        } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                dst[j + 2 * e] = __uint_as_float(w[e] << 16);
-                dst[j + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-            }
+            for (int c = 0; c < CW; ++c) dst[CW * m + c] = to_f32(src[c]);
         }
-    } else if constexpr (sizeof(T) == 4 && KV % 4 == 0) {
-#pragma unroll
-        for (int j = 0; j < KV; j += 4) {
-            const float4 q = *reinterpret_cast<const float4 *>(src + j);
-            dst[j] = q.x;
-            dst[j + 1] = q.y;
-            dst[j + 2] = q.z;
-            dst[j + 3] = q.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < KV; ++j) dst[j] = to_f32(src[j]);
-    }
-}
-
-template <int KV>
-__device__ __forceinline__ void load_state(const float *src, float (&h)[KV]) {
-    if constexpr (KV % 4 == 0) {
-#pragma unroll
-        for (int j = 0; j < KV; j += 4) {
-            const float4 q = *reinterpret_cast<const float4 *>(src + j);
-            h[j] = q.x;
-            h[j + 1] = q.y;
-            h[j + 2] = q.z;
-            h[j + 3] = q.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < KV; ++j) h[j] = src[j];
-    }
-}
-
-template <int KV>
-__device__ __forceinline__ void store_state(float *dst, const float (&h)[KV]) {
-    if constexpr (KV % 4 == 0) {
-#pragma unroll
-        for (int j = 0; j < KV; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(h[j], h[j + 1], h[j + 2], h[j + 3]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < KV; ++j) dst[j] = h[j];
     }
 }
 
@@ -120,11 +134,13 @@ __global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(c
     const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     const int g = hh / (p.H / p.G);
     const int rowlanes = p.N / KV;                   // threads per state row (power of 2, <= 32)
-    const int e0 = threadIdx.x * KV;                 // first state element of this thread
-    const bool active = e0 < p.P * p.N;
-    const int pr = active ? e0 / p.N : 0;            // state row p
-    const int n0 = e0 % p.N;                         // first column n
+    const int tl = threadIdx.x % rowlanes;           // this thread's index among them
+    const bool active = (int)threadIdx.x < p.P * rowlanes;
+    const int pr = active ? (int)threadIdx.x / rowlanes : 0;  // state row p
+    constexpr int CW = Chunks<KV>::CW;
+    const int col0 = CW * tl, cstride = CW * rowlanes;  // chunk m at column col0 + m cstride
     const size_t pn = (size_t)p.P * p.N, slot_elems = (size_t)p.H * pn;
+    const size_t row_off = (size_t)hh * pn + (size_t)pr * p.N;
     const ssd_decode_io &io = p.io;
 
     const int64_t a = p.cu[i], b = p.cu[i + 1];
@@ -140,7 +156,7 @@ __global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(c
         if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_INIT_SLOT);
     }
     if (active && rs >= 0 && rs < p.num_slots) {
-        load_state<KV>(io.state_pool + (size_t)rs * slot_elems + hh * pn + e0, h);
+        load_row_chunks<KV>(io.state_pool + (size_t)rs * slot_elems + row_off, col0, cstride, h);
     } else {
 #pragma unroll
         for (int j = 0; j < KV; ++j) h[j] = 0.f;
@@ -190,8 +206,8 @@ __global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(c
             float acc = 0.f;
             if (active) {
                 float bv[KV], cv[KV];
-                load_vec<T, KV>(sB + (size_t)tt * p.N + n0, bv);
-                load_vec<T, KV>(sC + (size_t)tt * p.N + n0, cv);
+                load_vec_chunks<T, KV>(sB + (size_t)tt * p.N, col0, cstride, bv);
+                load_vec_chunks<T, KV>(sC + (size_t)tt * p.N, col0, cstride, cv);
 #pragma unroll
                 for (int j = 0; j < KV; ++j) {
                     h[j] = fmaf(decay, h[j], coef * bv[j]);
@@ -200,7 +216,7 @@ __global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(c
             }
             // the row's C.h over its rowlanes adjacent lanes
             for (int o = rowlanes >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (active && n0 == 0) {
+            if (active && tl == 0) {
                 float yv = fmaf(Dh, xv, acc);
                 if (io.z) yv *= silu_f32(ld_val<T>(io.z, xi));
                 static_cast<T *>(io.y)[xi] = from_f32<T>(yv);
@@ -209,7 +225,7 @@ __global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(c
             if (ws >= p.num_slots) {
                 if (threadIdx.x == 0 && hh == 0) atomicOr(io.device_err, SSD_DEVERR_FINAL_SLOT);
             } else if (ws >= 0 && active) {
-                store_state<KV>(io.state_pool + (size_t)ws * slot_elems + hh * pn + e0, h);
+                store_row_chunks<KV>(io.state_pool + (size_t)ws * slot_elems + row_off, col0, cstride, h);
             }
         }
         __syncthreads();  // the stage is rewritten by the next tokens
