@@ -66,7 +66,11 @@ def test_tiny_fp32_config():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("P,N", [(64, 128), (128, 128), (32, 64), (16, 16), (8, 256)])
+# elements per thread KV and threads per row N / KV: (64, 128) 32 / 4, (128, 128) 64 / 2,
+# (32, 64) 8 / 8, (16, 16) 1 / 16, (8, 256) 8 / 32, (33, 64) 16 / 4 with idle threads,
+# (256, 64) 64 / 1, (24, 32) 4 / 8, (24, 16) 2 / 8
+@pytest.mark.parametrize("P,N", [(64, 128), (128, 128), (32, 64), (16, 16), (8, 256), (33, 64), (256, 64),
+                                 (24, 32), (24, 16)])
 def test_windows_every_shape(dtype, P, N):
     spec = _spec(P=P, N=N, dtype=dtype)
     run_and_check(workloads.make_decode_problem(spec, seed=11 + P + N, device="cuda", canary=3.5))
