@@ -307,16 +307,18 @@ cudaError_t conv_resident_ctas(int64_t &out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (cached[dev] == 0) {
-        int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv1d_kernel<T, W, kSilu>, kConvThreads, 0);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
-        cached[dev] = (int64_t)per_sm * sms;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (cacheable && cached[dev] > 0) {
+        out = cached[dev];
+        return cudaSuccess;
     }
-    out = cached[dev];
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv1d_kernel<T, W, kSilu>, kConvThreads, 0);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+    out = (int64_t)per_sm * sms;
+    if (cacheable) cached[dev] = out;
     return cudaSuccess;
 }
 
