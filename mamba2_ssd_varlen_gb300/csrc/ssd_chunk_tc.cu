@@ -1103,7 +1103,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 // Per (request, head): chains the segment end states of a long request,
 //   h <- initial state;  for every segment k but the last:
 //   h <- decay_k h + S_k  and store it in slot k (= entering state of segment k+1),
-// and writes an empty request's final state (its initial state).
+// and writes an empty request's final state (its initial state).  The chain
+// loads kSegPassBatch segments' states and decays before it updates and stores
+// them, so a batch costs one memory round trip instead of one per segment.
+constexpr int kSegPassBatch = 8;
+
 template <int P>
 __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
     const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
@@ -1117,14 +1121,14 @@ __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
     }
     if (p.segs[first].len == 0) {
         // An empty request: its final state is its initial state.
-        if (threadIdx.x == 0 && p.init_slots && p.init_slots[i] >= p.num_slots)
-            atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
+        const bool reporter = threadIdx.x == 0;
+        if (reporter && p.init_slots && p.init_slots[i] >= p.num_slots) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
         float *fd = p.final_states ? p.final_states + (size_t)i * slot_elems + hh * pn : nullptr;
         float *fs = nullptr;
         if (p.final_slots) {
             const int fslot = p.final_slots[i];
             if (fslot >= p.num_slots) {
-                if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
+                if (reporter) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_FINAL_SLOT);
             } else if (fslot >= 0) {
                 fs = p.pool + (size_t)fslot * slot_elems + hh * pn;
             }
@@ -1137,14 +1141,30 @@ __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
         return;
     }
     if (cnt <= 1) return;
+    const int nk = cnt - 1;
     for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
         float4 h = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < cnt - 1; ++k) {
-            const float dk = p.seg_decay[(size_t)(first + k) * p.H + hh];
-            float4 *sp = reinterpret_cast<float4 *>(p.seg_state + (size_t)(first + k) * slot_elems + hh * pn + e);
-            const float4 sv = *sp;
-            h = make_float4(fmaf(dk, h.x, sv.x), fmaf(dk, h.y, sv.y), fmaf(dk, h.z, sv.z), fmaf(dk, h.w, sv.w));
-            *sp = h;
+        for (int k0 = 0; k0 < nk; k0 += kSegPassBatch) {
+            float4 sv[kSegPassBatch];
+            float dk[kSegPassBatch];
+#pragma unroll
+            for (int j = 0; j < kSegPassBatch; ++j) {
+                sv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                dk[j] = 0.f;
+                if (k0 + j < nk) {
+                    const size_t sg = (size_t)(first + k0 + j);
+                    dk[j] = p.seg_decay[sg * p.H + hh];
+                    sv[j] = *reinterpret_cast<const float4 *>(p.seg_state + sg * slot_elems + hh * pn + e);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kSegPassBatch; ++j) {
+                if (k0 + j < nk) {
+                    h = make_float4(fmaf(dk[j], h.x, sv[j].x), fmaf(dk[j], h.y, sv[j].y), fmaf(dk[j], h.z, sv[j].z),
+                                    fmaf(dk[j], h.w, sv[j].w));
+                    *reinterpret_cast<float4 *>(p.seg_state + (size_t)(first + k0 + j) * slot_elems + hh * pn + e) = h;
+                }
+            }
         }
     }
 }
@@ -1178,6 +1198,8 @@ bool make_map(CUtensorMap *m, const void *g, uint64_t d0, uint64_t d1, uint64_t 
 
 template <int P>
 cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t stream) {
+    const int64_t seg_ctas = (int64_t)p.R * p.H;
+    if (seg_ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     TcMaps maps;
     if (!make_map(&maps.x, p.x, P, p.H, p.T) || !make_map(&maps.b, p.B, 128, p.G, p.T) ||
         !make_map(&maps.c, p.C, 128, p.G, p.T) || !make_map(&maps.z, p.z ? p.z : p.x, P, p.H, p.T))
@@ -1201,7 +1223,7 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t
     ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    seg_pass_kernel<P><<<(unsigned)((int64_t)p.R * p.H), 256, 0, stream>>>(p);
+    seg_pass_kernel<P><<<(unsigned)seg_ctas, 256, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ssd_chunk_tc_kernel<P, false><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
