@@ -34,11 +34,14 @@
 //           the x tile;
 //   warp 1  MMA issuer (one lane) and TMEM owner;
 //   G1      warps 2-9: w x split tiles, causal mask;
-//   G2      warps 10-17: state bookkeeping, epilogue (y staged in shared memory
-//           and stored with coalesced writes), chunk/block/final states;
-//   warp 18 B and C tiles by TMA, each reloaded as soon as its last MMA of the
-//           piece has read it (C after y_inter, B after the state update);
-//   warp 19 z tiles by TMA (P = 64).
+//   G2      warps 10-17: state bookkeeping, epilogue (z read from global memory,
+//           y staged in the piece's x tile and stored with coalesced writes),
+//           chunk/block/final states;
+//   warp 18 B and C tiles by TMA into double buffers (P = 64), each buffer
+//           reloaded as soon as its last MMA has read it (C after y_inter, B
+//           after the state update), so the next piece's tiles load while this
+//           piece computes;
+//   warp 19 z tiles by TMA when the layout stages z (no current layout does).
 // Each of G1 and G2 has two warps per TMEM lane quadrant (thread r owns tile
 // row / TMEM lane r) that split the columns; many warps per role hide the
 // latency of TMEM and shared-memory traffic.
@@ -71,17 +74,20 @@ constexpr int kRows = 128;                   // tile rows (tokens per piece, at 
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Per-P layout choices.  P = 64 has room to double-buffer the x/z stage and the
-// y accumulators and to keep the state update S in its own TMEM columns;
+// Per-P layout choices.  P = 64 has room to double-buffer the x stage, the B
+// and C tiles and the y accumulators and to keep the state update S in its own
+// TMEM columns (z is then read by the epilogue and y staged in the x tile, which
+// is what makes the second B and C tiles fit: 232,448 bytes, the limit);
 // P = 128 fills shared memory and TMEM with one of each and updates the state
 // in place.
 template <int P>
 struct TcCfg {
-    static constexpr int kNS = (P == 64) ? 2 : 1;     // x/z stages
+    static constexpr int kNS = (P == 64) ? 2 : 1;     // x stages
     static constexpr int kNY = (P == 64) ? 2 : 1;     // y_intra / y_inter accumulator pairs in TMEM
     static constexpr bool kSepS = (P == 64);          // state update in its own columns
-    static constexpr bool kZTile = (P == 64);         // z staged by TMA
-    static constexpr bool kSepY = (P == 64);          // y staged in its own tile (else in the x tile)
+    static constexpr bool kZTile = false;             // z read by the epilogue
+    static constexpr bool kSepY = false;              // y staged in the x tile
+    static constexpr int kNBC = (P == 64) ? 2 : 1;    // B and C tiles each
     // Slots of the per-piece decay values.  With y in its own tile G2 does not
     // hold the x stage, so the values G2 reads get their own deeper ring (and
     // barriers); otherwise they live and die with the x stage.
@@ -99,8 +105,8 @@ template <int P>
 struct __align__(1024) TcSmem {
     using Cfg = TcCfg<P>;
     uint8_t x[Cfg::kNS * Cfg::kXBytes];  // x tiles; a finished stage also stages y for the store
-    uint8_t b[kRows * 128 * 2];          // B tile: 2 sub-tiles (n 0-63, 64-127)
-    uint8_t c[kRows * 128 * 2];          // C tile
+    uint8_t b[Cfg::kNBC * kRows * 128 * 2];  // B tiles: 2 sub-tiles each (n 0-63, 64-127)
+    uint8_t c[Cfg::kNBC * kRows * 128 * 2];  // C tiles
     uint8_t xd_hi[Cfg::kXBytes];         // w x, hi and lo parts (MN-major B operand)
     uint8_t xd_lo[Cfg::kXBytes];
     uint8_t h_hi[128 * P * 2];           // h^T (rows n, P columns), hi and lo parts
@@ -111,7 +117,7 @@ struct __align__(1024) TcSmem {
     float dtp[Cfg::kNC][kRows];          // per slot: dt' (zero beyond the piece's length)
     float cslast[Cfg::kNC];              // per slot: the piece's total decay (log2 units)
     uint64_t full_x[2], empty_x[2], full_z[2], empty_z[2];
-    uint64_t full_b, empty_b, full_c, empty_c;
+    uint64_t full_b[2], empty_b[2], full_c[2], empty_c[2];
     uint64_t full_cs[4], empty_cs[4];    // decay-value ring (kSepY only)
     uint64_t cb_full, m_full, m_done;
     uint64_t y_full[2], y_empty[2];
@@ -434,10 +440,12 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             // every role but the producer takes each item: MMA, G1 and G2 warps, loaders
             mbar_init(&s.item_empty[i], 2 + 2 * kMathPerRole + (z_tile ? 1 : 0));
         }
-        mbar_init(&s.full_b, 1);
-        mbar_init(&s.empty_b, 1);
-        mbar_init(&s.full_c, 1);
-        mbar_init(&s.empty_c, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.full_b[i], 1);
+            mbar_init(&s.empty_b[i], 1);
+            mbar_init(&s.full_c[i], 1);
+            mbar_init(&s.empty_c[i], 1);
+        }
         mbar_init(&s.cb_full, 1);
         mbar_init(&s.m_full, kMathPerRole);
         mbar_init(&s.m_done, 1);
@@ -578,8 +586,10 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 int64_t ae;
                 while (pcs.next(t0, len, ae)) {
                     const int st = pc % kNS, yb = pc % kNY;
-                    if (!wait_bar(&s.full_b, par(pc), abort_flag, p.hdr)) { ok = false; break; }
-                    if (!STATE_ONLY && !wait_bar(&s.full_c, par(pc), abort_flag, p.hdr)) { ok = false; break; }
+                    const uint32_t bsl = pc % Cfg::kNBC, buse = pc / Cfg::kNBC;
+                    const uint32_t bo = bsl * (kRows * 128 * 2 >> 4);  // descriptor offset of the buffer
+                    if (!wait_bar(&s.full_b[bsl], par(buse), abort_flag, p.hdr)) { ok = false; break; }
+                    if (!STATE_ONLY && !wait_bar(&s.full_c[bsl], par(buse), abort_flag, p.hdr)) { ok = false; break; }
                     if (!STATE_ONLY) {
                         // CB = C B^T, once the previous piece's y_intra has read M out of these columns.
                         if (pc > 0 && !wait_bar(&s.m_done, par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
@@ -587,7 +597,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tbase, dC + (ko >> 4), dBk + (ko >> 4), i_cb, kk > 0);
+                            mma_ss(tbase, dC + bo + (ko >> 4), dBk + bo + (ko >> 4), i_cb, kk > 0);
                         }
                         mma_commit(&s.cb_full);
                         // y_inter = C h^T (h in hi + lo) into accumulator pair yb,
@@ -604,10 +614,10 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                mma_ss(tbase + Cfg::col_ye(yb), dC + (ko >> 4), dH + kk * 128, i_y, (part | kk) != 0);
+                                mma_ss(tbase + Cfg::col_ye(yb), dC + bo + (ko >> 4), dH + kk * 128, i_y, (part | kk) != 0);
                             }
                         }
-                        mma_commit(&s.empty_c);  // C has no further reader in this piece
+                        mma_commit(&s.empty_c[bsl]);  // C has no further reader in this piece
                     }
                     // state update: S = B^T (w x)  (or h^T += ... in place)
                     if (!wait_bar(&s.xd_full, par(pc), abort_flag, p.hdr)) { ok = false; break; }
@@ -618,11 +628,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         const uint64_t dXd = part ? dXl : dXh;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_ss(tbase + colS, dBm + kk * 128, dXd + kk * 128, i_s,
+                            mma_ss(tbase + colS, dBm + bo + kk * 128, dXd + kk * 128, i_s,
                                    Cfg::kSepS ? (uint32_t)((part | kk) != 0) : 1u);
                     }
                     mma_commit(&s.s_full);
-                    mma_commit(&s.empty_b);  // B has no further reader in this piece
+                    mma_commit(&s.empty_b[bsl]);  // B has no further reader in this piece
                     if (STATE_ONLY) {
                         mma_commit(&s.empty_x[st]);
                     } else {
@@ -1055,22 +1065,24 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             uint32_t pc = 0;
             while (cursor_next<false, STATE_ONLY>(cur, s, p, n_work, Qi, abort_flag, t0, len, ae)) {
                 const int g = cur.it.head / (p.H / p.G);
+                const uint32_t bsl = pc % Cfg::kNBC, buse = pc / Cfg::kNBC;
+                uint8_t *const cb = s.c + bsl * tbytes, *const bb = s.b + bsl * tbytes;
                 if (!STATE_ONLY) {
-                    if (pc >= 1 && !wait_bar(&s.empty_c, par(pc - 1), abort_flag, p.hdr)) break;
-                    mbar_arrive_expect_tx(&s.full_c, tbytes);
-                    tma_load_3d(s.c, &maps.c, &s.full_c, 0, g, t0);
-                    tma_load_3d(s.c + 16384, &maps.c, &s.full_c, 64, g, t0);
+                    if (buse >= 1 && !wait_bar(&s.empty_c[bsl], par(buse - 1), abort_flag, p.hdr)) break;
+                    mbar_arrive_expect_tx(&s.full_c[bsl], tbytes);
+                    tma_load_3d(cb, &maps.c, &s.full_c[bsl], 0, g, t0);
+                    tma_load_3d(cb + 16384, &maps.c, &s.full_c[bsl], 64, g, t0);
                 }
-                if (pc >= 1 && !wait_bar(&s.empty_b, par(pc - 1), abort_flag, p.hdr)) break;
-                mbar_arrive_expect_tx(&s.full_b, tbytes);
-                tma_load_3d(s.b, &maps.b, &s.full_b, 0, g, t0);
-                tma_load_3d(s.b + 16384, &maps.b, &s.full_b, 64, g, t0);
+                if (buse >= 1 && !wait_bar(&s.empty_b[bsl], par(buse - 1), abort_flag, p.hdr)) break;
+                mbar_arrive_expect_tx(&s.full_b[bsl], tbytes);
+                tma_load_3d(bb, &maps.b, &s.full_b[bsl], 0, g, t0);
+                tma_load_3d(bb + 16384, &maps.b, &s.full_b[bsl], 64, g, t0);
                 ++pc;
             }
             // Never leave a copy in flight.
-            if (pc > 0) {
-                mbar_wait(&s.full_b, par(pc - 1), kWaitNs);
-                if (!STATE_ONLY) mbar_wait(&s.full_c, par(pc - 1), kWaitNs);
+            for (uint32_t k = pc > (uint32_t)Cfg::kNBC ? pc - Cfg::kNBC : 0; k < pc; ++k) {
+                mbar_wait(&s.full_b[k % Cfg::kNBC], par(k / Cfg::kNBC), kWaitNs);
+                if (!STATE_ONLY) mbar_wait(&s.full_c[k % Cfg::kNBC], par(k / Cfg::kNBC), kWaitNs);
             }
         }
     } else {
