@@ -167,9 +167,26 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
 int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out,
                        cudaStream_t stream);
 
-/* Synchronises the plan's stream, returns the device error bits in
- * *device_err and clears them.  Returns SSD_OK or SSD_ERR_CUDA. */
+/* Synchronises the plan's stream (only that stream), returns the device error
+ * bits in *device_err and clears them.  Returns SSD_OK or SSD_ERR_CUDA. */
 int ssd_varlen_status(const ssd_plan *plan, int *device_err);
+
+/* Which kernel path ssd_varlen_forward takes for these arguments, without
+ * launching anything (same validation and return codes as the forward).
+ *   SSD_PATH_TENSOR_CORE: the fused chunked scan on the tensor cores (tcgen05,
+ *     TMEM, TMA): bf16 with P in {64, 128} and N = 128.  *tile (nullable)
+ *     receives its internal tile length in tokens: 128, or the chunk / block
+ *     granularity when exports or block checkpoints need a finer cut.  The
+ *     result does not depend on the tile (chunk_size only decides where
+ *     exports fall: "[Bugfix] Mamba2 SSD varlen bug fix initstates decay",
+ *     Purpose).
+ *   SSD_PATH_GENERAL: a token-serial recurrence on the CUDA cores, for fp32
+ *     inputs, every other bf16 shape and an all-empty batch; correct but one to
+ *     two orders of magnitude slower per token than the tensor-core path.
+ *     *tile receives 1. */
+enum ssd_path { SSD_PATH_TENSOR_CORE = 1, SSD_PATH_GENERAL = 2 };
+int ssd_varlen_forward_path(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out, int *path,
+                            int *tile);
 
 /* Static description of a status code or device error bit set. */
 const char *ssd_varlen_strerror(int code);
@@ -193,7 +210,9 @@ const char *ssd_varlen_strerror(int code);
  *   launch; invalid dims return the same codes as ssd_varlen_plan.
  * - The first call on a device looks up the array's device address with that
  *   device current (cudaGetSymbolAddress); make that first call before any
- *   stream capture on the device.
+ *   stream capture on the device.  The address is kept for the life of the
+ *   process: do not call this entry point again on a device after
+ *   cudaDeviceReset on it (the array may then live elsewhere).
  * - Every call shares the one array, which keeps the previous call's
  *   contents.  Calls whose GPU work overlaps (different streams or host
  *   threads without ordering) race on it: order them on one stream.  Each

@@ -11,6 +11,7 @@ The functions keep the C names:
   ssd_varlen_plan(dims, cu_seqlens, num_computed, workspace) -> Plan
   ssd_varlen_forward(plan, inputs, outputs)
   ssd_varlen_status(plan)                          -> device error bits
+  ssd_varlen_forward_path(plan, inputs, outputs)   -> (path, tile), no launch
   ssd_varlen_strerror(code)                        -> text
   ssd_varlen_forward_static(...)   (C only: forward without a caller workspace)
   ssd_varlen_decode(dims, cu_seqlens, io)        (decode / speculative-decode step)
@@ -42,7 +43,11 @@ STATUS = {
 EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_plan",
             "ssd_varlen_forward", "ssd_varlen_status", "ssd_varlen_strerror",
             "ssd_varlen_forward_static", "ssd_varlen_decode", "ssd_varlen_conv1d",
-            "ssd_varlen_align_bite", "ssd_varlen_gdn_forward", "ssd_varlen_check_slots"]
+            "ssd_varlen_align_bite", "ssd_varlen_gdn_forward", "ssd_varlen_check_slots",
+            "ssd_varlen_forward_path"]
+# enum ssd_path
+PATH_TENSOR_CORE = 1
+PATH_GENERAL = 2
 # Size of the library-owned scratch array used by ssd_varlen_forward_static.
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -147,6 +152,10 @@ def load_library():
     lib.ssd_varlen_gdn_forward.restype = ctypes.c_int
     lib.ssd_varlen_check_slots.argtypes = [ctypes.POINTER(ssd_dims), c_vp, c_vp, c_vp, c_vp, c_vp]
     lib.ssd_varlen_check_slots.restype = ctypes.c_int
+    lib.ssd_varlen_forward_path.argtypes = [ctypes.POINTER(ssd_plan), ctypes.POINTER(ssd_inputs),
+                                            ctypes.POINTER(ssd_outputs), ctypes.POINTER(ctypes.c_int),
+                                            ctypes.POINTER(ctypes.c_int)]
+    lib.ssd_varlen_forward_path.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -211,6 +220,18 @@ def ssd_varlen_status(plan: ssd_plan) -> int:
     if rc != 0:
         raise SsdError(rc, "ssd_varlen_status")
     return int(v.value)
+
+
+def ssd_varlen_forward_path(plan: ssd_plan, inputs: ssd_inputs, outputs: ssd_outputs):
+    """(path, tile): the kernel path ssd_varlen_forward takes for these arguments
+    (PATH_TENSOR_CORE or PATH_GENERAL) and its internal tile in tokens."""
+    path, tile = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load_library().ssd_varlen_forward_path(ctypes.byref(plan), ctypes.byref(inputs),
+                                                ctypes.byref(outputs), ctypes.byref(path),
+                                                ctypes.byref(tile))
+    if rc != 0:
+        raise SsdError(rc, "ssd_varlen_forward_path")
+    return int(path.value), int(tile.value)
 
 
 def make_inputs(x, dt, dt_bias, A, B, C, D=None, z=None, init_slots=None, state_pool=None):
@@ -279,6 +300,12 @@ class Call:
 
     def status(self) -> int:
         return ssd_varlen_status(self.plan)
+
+    def path(self):
+        """(path, tile) the forward of this call takes (plans first if needed)."""
+        if self.plan is None:
+            self.make_plan()
+        return ssd_varlen_forward_path(self.plan, self.inputs, self.outputs)
 
 
 def run(prob: dict, **kw) -> Call:

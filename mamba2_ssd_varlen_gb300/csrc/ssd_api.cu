@@ -8,6 +8,8 @@
 // metadata builder (plan) or the forward kernels on the caller's stream.
 #include <string.h>
 
+#include <algorithm>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -37,8 +39,20 @@ static int32_t pick_seg_len(const ssd_dims *d) {
     return 2048;
 }
 
+// Work segments of a batch, at most.  Every request has exactly one final
+// segment (an empty request one empty segment); its other segments end on a
+// multiple of seg_len strictly inside its positions (s, s + L - 1].  Such
+// boundaries number at most ceil((L - 1) / seg_len) per request, so over the
+// batch at most floor((T + R (seg_len - 2)) / seg_len); and as every segment
+// holds a token, at most T - 1.
+static int64_t nonfinal_segs_of(const ssd_dims *d, int32_t seg_len) {
+    const int64_t by_len = (d->T + (int64_t)d->R * (seg_len - 2)) / seg_len;
+    const int64_t by_tokens = d->T - 1;
+    return std::max<int64_t>(0, std::min(by_len, by_tokens));
+}
+
 static int64_t max_segs_of(const ssd_dims *d, int32_t seg_len) {
-    return d->T / seg_len + 2LL * d->R + 1;
+    return nonfinal_segs_of(d, seg_len) + d->R;
 }
 
 static WsLayout layout_of(const ssd_dims *d, int32_t seg_len) {
@@ -54,14 +68,87 @@ static WsLayout layout_of(const ssd_dims *d, int32_t seg_len) {
     w.req_first_chunk = take(sizeof(int32_t) * ((size_t)d->R + 1));
     w.req_first_seg = take(sizeof(int32_t) * ((size_t)d->R + 1));
     w.segs = take(sizeof(Seg) * (size_t)ms);
-    w.seg_state = take(sizeof(float) * (size_t)ms * d->H * d->P * d->N);
-    w.seg_decay = take(sizeof(float) * (size_t)ms * d->H);
+    // one state (and one decay per head) for each segment that is not the last of
+    // its request, indexed compactly: segment k of request i uses entry k - i
+    const int64_t nf = nonfinal_segs_of(d, seg_len);
+    w.seg_state = take(sizeof(float) * (size_t)nf * d->H * d->P * d->N);
+    w.seg_decay = take(sizeof(float) * (size_t)nf * d->H);
     w.total = off;
     return w;
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+// Checks every host-visible precondition of a forward and fills the kernel
+// parameters.  Launches nothing.
+static int forward_params(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out, FwdParams *p) {
+    if (!plan || !in || !out) return SSD_ERR_NULL;
+    if (plan->magic != kPlanMagic) return SSD_ERR_PLAN;
+    const ssd_dims *d = &plan->dims;
+    int rc = check_dims(d);
+    if (rc != SSD_OK) return rc;
+    if (!in->dt_bias || !in->A) return SSD_ERR_NULL;
+    // with no tokens (every request empty) the token buffers may be NULL
+    if (d->T > 0 && (!in->x || !in->dt || !in->B || !in->C || !out->y)) return SSD_ERR_NULL;
+    const void *big[] = {in->x, in->dt, in->B, in->C, in->z, out->y, in->state_pool,
+                         out->final_states, out->chunk_states};
+    for (const void *ptr : big)
+        if (ptr && !aligned16(ptr)) return SSD_ERR_ALIGN;
+    const void *small[] = {in->dt_bias, in->A, in->D, in->init_slots, out->final_slots, out->block_table};
+    for (const void *ptr : small)
+        if (ptr && !aligned4(ptr)) return SSD_ERR_ALIGN;
+    const bool uses_pool = in->init_slots || out->final_slots || out->block_table;
+    if (uses_pool && (!in->state_pool || d->num_slots < 1)) return SSD_ERR_NULL;
+    if (out->block_table && (d->block_size <= 0 || d->block_table_width < 1)) return SSD_ERR_BLOCK_SIZE;
+
+    const WsLayout w = layout_of(d, plan->seg_len);
+    if (plan->workspace_bytes < w.total) return SSD_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(plan->workspace);
+    p->T = d->T;
+    p->R = d->R;
+    p->H = d->H;
+    p->P = d->P;
+    p->N = d->N;
+    p->G = d->G;
+    p->Q = d->chunk_size;
+    p->num_slots = d->num_slots;
+    p->block_size = d->block_size;
+    p->bt_width = d->block_table_width;
+    p->seg_len = plan->seg_len;
+    p->cu_seqlens = plan->cu_seqlens;
+    p->num_computed = plan->num_computed;
+    p->hdr = (int32_t *)(ws + w.hdr);
+    p->req_first_chunk = (const int32_t *)(ws + w.req_first_chunk);
+    p->req_first_seg = (const int32_t *)(ws + w.req_first_seg);
+    p->segs = (const Seg *)(ws + w.segs);
+    p->seg_state = (float *)(ws + w.seg_state);
+    p->seg_decay = (float *)(ws + w.seg_decay);
+    p->x = in->x;
+    p->dt = in->dt;
+    p->B = in->B;
+    p->C = in->C;
+    p->z = in->z;
+    p->dt_bias = in->dt_bias;
+    p->A = in->A;
+    p->D = in->D;
+    p->init_slots = in->init_slots;
+    p->pool = in->state_pool;
+    p->y = out->y;
+    p->final_states = out->final_states;
+    p->final_slots = out->final_slots;
+    p->chunk_states = out->chunk_states;
+    p->block_table = out->block_table;
+    return SSD_OK;
+}
+
+// The kernel path a forward takes.  An empty batch (final = initial state for
+// every request) takes the general path, which needs no tensor maps over the
+// absent token buffers.
+static int path_of(const FwdParams &p, const ssd_dims *d) {
+    if (d->T > 0 && chunk_tc_supported(p, d->dtype)) return SSD_PATH_TENSOR_CORE;
+    return SSD_PATH_GENERAL;
+}
 
 }  // namespace ssd
 
@@ -119,69 +206,25 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
 
 int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out,
                        cudaStream_t stream) {
-    if (!plan || !in || !out) return SSD_ERR_NULL;
-    if (plan->magic != kPlanMagic) return SSD_ERR_PLAN;
-    const ssd_dims *d = &plan->dims;
-    int rc = check_dims(d);
-    if (rc != SSD_OK) return rc;
-    if (!in->dt_bias || !in->A) return SSD_ERR_NULL;
-    // with no tokens (every request empty) the token buffers may be NULL
-    if (d->T > 0 && (!in->x || !in->dt || !in->B || !in->C || !out->y)) return SSD_ERR_NULL;
-    const void *big[] = {in->x, in->dt, in->B, in->C, in->z, out->y, in->state_pool,
-                         out->final_states, out->chunk_states};
-    for (const void *ptr : big)
-        if (ptr && !aligned16(ptr)) return SSD_ERR_ALIGN;
-    const void *small[] = {in->dt_bias, in->A, in->D, in->init_slots, out->final_slots, out->block_table};
-    for (const void *ptr : small)
-        if (ptr && !aligned4(ptr)) return SSD_ERR_ALIGN;
-    const bool uses_pool = in->init_slots || out->final_slots || out->block_table;
-    if (uses_pool && (!in->state_pool || d->num_slots < 1)) return SSD_ERR_NULL;
-    if (out->block_table && (d->block_size <= 0 || d->block_table_width < 1)) return SSD_ERR_BLOCK_SIZE;
-
-    const WsLayout w = layout_of(d, plan->seg_len);
-    if (plan->workspace_bytes < w.total) return SSD_ERR_WORKSPACE;
-    char *ws = static_cast<char *>(plan->workspace);
     FwdParams p{};
-    p.T = d->T;
-    p.R = d->R;
-    p.H = d->H;
-    p.P = d->P;
-    p.N = d->N;
-    p.G = d->G;
-    p.Q = d->chunk_size;
-    p.num_slots = d->num_slots;
-    p.block_size = d->block_size;
-    p.bt_width = d->block_table_width;
-    p.seg_len = plan->seg_len;
-    p.cu_seqlens = plan->cu_seqlens;
-    p.num_computed = plan->num_computed;
-    p.hdr = (int32_t *)(ws + w.hdr);
-    p.req_first_chunk = (const int32_t *)(ws + w.req_first_chunk);
-    p.req_first_seg = (const int32_t *)(ws + w.req_first_seg);
-    p.segs = (const Seg *)(ws + w.segs);
-    p.seg_state = (float *)(ws + w.seg_state);
-    p.seg_decay = (float *)(ws + w.seg_decay);
-    p.x = in->x;
-    p.dt = in->dt;
-    p.B = in->B;
-    p.C = in->C;
-    p.z = in->z;
-    p.dt_bias = in->dt_bias;
-    p.A = in->A;
-    p.D = in->D;
-    p.init_slots = in->init_slots;
-    p.pool = in->state_pool;
-    p.y = out->y;
-    p.final_states = out->final_states;
-    p.final_slots = out->final_slots;
-    p.chunk_states = out->chunk_states;
-    p.block_table = out->block_table;
+    const int rc = forward_params(plan, in, out, &p);
+    if (rc != SSD_OK) return rc;
+    const ssd_dims *d = &plan->dims;
     if (d->T == 0 && !out->final_states && !out->final_slots) return SSD_OK;
-    // an empty batch (final = initial state for every request) takes the general
-    // path, which needs no tensor maps over the absent token buffers
-    cudaError_t e = (d->T > 0 && chunk_tc_supported(p, d->dtype)) ? launch_chunk_tc(p, plan->max_segs, stream)
-                                                                  : launch_recurrent(p, d->dtype, stream);
+    cudaError_t e = path_of(p, d) == SSD_PATH_GENERAL ? launch_recurrent(p, d->dtype, stream)
+                                                       : launch_chunk_tc(p, plan->max_segs, stream);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_varlen_forward_path(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out, int *path,
+                            int *tile) {
+    if (!path) return SSD_ERR_NULL;
+    FwdParams p{};
+    const int rc = forward_params(plan, in, out, &p);
+    if (rc != SSD_OK) return rc;
+    *path = path_of(p, &plan->dims);
+    if (tile) *tile = *path == SSD_PATH_GENERAL ? 1 : chunk_tc_tile(p);
+    return SSD_OK;
 }
 
 int ssd_varlen_status(const ssd_plan *plan, int *device_err) {
@@ -189,11 +232,13 @@ int ssd_varlen_status(const ssd_plan *plan, int *device_err) {
     if (plan->magic != kPlanMagic) return SSD_ERR_PLAN;
     const WsLayout w = layout_of(&plan->dims, plan->seg_len);
     int32_t *hdr = (int32_t *)((char *)plan->workspace + w.hdr);
-    if (cudaStreamSynchronize(plan->stream) != cudaSuccess) return SSD_ERR_CUDA;
+    // Only the plan's stream is synchronised (its work, then the read and the
+    // clear, in stream order); other streams of the device keep running.
     int v = 0;
-    if (cudaMemcpy(&v, hdr + kHdrErr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
-    if (cudaMemset(hdr + kHdrErr, 0, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, hdr + kHdrErr, sizeof(int), cudaMemcpyDeviceToHost, plan->stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (cudaMemsetAsync(hdr + kHdrErr, 0, sizeof(int), plan->stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(plan->stream) != cudaSuccess) return SSD_ERR_CUDA;
     *device_err = v;
     return SSD_OK;
 }

@@ -58,13 +58,16 @@
 
 #include <algorithm>
 #include <cstddef>
+#include <mutex>
 
 #include "sm100.cuh"
 #include "ssd_internal.cuh"
+#include "tc_util.cuh"
 
 namespace ssd {
 namespace {
 using namespace sm100;
+using namespace tc;
 
 constexpr int kMathPerRole = 8;              // G1 and G2 warps each (two per TMEM lane quadrant)
 constexpr int kWarpBC = 2 + 2 * kMathPerRole;   // B/C loader warp
@@ -72,7 +75,6 @@ constexpr int kWarpZ = kWarpBC + 1;               // z loader warp
 constexpr int kThreads = 32 * (kWarpZ + 1);       // x/dt producer, MMA, G1, G2, B/C loader, z loader
 constexpr int kRows = 128;                   // tile rows (tokens per piece, at most)
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
-constexpr float kLog2e = 1.4426950408889634f;
 
 // Per-P layout choices.  P = 64 has room to double-buffer the x stage, the B
 // and C tiles and the y accumulators and to keep the state update S in its own
@@ -186,8 +188,6 @@ struct Pieces {
 
 extern __shared__ __align__(1024) uint8_t tc_smem[];
 
-// Phase parity of a barrier's use-th completion.
-__device__ __forceinline__ uint32_t par(uint32_t use) { return use & 1u; }
 
 // The first wait of a launch to time out leaves where it was: header word
 // kHdrTimeoutAt = 1 + the waited barrier's byte offset in shared memory, the
@@ -291,86 +291,6 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, Smem &s, const FwdParams 
     return false;
 }
 
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// 2^x on the special-function unit (flushes denormal results to zero).
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float fast_rcp(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float fast_lg2(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-// softplus(v) = ln 2 * log2(1 + 2^(v log2 e)); the identity above 20
-__device__ __forceinline__ float softplus_fast(float v) {
-    return v > 20.f ? v : 0.69314718055994531f * fast_lg2(1.f + fast_exp2(v * kLog2e));
-}
-
-// ---- packed fp32 pairs (one 64-bit register pair) for the f32x2 instructions
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-    uint64_t d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
-    return d;
-}
-__device__ __forceinline__ void f2_get(uint64_t d, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-// bf16x2 word (low half first) -> the two values as an exact fp32 pair
-__device__ __forceinline__ uint64_t f2_bf16x2(uint32_t w) {
-    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-
-// silu of a pair, v / (1 + e^-v), on the special-function unit (exp2 and an
-// approximate reciprocal, both to ~2^-22 relative).
-__device__ __forceinline__ uint64_t silu2(uint64_t z) {
-    float a, b;
-    f2_get(f2_mul(z, f2(-kLog2e, -kLog2e)), a, b);
-    const uint64_t den = f2_add(f2(fast_exp2(a), fast_exp2(b)), f2(1.f, 1.f));
-    float da, db;
-    f2_get(den, da, db);
-    return f2_mul(z, f2(fast_rcp(da), fast_rcp(db)));
-}
-
-// Pair (a, b) ~= hi + lo in bf16x2: hi is each value truncated to bf16 (its
-// upper 16 bits, exact), lo = bf16(v - hi) rounded; 16 significant bits kept.
-__device__ __forceinline__ void split_pair(uint64_t ab, uint32_t &hi, uint32_t &lo) {
-    uint32_t ua, ub;
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(ua), "=r"(ub) : "l"(ab));
-    hi = __byte_perm(ua, ub, 0x7632);
-    const uint64_t rest = f2_sub(ab, f2(__uint_as_float(ua & 0xFFFF0000u), __uint_as_float(ub & 0xFFFF0000u)));
-    float ra, rb;
-    f2_get(rest, ra, rb);
-    lo = pack_bf16x2(ra, rb);
-}
-
 // 16 columns (p0 .. p0+15) of state row n -> bf16 hi/lo copies of h^T row n.
 template <int P>
 __device__ __forceinline__ void write_h_copy16(TcSmem<P> &s, int n, int pcol0, const uint32_t (&v)[16]) {
@@ -408,6 +328,9 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     if (STATE_ONLY && blockIdx.x == 0 && threadIdx.x == 0) p.hdr[kHdrTicket] = 0;
     // The tiles need 1024-byte alignment (swizzle atoms); the dynamic shared
     // window starts there on this architecture.  Refuse to run otherwise.
+    // The state pre-pass has nothing to do for batches whose requests each fit
+    // one segment: leave before setting up barriers and TMEM.
+    if (STATE_ONLY && p.hdr[kHdrNonFinal] == 0) return;
     if ((smem_u32(tc_smem) & 1023u) != 0) {
         if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
         return;
@@ -826,7 +749,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         }
                     }
                 } else {
-                    src = p.seg_state + (size_t)(it.seg - 1) * slot_elems + head_off;
+                    src = p.seg_state + (size_t)(it.seg - 1 - it.req) * slot_elems + head_off;
                 }
             }
             // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
@@ -924,8 +847,8 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         }
                     }
                 } else if (seg_end) {
-                    dsts[nd++] = p.seg_state + (size_t)it.seg * slot_elems + head_off;
-                    if (r == 0 && hf == 0) p.seg_decay[(size_t)it.seg * p.H + hh] = fast_exp2(decay_sum2);
+                    dsts[nd++] = p.seg_state + (size_t)(it.seg - it.req) * slot_elems + head_off;
+                    if (r == 0 && hf == 0) p.seg_decay[(size_t)(it.seg - it.req) * p.H + hh] = fast_exp2(decay_sum2);
                 }
                 const bool need_copy = !STATE_ONLY && !seg_end;
                 if (Cfg::kSepS || need_copy || nd > 0) {
@@ -1121,9 +1044,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
 constexpr int kSegPassBatch = 8;
 
 template <int P>
-__global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
-    const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
-    if (p.hdr[kHdrSegs] == 0 || i >= p.R) return;
+__device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
     const int first = p.req_first_seg[i], cnt = p.req_first_seg[i + 1] - first;
     const size_t pn = (size_t)P * 128, slot_elems = (size_t)p.H * pn;
     const float *init = nullptr;
@@ -1164,7 +1085,7 @@ __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
                 sv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                 dk[j] = 0.f;
                 if (k0 + j < nk) {
-                    const size_t sg = (size_t)(first + k0 + j);
+                    const size_t sg = (size_t)(first + k0 + j - i);  // compact index
                     dk[j] = p.seg_decay[sg * p.H + hh];
                     sv[j] = *reinterpret_cast<const float4 *>(p.seg_state + sg * slot_elems + hh * pn + e);
                 }
@@ -1174,24 +1095,36 @@ __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
                 if (k0 + j < nk) {
                     h = make_float4(fmaf(dk[j], h.x, sv[j].x), fmaf(dk[j], h.y, sv[j].y), fmaf(dk[j], h.z, sv[j].z),
                                     fmaf(dk[j], h.w, sv[j].w));
-                    *reinterpret_cast<float4 *>(p.seg_state + (size_t)(first + k0 + j) * slot_elems + hh * pn + e) = h;
+                    *reinterpret_cast<float4 *>(p.seg_state + (size_t)(first + k0 + j - i) * slot_elems + hh * pn +
+                                                e) = h;
                 }
             }
         }
     }
 }
 
+// A grid of at most a few CTAs per SM strides over the (request, head) pairs.
+// Batches with no multi-segment and no empty request leave at once.
+template <int P>
+__global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
+    if (p.hdr[kHdrSegs] == 0) return;  // the plan rejected the batch
+    if (p.hdr[kHdrNonFinal] == 0 && p.hdr[kHdrEmpty] == 0) return;
+    const int64_t pairs = (int64_t)p.R * p.H;
+    for (int64_t w = blockIdx.x; w < pairs; w += gridDim.x) seg_pass_one<P>(p, (int)(w / p.H), (int)(w % p.H));
+}
+
+// The driver's tensor-map encoder, looked up once per process (thread-safe).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    std::call_once(once, [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
     return fn;
 }
 
@@ -1209,7 +1142,7 @@ bool make_map(CUtensorMap *m, const void *g, uint64_t d0, uint64_t d1, uint64_t 
 }
 
 template <int P>
-cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t stream) {
+cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, bool pair, cudaStream_t stream) {
     const int64_t seg_ctas = (int64_t)p.R * p.H;
     if (seg_ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     TcMaps maps;
@@ -1219,25 +1152,33 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t
     const int smem = (int)sizeof(TcSmem<P>);
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
-    // the shared-memory attribute is per device: set once on each device this process uses
+    // The shared-memory attribute is per device: set once on each device this
+    // process uses, under a lock (host threads may launch concurrently).
+    static std::mutex mu;
     static bool attr_done[64] = {};
-    const bool known = dev >= 0 && dev < 64;
-    if (!known || !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (known) attr_done[dev] = true;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const bool known = dev >= 0 && dev < 64;
+        if (!known || !attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<P, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
+            if (e != cudaSuccess) return e;
+            if (known) attr_done[dev] = true;
+        }
     }
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_items));
     ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    seg_pass_kernel<P><<<(unsigned)seg_ctas, 256, 0, stream>>>(p);
+    const int pass_grid = (int)std::max<int64_t>(1, std::min<int64_t>(seg_ctas, 4LL * std::max(sms, 1)));
+    seg_pass_kernel<P><<<pass_grid, 256, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    (void)pair;
     ssd_chunk_tc_kernel<P, false><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
     return cudaGetLastError();
 }
@@ -1261,7 +1202,8 @@ int chunk_tc_tile(const FwdParams &p) {
 cudaError_t launch_chunk_tc(const FwdParams &p, int64_t max_segs, cudaStream_t stream) {
     const int Qi = chunk_tc_tile(p);
     const int64_t max_items = max_segs * p.H;
-    return p.P == 64 ? launch_p<64>(p, Qi, max_items, stream) : launch_p<128>(p, Qi, max_items, stream);
+    return p.P == 64 ? launch_p<64>(p, Qi, max_items, false, stream)
+                     : launch_p<128>(p, Qi, max_items, false, stream);
 }
 
 }  // namespace ssd

@@ -17,6 +17,8 @@ constexpr int kHdrChunks = 1;    // export rows of the batch
 constexpr int kHdrSegs = 2;      // work segments of the batch
 constexpr int kHdrTicket = 3;    // next work item of the scan kernel (a ticket counter)
 constexpr int kHdrTimeoutAt = 4; // words 4-6: where the first timed-out wait of a launch was
+constexpr int kHdrNonFinal = 7;  // segments that are not the last of their request (chained states)
+constexpr int kHdrEmpty = 8;     // empty requests (final state = initial state)
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
@@ -48,8 +50,10 @@ struct FwdParams {
     const int32_t *req_first_chunk;
     const int32_t *req_first_seg;
     const Seg *segs;
-    float *seg_state;   // (max_segs, H, P, N) workspace: a segment's state (see kernels)
-    float *seg_decay;   // (max_segs, H) workspace
+    // Chained states of the segments that are not the last of their request,
+    // indexed compactly: segment k of request i (k not its last) is entry k - i.
+    float *seg_state;   // (non-final segments, H, P, N) workspace (see kernels)
+    float *seg_decay;   // (non-final segments, H) workspace
     // inputs
     const void *x, *dt, *B, *C, *z;
     const float *dt_bias, *A, *D;

@@ -54,10 +54,10 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
             int32_t Q, int32_t seg_len, int64_t max_segs, int32_t *hdr,
             int32_t *__restrict__ req_first_chunk, int32_t *__restrict__ req_first_seg,
             Seg *__restrict__ segs) {
-    __shared__ int s_err;
-    if (threadIdx.x == 0) s_err = 0;
+    __shared__ int s_err, s_empty;
+    if (threadIdx.x == 0) s_err = s_empty = 0;
     __syncthreads();
-    int err = 0;
+    int err = 0, n_empty = 0;
     int carry_c = 0, carry_s = 0;
     for (int base = 0; base < R; base += kPlanThreads) {
         const int i = base + threadIdx.x;
@@ -73,6 +73,7 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
                 ns = (int)((s + L - 1) / seg_len - s / seg_len + 1);
             } else {
                 ns = 1;  // an empty request still gets one (empty) segment: final = initial
+                ++n_empty;
             }
         }
         int ec, es, tc, ts;
@@ -90,6 +91,7 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
         req_first_seg[R] = carry_s;
     }
     if (err) atomicOr(&s_err, err);
+    if (n_empty) atomicAdd(&s_empty, n_empty);
     __syncthreads();
     const int all_err = s_err;
     const bool bad = (all_err & (SSD_DEVERR_CU_SEQLENS | SSD_DEVERR_NUM_COMPUTED)) != 0 ||
@@ -100,6 +102,9 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
         hdr[kHdrSegs] = bad ? 0 : carry_s;
         hdr[kHdrTicket] = 0;
         hdr[kHdrTimeoutAt] = hdr[kHdrTimeoutAt + 1] = hdr[kHdrTimeoutAt + 2] = 0;
+        // every request has exactly one final segment
+        hdr[kHdrNonFinal] = bad ? 0 : carry_s - R;
+        hdr[kHdrEmpty] = bad ? 0 : s_empty;
     }
     if (bad) return;  // forward kernels see zero segments and write nothing
     __syncthreads();

