@@ -173,18 +173,21 @@ int ssd_varlen_status(const ssd_plan *plan, int *device_err);
 
 /* Which kernel path ssd_varlen_forward takes for these arguments, without
  * launching anything (same validation and return codes as the forward).
- *   SSD_PATH_TENSOR_CORE: the fused chunked scan on the tensor cores (tcgen05,
- *     TMEM, TMA): bf16 with P in {64, 128} and N = 128.  *tile (nullable)
- *     receives its internal tile length in tokens: 128, or the chunk / block
- *     granularity when exports or block checkpoints need a finer cut.  The
- *     result does not depend on the tile (chunk_size only decides where
- *     exports fall: "[Bugfix] Mamba2 SSD varlen bug fix initstates decay",
- *     Purpose).
+ *   SSD_PATH_TENSOR_CORE_PAIRED: the fused chunked scan on the tensor cores
+ *     (tcgen05, TMEM, TMA) with two heads of a group per CTA sharing their B
+ *     and C tiles: bf16, P = 64, N = 128 and an even number of heads per group.
+ *   SSD_PATH_TENSOR_CORE: the same scan with one head per CTA: the other bf16
+ *     shapes with P in {64, 128} and N = 128.
+ *   For both, *tile (nullable) receives the internal tile length in tokens:
+ *     128, or the chunk / block granularity when exports or block checkpoints
+ *     need a finer cut.  The result does not depend on the tile (chunk_size
+ *     only decides where exports fall: "[Bugfix] Mamba2 SSD varlen bug fix
+ *     initstates decay", Purpose).
  *   SSD_PATH_GENERAL: a token-serial recurrence on the CUDA cores, for fp32
  *     inputs, every other bf16 shape and an all-empty batch; correct but one to
  *     two orders of magnitude slower per token than the tensor-core path.
  *     *tile receives 1. */
-enum ssd_path { SSD_PATH_TENSOR_CORE = 1, SSD_PATH_GENERAL = 2 };
+enum ssd_path { SSD_PATH_TENSOR_CORE = 1, SSD_PATH_GENERAL = 2, SSD_PATH_TENSOR_CORE_PAIRED = 3 };
 int ssd_varlen_forward_path(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out, int *path,
                             int *tile);
 

@@ -48,6 +48,8 @@ EXPORTED = ["ssd_varlen_workspace_size", "ssd_varlen_count_chunks", "ssd_varlen_
 # enum ssd_path
 PATH_TENSOR_CORE = 1
 PATH_GENERAL = 2
+PATH_TENSOR_CORE_PAIRED = 3
+PATHS_TENSOR_CORE = (PATH_TENSOR_CORE, PATH_TENSOR_CORE_PAIRED)
 # Size of the library-owned scratch array used by ssd_varlen_forward_static.
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -224,7 +226,7 @@ def ssd_varlen_status(plan: ssd_plan) -> int:
 
 def ssd_varlen_forward_path(plan: ssd_plan, inputs: ssd_inputs, outputs: ssd_outputs):
     """(path, tile): the kernel path ssd_varlen_forward takes for these arguments
-    (PATH_TENSOR_CORE or PATH_GENERAL) and its internal tile in tokens."""
+    (PATH_TENSOR_CORE_PAIRED, PATH_TENSOR_CORE or PATH_GENERAL) and its internal tile in tokens."""
     path, tile = ctypes.c_int(0), ctypes.c_int(0)
     rc = load_library().ssd_varlen_forward_path(ctypes.byref(plan), ctypes.byref(inputs),
                                                 ctypes.byref(outputs), ctypes.byref(path),

@@ -146,7 +146,8 @@ static int forward_params(const ssd_plan *plan, const ssd_inputs *in, const ssd_
 // every request) takes the general path, which needs no tensor maps over the
 // absent token buffers.
 static int path_of(const FwdParams &p, const ssd_dims *d) {
-    if (d->T > 0 && chunk_tc_supported(p, d->dtype)) return SSD_PATH_TENSOR_CORE;
+    if (d->T > 0 && chunk_tc_supported(p, d->dtype))
+        return pair_supported(p) ? SSD_PATH_TENSOR_CORE_PAIRED : SSD_PATH_TENSOR_CORE;
     return SSD_PATH_GENERAL;
 }
 

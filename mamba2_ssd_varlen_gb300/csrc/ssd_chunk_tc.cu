@@ -1178,7 +1178,7 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, bool pair, c
     seg_pass_kernel<P><<<pass_grid, 256, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    (void)pair;
+    if (pair) return launch_pair_scan(p, Qi, max_items, stream);
     ssd_chunk_tc_kernel<P, false><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
     return cudaGetLastError();
 }
@@ -1202,7 +1202,7 @@ int chunk_tc_tile(const FwdParams &p) {
 cudaError_t launch_chunk_tc(const FwdParams &p, int64_t max_segs, cudaStream_t stream) {
     const int Qi = chunk_tc_tile(p);
     const int64_t max_items = max_segs * p.H;
-    return p.P == 64 ? launch_p<64>(p, Qi, max_items, false, stream)
+    return p.P == 64 ? launch_p<64>(p, Qi, max_items, pair_supported(p), stream)
                      : launch_p<128>(p, Qi, max_items, false, stream);
 }
 

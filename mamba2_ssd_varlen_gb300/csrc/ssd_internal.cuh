@@ -93,5 +93,9 @@ cudaError_t launch_recurrent(const FwdParams &p, int dtype, cudaStream_t stream)
 bool chunk_tc_supported(const FwdParams &p, int dtype);
 int chunk_tc_tile(const FwdParams &p);
 cudaError_t launch_chunk_tc(const FwdParams &p, int64_t max_segs, cudaStream_t stream);
+// The scan with two heads of a group per CTA (P = 64, N = 128, an even number of
+// heads per group); launched by launch_chunk_tc after the segment-state passes.
+bool pair_supported(const FwdParams &p);
+cudaError_t launch_pair_scan(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t stream);
 
 }  // namespace ssd

@@ -144,7 +144,7 @@ def test_chunk_size_does_not_change_results():
                                       num_computed=[3, 0, 64])
         call, ref, _ = run_full(prob)
         path, tiles[Q] = call.path()
-        assert path == m.PATH_TENSOR_CORE
+        assert path == m.PATH_TENSOR_CORE_PAIRED
         outs[Q] = (host(call.y), host(call.final_states), host(prob["state_pool"]))
     assert tiles == {16: 16, 32: 32, 64: 64, 128: 128, 256: 128}
     for Q in (16, 32, 64, 128):
@@ -163,7 +163,7 @@ def test_tile_follows_block_size_with_a_block_table():
     prob = workloads.make_problem(spec, seed=17, device="cuda", lengths=[200, 97, 5],
                                   num_computed=[0, 95, 3], canary=-1.0)
     call, _, _ = run_full(prob)
-    assert call.path() == (m.PATH_TENSOR_CORE, 32)
+    assert call.path() == (m.PATH_TENSOR_CORE_PAIRED, 32)
 
 
 def test_every_request_crosses_a_segment_boundary():
