@@ -61,6 +61,11 @@ constexpr int kWarpProd = 0, kWarpBC = 1, kWarpMma = 2, kWarpG1 = 4, kWarpG2 = 1
 constexpr int kItemRing = 8;
 constexpr int kItemTakers = 2 + 8 + 8 + 1;  // MMA, G1, G2 warps and the B/C loader
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
+// Rows of the w x tile each G1 warp (TMEM lane quadrant 0..3) computes: the
+// quadrant q mask has one diagonal block and q blocks below it, so the lower
+// quadrants take more w x rows.
+constexpr int kWxRows0 = 48, kWxRows1 = 36, kWxRows2 = 26, kWxRows3 = 18;
+static_assert(kWxRows0 + kWxRows1 + kWxRows2 + kWxRows3 == kRows, "w x rows");
 
 __host__ __device__ constexpr uint32_t colM(int k) { return 128u * (uint32_t)k; }
 __host__ __device__ constexpr uint32_t colY(int k) { return 256u + 64u * (uint32_t)k; }
@@ -542,18 +547,26 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                 if (!wait_bar_warp(&s.x_full[k], par(pc), abort_flag, p.hdr)) { ok = false; break; }
                 const float *cs2v = s.cs2[k];
                 const float *dv = s.dtp[k];
-                const float cs2 = cs2v[r], d = dv[r], cs2_last = s.cslast[k];
+                const float cs2 = cs2v[r], cs2_last = s.cslast[k];
                 // the quadrant's reference row 32q - 1 (used below the diagonal only, q > 0)
                 const float cs2_ref = cs2v[(32 * q + 127) & 127];
                 // ---- w x (hi, lo) of row r, once the last epilogue has released
                 // the tiles (it staged y and z there, after the last state MMA)
                 if (pc > 0 && !wait_bar_warp(&s.stage_free[k], par(pc - 1), abort_flag, p.hdr)) { ok = false; break; }
                 {
-                    const float wr = (r < len) ? fast_exp2(cs2_last - cs2) * d : 0.f;
-                    const uint64_t wr2 = f2(wr, wr);
+                    // The rows are shared out unevenly -- the quadrants with fewer mask
+                    // blocks below the diagonal take more -- so that the four warps finish
+                    // w x and the mask together.  Lane l takes (row, 16-byte chunk) items
+                    // l, l + 32, ... of the warp's rows.
+                    const int row0 = q == 0 ? 0 : q == 1 ? kWxRows0 : q == 2 ? kWxRows0 + kWxRows1
+                                                                              : kWxRows0 + kWxRows1 + kWxRows2;
+                    const int nitems = 8 * (q == 0 ? kWxRows0 : q == 1 ? kWxRows1 : q == 2 ? kWxRows2 : kWxRows3);
 #pragma unroll 2
-                    for (int cb = 0; cb < 8; ++cb) {
-                        const uint32_t off = sw128_off(r, cb);
+                    for (int i = lane; i < nitems; i += 32) {
+                        const int row = row0 + (i >> 3), cb = i & 7;
+                        const float wr = row < len ? fast_exp2(cs2_last - cs2v[row]) * dv[row] : 0.f;
+                        const uint64_t wr2 = f2(wr, wr);
+                        const uint32_t off = sw128_off(row, cb);
                         const uint4 xv = *reinterpret_cast<const uint4 *>(xs + off);
                         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
                         uint32_t hi[4], lo[4];
@@ -820,14 +833,19 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                 if (!wait_bar_warp(&s.y_done[k], par(pc), abort_flag, p.hdr)) { ok = false; break; }
                 if (has_z && !wait_bar_warp(&s.z_full[k], par(pc), abort_flag, p.hdr)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll 1
-                for (int cs = 0; cs < kP; cs += 16) {
-                    uint32_t vy[16];
-                    tmem_ld16(tY + cs, vy);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int c8 = 0; c8 < 2; ++c8) {
-                        const uint32_t off = sw128_off(r, (cs >> 3) + c8);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t vy[32];
+                    tmem_ld32(tY + 32 * half, vy);
+                    tmem_ld_wait();
+                    if (half == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&s.y_empty[k]);  // Y read: the next y_inter may go
+                    }
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const uint32_t off = sw128_off(r, half * 4 + c8);
                         uint32_t zw[4] = {0u, 0u, 0u, 0u};
                         if (has_z) {
                             const uint4 zq = *reinterpret_cast<const uint4 *>(zs + off);
@@ -846,18 +864,19 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                         *reinterpret_cast<uint4 *>(ys + off) = make_uint4(out[0], out[1], out[2], out[3]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.y_empty[k]);  // Y read: the next y_inter may go
                 // coalesced copy of the quadrant's 32 rows: lane l takes 16-byte chunk
-                // l % 8 of row 32q + 4 i + l / 8
-#pragma unroll 2
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = q * 32 + i * 4 + (lane >> 3);
-                    const int ch = lane & 7;
-                    if (rr < len) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(ys + sw128_off(rr, ch));
-                        *reinterpret_cast<uint4 *>(yv + ((size_t)(t0 + rr) * p.H + hh) * kP + ch * 8) = v;
+                // l % 8 of row 32q + 4 i + l / 8 (all eight loads first, then the stores)
+                __syncwarp();
+                {
+                    uint4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = *reinterpret_cast<const uint4 *>(ys + sw128_off(q * 32 + i * 4 + (lane >> 3), lane & 7));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = q * 32 + i * 4 + (lane >> 3);
+                        if (rr < len)
+                            *reinterpret_cast<uint4 *>(yv + ((size_t)(t0 + rr) * p.H + hh) * kP + (lane & 7) * 8) = v[i];
                     }
                 }
                 // the tiles go back to G1 (and, for a later piece, to the z load)
