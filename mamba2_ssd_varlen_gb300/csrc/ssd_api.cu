@@ -34,9 +34,22 @@ static int check_dims(const ssd_dims *d) {
 
 // Tokens per work segment: long requests are cut into segments that CTAs walk
 // in parallel (the state chain between them is resolved by the forward path).
+// Batches of requests averaging at most 2048 tokens take 1024-token segments,
+// so that a batch has enough (segment, head) items to keep every SM busy to
+// the end; others 2048.
 static int32_t pick_seg_len(const ssd_dims *d) {
-    (void)d;
-    return 2048;
+    return d->T <= 2048LL * d->R ? 1024 : 2048;
+}
+
+// The longest request the chained mode takes: its segments form one serial
+// chain per head, which must not outlast the work a CTA does anyway
+// (T H / (2 SMs) tokens of one head's worth).
+static int64_t chain_max_len_of(const ssd_dims *d) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess || sms < 1)
+        sms = 1;
+    return d->T * (int64_t)d->H / (2LL * sms);
 }
 
 // Work segments of a batch, at most.  Every request has exactly one final
@@ -68,11 +81,13 @@ static WsLayout layout_of(const ssd_dims *d, int32_t seg_len) {
     w.req_first_chunk = take(sizeof(int32_t) * ((size_t)d->R + 1));
     w.req_first_seg = take(sizeof(int32_t) * ((size_t)d->R + 1));
     w.segs = take(sizeof(Seg) * (size_t)ms);
+    w.seg_order = take(sizeof(int32_t) * (size_t)ms);
     // one state (and one decay per head) for each segment that is not the last of
     // its request, indexed compactly: segment k of request i uses entry k - i
     const int64_t nf = nonfinal_segs_of(d, seg_len);
     w.seg_state = take(sizeof(float) * (size_t)nf * d->H * d->P * d->N);
     w.seg_decay = take(sizeof(float) * (size_t)nf * d->H);
+    w.seg_flags = take(sizeof(int32_t) * (size_t)nf * d->H);
     w.total = off;
     return w;
 }
@@ -124,6 +139,8 @@ static int forward_params(const ssd_plan *plan, const ssd_inputs *in, const ssd_
     p->segs = (const Seg *)(ws + w.segs);
     p->seg_state = (float *)(ws + w.seg_state);
     p->seg_decay = (float *)(ws + w.seg_decay);
+    p->seg_order = (const int32_t *)(ws + w.seg_order);
+    p->seg_flags = (int32_t *)(ws + w.seg_flags);
     p->x = in->x;
     p->dt = in->dt;
     p->B = in->B;
@@ -186,10 +203,23 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
     if (!aligned16(workspace)) return SSD_ERR_WORKSPACE;
     if (workspace_bytes < w.total) return SSD_ERR_WORKSPACE;
     char *ws = static_cast<char *>(workspace);
-    cudaError_t e = launch_plan(cu_seqlens, num_computed, dims->R, dims->T, dims->chunk_size, seg_len,
-                                max_segs_of(dims, seg_len), (int32_t *)(ws + w.hdr),
-                                (int32_t *)(ws + w.req_first_chunk), (int32_t *)(ws + w.req_first_seg),
-                                (Seg *)(ws + w.segs), stream);
+    PlanArgs a{};
+    a.cu = cu_seqlens;
+    a.ncomp = num_computed;
+    a.R = dims->R;
+    a.H = dims->H;
+    a.Q = dims->chunk_size;
+    a.seg_len = seg_len;
+    a.T = dims->T;
+    a.max_segs = max_segs_of(dims, seg_len);
+    a.chain_max_len = chain_max_len_of(dims);
+    a.hdr = (int32_t *)(ws + w.hdr);
+    a.req_first_chunk = (int32_t *)(ws + w.req_first_chunk);
+    a.req_first_seg = (int32_t *)(ws + w.req_first_seg);
+    a.segs = (Seg *)(ws + w.segs);
+    a.seg_order = (int32_t *)(ws + w.seg_order);
+    a.seg_flags = (int32_t *)(ws + w.seg_flags);
+    cudaError_t e = launch_plan(a, stream);
     if (e != cudaSuccess) return SSD_ERR_CUDA;
     memset(out, 0, sizeof(*out));
     out->dims = *dims;

@@ -154,9 +154,10 @@ struct Item {
 
 __device__ __forceinline__ bool load_item(const FwdParams &p, int w, bool state_only, Item &it) {
     const int nseg = p.hdr[kHdrSegs];
-    it.seg = w / p.H;
+    const int pos = w / p.H;
     it.head = w % p.H;
-    if (it.seg >= nseg) return false;
+    if (pos >= nseg) return false;
+    it.seg = p.seg_order[pos];
     const Seg sg = p.segs[it.seg];
     it.req = sg.req;
     it.tok = sg.tok;
@@ -205,6 +206,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     if (mbar_wait(bar, parity, kWaitNs)) return true;
     *abort_flag = 1;
     record_timeout(hdr, (int)(smem_u32(bar) - smem_u32(tc_smem)));
+    return false;
+}
+
+// A wait for the state of the previous segment (chained mode), recorded as
+// site kSiteSegState when it gives up.
+__device__ __forceinline__ bool wait_counter(const int32_t *counter, int target, volatile int *abort_flag,
+                                             int32_t *hdr) {
+    if (*abort_flag) return false;
+    if (poll_counter(counter, target, kWaitNs)) return true;
+    *abort_flag = 1;
+    record_timeout(hdr, kSiteSegState);
     return false;
 }
 
@@ -325,12 +337,17 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     using Cfg = TcCfg<P>;
     using Smem = TcSmem<P>;
     // The first kernel of a forward rewinds the scan's work ticket.
-    if (STATE_ONLY && blockIdx.x == 0 && threadIdx.x == 0) p.hdr[kHdrTicket] = 0;
+    // The first kernel of a forward rewinds the scan's work ticket and counts the
+    // forward (the chained mode's publication counters grow by one round per forward).
+    if (STATE_ONLY && blockIdx.x == 0 && threadIdx.x == 0) {
+        p.hdr[kHdrTicket] = 0;
+        p.hdr[kHdrEpoch] += 1;
+    }
     // The tiles need 1024-byte alignment (swizzle atoms); the dynamic shared
     // window starts there on this architecture.  Refuse to run otherwise.
     // The state pre-pass has nothing to do for batches whose requests each fit
     // one segment: leave before setting up barriers and TMEM.
-    if (STATE_ONLY && p.hdr[kHdrNonFinal] == 0) return;
+    if (STATE_ONLY && (p.hdr[kHdrNonFinal] == 0 || p.hdr[kHdrMode] == kModeChained)) return;
     if ((smem_u32(tc_smem) & 1023u) != 0) {
         if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
         return;
@@ -749,7 +766,16 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         }
                     }
                 } else {
-                    src = p.seg_state + (size_t)(it.seg - 1 - it.req) * slot_elems + head_off;
+                    // the state after the previous segment: chained there by seg_pass_kernel,
+                    // or (chained mode) published by the CTA that ran that segment
+                    const size_t prev = (size_t)(it.seg - 1 - it.req);
+                    if (p.hdr[kHdrMode] == kModeChained &&
+                        !__all_sync(0xffffffffu, wait_counter(p.seg_flags + prev * p.H + hh,
+                                                              kMathPerRole * p.hdr[kHdrEpoch], abort_flag, p.hdr))) {
+                        ok = false;
+                        break;
+                    }
+                    src = p.seg_state + prev * slot_elems + head_off;
                 }
             }
             // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
@@ -850,6 +876,10 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     dsts[nd++] = p.seg_state + (size_t)(it.seg - it.req) * slot_elems + head_off;
                     if (r == 0 && hf == 0) p.seg_decay[(size_t)(it.seg - it.req) * p.H + hh] = fast_exp2(decay_sum2);
                 }
+                // chained mode: the end state of a segment that is not its request's last
+                // goes to the next segment through the workspace
+                const bool publish = !STATE_ONLY && seg_end && !it.last_seg && p.hdr[kHdrMode] == kModeChained;
+                if (publish) dsts[nd++] = p.seg_state + (size_t)(it.seg - it.req) * slot_elems + head_off;
                 const bool need_copy = !STATE_ONLY && !seg_end;
                 if (Cfg::kSepS || need_copy || nd > 0) {
 #pragma unroll 1
@@ -898,6 +928,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                         if (Cfg::kSepS && has_next) mbar_arrive(&s.s_free);  // S read: next state MMA may go
                     }
                 }
+                if (publish) publish_warp(p.seg_flags + (size_t)(it.seg - it.req) * p.H + hh, lane);
                 if (STATE_ONLY) {
                     if (!Cfg::kSepY && lane == 0) mbar_arrive(&s.empty_x[st]);
                 } else {
@@ -1073,7 +1104,7 @@ __device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
         }
         return;
     }
-    if (cnt <= 1) return;
+    if (cnt <= 1 || p.hdr[kHdrMode] == kModeChained) return;  // chained mode: the scan carries the states
     const int nk = cnt - 1;
     for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
         float4 h = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1108,7 +1139,7 @@ __device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
 template <int P>
 __global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
     if (p.hdr[kHdrSegs] == 0) return;  // the plan rejected the batch
-    if (p.hdr[kHdrNonFinal] == 0 && p.hdr[kHdrEmpty] == 0) return;
+    if (p.hdr[kHdrEmpty] == 0 && (p.hdr[kHdrNonFinal] == 0 || p.hdr[kHdrMode] == kModeChained)) return;
     const int64_t pairs = (int64_t)p.R * p.H;
     for (int64_t w = blockIdx.x; w < pairs; w += gridDim.x) seg_pass_one<P>(p, (int)(w / p.H), (int)(w % p.H));
 }

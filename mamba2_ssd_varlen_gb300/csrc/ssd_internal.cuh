@@ -19,10 +19,19 @@ constexpr int kHdrTicket = 3;    // next work item of the scan kernel (a ticket 
 constexpr int kHdrTimeoutAt = 4; // words 4-6: where the first timed-out wait of a launch was
 constexpr int kHdrNonFinal = 7;  // segments that are not the last of their request (chained states)
 constexpr int kHdrEmpty = 8;     // empty requests (final state = initial state)
+constexpr int kHdrMode = 9;      // how segment states are carried (kMode*)
+constexpr int kHdrEpoch = 10;    // forwards run on this plan (bumped by each forward's first kernel)
+// kHdrMode values: chained (a segment's end state is published for the next
+// segment of its request) or pre-pass (all segment states computed first).
+constexpr int kModePrepass = 0;
+constexpr int kModeChained = 1;
+// Timeout site recorded for a wait on a previous segment's published state
+// (the other sites are barrier offsets in shared memory, all below it).
+constexpr int kSiteSegState = 0x40000;
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-    size_t hdr, req_first_chunk, req_first_seg, segs, seg_state, seg_decay, total;
+    size_t hdr, req_first_chunk, req_first_seg, segs, seg_order, seg_state, seg_decay, seg_flags, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -54,6 +63,8 @@ struct FwdParams {
     // indexed compactly: segment k of request i (k not its last) is entry k - i.
     float *seg_state;   // (non-final segments, H, P, N) workspace (see kernels)
     float *seg_decay;   // (non-final segments, H) workspace
+    const int32_t *seg_order;  // segments in the order the kernels take them
+    int32_t *seg_flags;        // (non-final segments, H): publication counters (chained mode)
     // inputs
     const void *x, *dt, *B, *C, *z;
     const float *dt_bias, *A, *D;
@@ -83,9 +94,16 @@ __device__ __forceinline__ float silu_f32(float v) { return v / (1.f + expf(-v))
 __device__ __forceinline__ void set_err(int32_t *hdr, int bits) { atomicOr(hdr + kHdrErr, bits); }
 
 // ---- launchers (defined in the .cu files) ---------------------------------
-cudaError_t launch_plan(const int32_t *cu, const int32_t *ncomp, int32_t R, int64_t T, int32_t Q,
-                        int32_t seg_len, int64_t max_segs, int32_t *hdr, int32_t *req_first_chunk,
-                        int32_t *req_first_seg, Seg *segs, cudaStream_t stream);
+struct PlanArgs {
+    const int32_t *cu, *ncomp;
+    int32_t R, H, Q, seg_len;
+    int64_t T, max_segs;
+    int64_t chain_max_len;  // longest request (tokens) the chained mode takes
+    int32_t *hdr, *req_first_chunk, *req_first_seg;
+    Seg *segs;
+    int32_t *seg_order, *seg_flags;
+};
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream);
 
 cudaError_t launch_recurrent(const FwdParams &p, int dtype, cudaStream_t stream);
 

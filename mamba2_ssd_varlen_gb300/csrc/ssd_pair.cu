@@ -107,20 +107,22 @@ struct Item {
     int tok, len;
     int64_t abs0;            // absolute position of the segment's first token
     int64_t req_s, req_end;  // request's num_computed and absolute end
-    bool first_seg;
+    bool first_seg, last_seg;
 };
 
 __device__ __forceinline__ bool load_item(const FwdParams &p, int w, Item &it) {
     const int pairs = p.H >> 1;
-    it.seg = w / pairs;
+    const int pos = w / pairs;
     it.pair = w % pairs;
-    if (it.seg >= p.hdr[kHdrSegs]) return false;
+    if (pos >= p.hdr[kHdrSegs]) return false;
+    it.seg = p.seg_order[pos];
     const Seg sg = p.segs[it.seg];
     it.req = sg.req;
     it.tok = sg.tok;
     it.len = sg.len;
     it.abs0 = sg.abs_start;
     it.first_seg = it.seg == p.req_first_seg[it.req];
+    it.last_seg = it.seg == p.req_first_seg[it.req + 1] - 1;
     it.req_s = p.num_computed ? (int64_t)p.num_computed[it.req] : 0;
     it.req_end = it.req_s + (int64_t)p.cu_seqlens[it.req + 1] - p.cu_seqlens[it.req];
     return true;
@@ -160,6 +162,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     if (mbar_wait(bar, parity, kWaitNs)) return true;
     *abort_flag = 1;
     record_timeout(hdr, (int)(smem_u32(bar) - smem_u32(pair_smem)));
+    return false;
+}
+
+// A wait for the state of the previous segment (chained mode), recorded as
+// site kSiteSegState when it gives up.
+__device__ __forceinline__ bool wait_counter(const int32_t *counter, int target, volatile int *abort_flag,
+                                             int32_t *hdr) {
+    if (*abort_flag) return false;
+    if (poll_counter(counter, target, kWaitNs)) return true;
+    *abort_flag = 1;
+    record_timeout(hdr, kSiteSegState);
     return false;
 }
 
@@ -692,7 +705,16 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                     }
                 }
             } else {
-                src = p.seg_state + (size_t)(it.seg - 1 - it.req) * slot_elems + head_off;
+                // the state after the previous segment: chained there by seg_pass_kernel,
+                // or (chained mode) published by the CTA that ran that segment
+                const size_t prev = (size_t)(it.seg - 1 - it.req);
+                if (p.hdr[kHdrMode] == kModeChained &&
+                    !__all_sync(0xffffffffu, wait_counter(p.seg_flags + prev * p.H + hh, 4 * p.hdr[kHdrEpoch],
+                                                          abort_flag, p.hdr))) {
+                    ok = false;
+                    break;
+                }
+                src = p.seg_state + prev * slot_elems + head_off;
             }
             // H in TMEM (thread r: state column n = r) and its bf16 hi/lo copy for
             // the first y_inter.  The previous item's last state MMA and y_inter
@@ -770,7 +792,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                     ++zissued;
                 }
                 const bool req_end = (ae == it.req_end);
-                float *dsts[3];
+                float *dsts[5];  // chunk export, block checkpoint, two finals (or the published state)
                 int nd = 0;
                 if (p.chunk_states && (ae % p.Q == 0 || req_end)) {
                     const int64_t row = (int64_t)p.req_first_chunk[it.req] + (ae - 1) / p.Q - it.req_s / p.Q;
@@ -803,6 +825,10 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                     }
                 }
                 for (int f = 0; f < nf; ++f) dsts[nd++] = fdst[f];
+                // chained mode: the end state of a segment that is not its request's last
+                // goes to the next segment through the workspace
+                const bool publish = !has_next && !it.last_seg && p.hdr[kHdrMode] == kModeChained;
+                if (publish) dsts[nd++] = p.seg_state + (size_t)(it.seg - it.req) * slot_elems + head_off;
                 const bool need_copy = has_next;
                 if (need_copy || nd > 0) {
 #pragma unroll 1
@@ -828,6 +854,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&s.h_copy[k]);
                 }
+                if (publish) publish_warp(p.seg_flags + (size_t)(it.seg - it.req) * p.H + hh, lane);
                 // ---- epilogue: y = Y * silu(z), staged in the w x hi tile, then
                 // stored with coalesced 16-byte writes
                 if (!wait_bar_warp(&s.y_done[k], par(pc), abort_flag, p.hdr)) { ok = false; break; }

@@ -9,6 +9,16 @@
 //     of chunk_size, so a resumed request's first chunk may be partial);
 //   * req_first_seg[i] and the segment list: runs of at most seg_len tokens,
 //     cut at absolute multiples of seg_len, that the forward kernels walk;
+//   * how the state is carried from one segment of a request to the next, and
+//     the order in which the forward kernels take the segments (seg_order):
+//       chained: the kernel that finishes a segment publishes its end state,
+//       and the next segment of the request, ordered at least one round of
+//       first segments later (the k-th segments of all requests are taken
+//       after every (k-1)-th one), picks it up -- one pass over the data;
+//       pre-pass: every segment's state from zero and its total decay are
+//       computed first and chained (ssd_chunk_tc.cu), for batches whose
+//       longest request would otherwise be a serial chain longer than the
+//       work of a CTA (a few long requests);
 //   * validation bits for the device error word.
 // One CTA of 1024 threads; no host synchronisation.
 #include "ssd_internal.cuh"
@@ -49,15 +59,34 @@ __device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, int32_t R, int64_t T,
-            int32_t Q, int32_t seg_len, int64_t max_segs, int32_t *hdr,
-            int32_t *__restrict__ req_first_chunk, int32_t *__restrict__ req_first_seg,
-            Seg *__restrict__ segs) {
-    __shared__ int s_err, s_empty;
-    if (threadIdx.x == 0) s_err = s_empty = 0;
+// Segments per request at most for the chained mode (one ordering pass each).
+constexpr int kMaxChainSegs = 16;
+
+__device__ __forceinline__ int segs_of(const int32_t *cu, const int32_t *ncomp, int i, int32_t seg_len) {
+    const int64_t L = (int64_t)cu[i + 1] - cu[i];
+    const int64_t s = ncomp ? (int64_t)ncomp[i] : 0;
+    if (L <= 0) return 1;
+    return (int)((s + L - 1) / seg_len - s / seg_len + 1);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
+    const int32_t *__restrict__ cu = a.cu;
+    const int32_t *__restrict__ ncomp = a.ncomp;
+    const int32_t R = a.R, Q = a.Q, seg_len = a.seg_len;
+    const int64_t T = a.T;
+    int32_t *hdr = a.hdr;
+    int32_t *__restrict__ req_first_chunk = a.req_first_chunk;
+    int32_t *__restrict__ req_first_seg = a.req_first_seg;
+    Seg *__restrict__ segs = a.segs;
+    __shared__ int s_err, s_empty, s_max_segs;
+    __shared__ long long s_max_len;
+    if (threadIdx.x == 0) {
+        s_err = s_empty = s_max_segs = 0;
+        s_max_len = 0;
+    }
     __syncthreads();
-    int err = 0, n_empty = 0;
+    int err = 0, n_empty = 0, my_max_segs = 0;
+    long long my_max_len = 0;
     int carry_c = 0, carry_s = 0;
     for (int base = 0; base < R; base += kPlanThreads) {
         const int i = base + threadIdx.x;
@@ -75,6 +104,8 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
                 ns = 1;  // an empty request still gets one (empty) segment: final = initial
                 ++n_empty;
             }
+            my_max_segs = max(my_max_segs, ns);
+            my_max_len = max(my_max_len, (long long)L);
         }
         int ec, es, tc, ts;
         block_scan2(nc, ns, ec, es, tc, ts);
@@ -92,10 +123,17 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
     }
     if (err) atomicOr(&s_err, err);
     if (n_empty) atomicAdd(&s_empty, n_empty);
+    if (my_max_segs) atomicMax(&s_max_segs, my_max_segs);
+    if (my_max_len) atomicMax(&s_max_len, my_max_len);
     __syncthreads();
     const int all_err = s_err;
     const bool bad = (all_err & (SSD_DEVERR_CU_SEQLENS | SSD_DEVERR_NUM_COMPUTED)) != 0 ||
-                     (int64_t)carry_s > max_segs;
+                     (int64_t)carry_s > a.max_segs;
+    // Chained when some request has more than one segment, none has more than
+    // kMaxChainSegs, and the longest request is no longer than chain_max_len
+    // tokens (its serial chain then fits the work one CTA does anyway).
+    const int maxk = s_max_segs;
+    const bool chained = !bad && maxk > 1 && maxk <= kMaxChainSegs && (int64_t)s_max_len <= a.chain_max_len;
     if (threadIdx.x == 0) {
         hdr[kHdrErr] = all_err;
         hdr[kHdrChunks] = bad ? 0 : carry_c;
@@ -105,9 +143,32 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
         // every request has exactly one final segment
         hdr[kHdrNonFinal] = bad ? 0 : carry_s - R;
         hdr[kHdrEmpty] = bad ? 0 : s_empty;
+        hdr[kHdrMode] = chained ? kModeChained : kModePrepass;
+        hdr[kHdrEpoch] = 0;
     }
     if (bad) return;  // forward kernels see zero segments and write nothing
     __syncthreads();
+    // The order the forward kernels take the segments in: chained, the k-th
+    // segments of all requests (k = 0, 1, ...), each round in request order;
+    // otherwise the segment list itself.  Chained, the per-(segment, head)
+    // publication counters start from zero.
+    if (chained) {
+        int base = 0;
+        for (int k = 0; k < maxk; ++k) {
+            for (int b0 = 0; b0 < R; b0 += kPlanThreads) {
+                const int i = b0 + threadIdx.x;
+                const int has = (i < R && segs_of(cu, ncomp, i, seg_len) > k) ? 1 : 0;
+                int e1, e2, t1, t2;
+                block_scan2(has, 0, e1, e2, t1, t2);
+                if (has) a.seg_order[base + e1] = req_first_seg[i] + k;
+                base += t1;
+            }
+        }
+        const int64_t nflags = (int64_t)(carry_s - R) * a.H;
+        for (int64_t j = threadIdx.x; j < nflags; j += kPlanThreads) a.seg_flags[j] = 0;
+    } else {
+        for (int j = threadIdx.x; j < carry_s; j += kPlanThreads) a.seg_order[j] = j;
+    }
     // Fill the segment list (one thread per request; long requests loop).
     for (int i = threadIdx.x; i < R; i += kPlanThreads) {
         const int64_t a = cu[i], L = (int64_t)cu[i + 1] - a;
@@ -128,11 +189,8 @@ plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ ncomp, i
 
 }  // namespace
 
-cudaError_t launch_plan(const int32_t *cu, const int32_t *ncomp, int32_t R, int64_t T, int32_t Q,
-                        int32_t seg_len, int64_t max_segs, int32_t *hdr, int32_t *req_first_chunk,
-                        int32_t *req_first_seg, Seg *segs, cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, ncomp, R, T, Q, seg_len, max_segs, hdr,
-                                                req_first_chunk, req_first_seg, segs);
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream) {
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -96,5 +96,31 @@ __device__ __forceinline__ void split_pair(uint64_t ab, uint32_t &hi, uint32_t &
     lo = pack_bf16x2(ra, rb);
 }
 
+// ---- segment-state hand-off between CTAs (chained mode) ---------------------
+// The CTA that finishes a segment writes its end state with plain stores, then
+// every writing warp publishes: each lane fences its stores, then lane 0 adds
+// one to the segment's counter.  A reader polls the counter with acquire loads
+// until it reaches count x epoch (counters grow by `count` per forward) or the
+// time limit passes.
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void publish_warp(int32_t *counter, int lane) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(counter, 1);
+}
+__device__ __forceinline__ bool poll_counter(const int32_t *counter, int target, uint64_t limit_ns) {
+    if (ld_acquire(counter) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire(counter) >= target) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 }  // namespace tc
 }  // namespace ssd

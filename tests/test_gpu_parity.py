@@ -106,6 +106,43 @@ def test_long_requests_span_several_segments(P):
     run_full(prob)
 
 
+HDR_MODE, MODE_PREPASS, MODE_CHAINED = 9, 0, 1  # plan header word: how segment states are carried
+
+
+def plan_mode(call):
+    return int(call.workspace[:64].view(torch.int32)[HDR_MODE].item())
+
+
+@pytest.mark.parametrize("P", [64, 128])
+def test_chained_segment_states(P):
+    # Twelve requests of 2000-2600 tokens, most crossing a 2048-token segment
+    # boundary (some from a resume offset), none long next to the batch: the
+    # plan chains the segment states through the workspace -- the CTA that ends
+    # a segment publishes its state, the one running the next segment picks it
+    # up -- with no state pre-pass.  Every output of sampled requests and heads
+    # against the oracle.
+    spec = workloads.Spec("chain", H=32, P=P, N=128, G=4, chunk_size=128, dtype="bf16", has_D=True,
+                          has_z=True, init="all", pool_slots=200, final_slots=True, export_chunks=True,
+                          block_size=256)
+    lengths = [2600, 2100, 2500, 2300, 2450, 2000, 2550, 2200, 2350, 2400, 2150, 2250]
+    ncomp = [0, 100, 1500, 0, 40, 2047, 0, 1000, 7, 0, 300, 1]
+    prob = workloads.make_problem(spec, seed=61 + P, device="cuda", lengths=lengths, num_computed=ncomp,
+                                  canary=0.75)
+    call = _sampled_check(prob, [0, 2, 5, 7, 11], [0, 13, 31])
+    assert plan_mode(call) == MODE_CHAINED
+
+
+def test_long_request_uses_the_state_pre_pass():
+    # One request far longer than the rest of the batch: chaining its segments
+    # would make it one serial chain, so the plan computes the segment states
+    # in a pre-pass instead.
+    spec = workloads.Spec("prepass", H=4, P=64, N=128, G=2, chunk_size=128, dtype="bf16", has_D=True,
+                          has_z=False, init="all", pool_slots=16, final_slots=True)
+    prob = workloads.make_problem(spec, seed=71, device="cuda", lengths=[6000, 10], num_computed=[100, 0])
+    call, _, _ = run_full(prob)
+    assert plan_mode(call) == MODE_PREPASS
+
+
 @pytest.mark.parametrize("P,Q", [(64, 64), (128, 128)])
 def test_more_items_than_sms(P, Q):
     # More (segment, head) work items than SMs, so CTAs draw several items
