@@ -39,15 +39,18 @@ def _needs(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=(), lib_path: str = LIB,
+          obj_dir: str = OBJ_DIR) -> str:
+    """Compile csrc/*.cu and link lib_path.  extra_flags (e.g. a -D for a test
+    build) go to every compile; give such a build its own lib_path and obj_dir."""
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(OBJ_DIR, os.path.basename(s) + ".o")
+        o = os.path.join(obj_dir, os.path.basename(s) + ".o")
         objs.append(o)
         if force or _needs(o, [s, *headers]):
             jobs.append((s, o))
@@ -66,14 +69,14 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
         for msg in ex.map(compile_one, jobs):
             if verbose and msg:
                 print(msg)
-    if force or jobs or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or not os.path.exists(lib_path):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -21,6 +21,7 @@ constexpr int kHdrNonFinal = 7;  // segments that are not the last of their requ
 constexpr int kHdrEmpty = 8;     // empty requests (final state = initial state)
 constexpr int kHdrMode = 9;      // how segment states are carried (kMode*)
 constexpr int kHdrEpoch = 10;    // forwards run on this plan (bumped by each forward's first kernel)
+constexpr int kHdrTestHook = 11; // zero; read only by the timeout-test build of the scan
 // kHdrMode values: chained (a segment's end state is published for the next
 // segment of its request) or pre-pass (all segment states computed first).
 constexpr int kModePrepass = 0;

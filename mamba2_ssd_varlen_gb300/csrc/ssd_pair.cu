@@ -60,7 +60,15 @@ constexpr int kThreads = 640;
 constexpr int kWarpProd = 0, kWarpBC = 1, kWarpMma = 2, kWarpG1 = 4, kWarpG2 = 12;
 constexpr int kItemRing = 8;
 constexpr int kItemTakers = 2 + 8 + 8 + 1;  // MMA, G1, G2 warps and the B/C loader
+#ifdef SSD_TIMEOUT_TEST
+// Test build only (never the library's default build): waits give up after
+// 20 ms, and when header word kHdrTestHook is set, block 0's producer publishes
+// no work item, so that block's other roles time out on the item ring before
+// any copy or MMA is issued while the other CTAs take all the work.
+constexpr uint64_t kWaitNs = 20000000ull;
+#else
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s, then abort
+#endif
 // Rows of the w x tile each G1 warp (TMEM lane quadrant 0..3) computes: the
 // quadrant q mask has one diagonal block and q blocks below it, so the lower
 // quadrants take more w x rows.
@@ -365,8 +373,15 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
             }
         };
         Ahead a0, a1, a2;
-        next_piece(a0);
-        next_piece(a1);
+#ifdef SSD_TIMEOUT_TEST
+        if (blockIdx.x == 0 && p.hdr[kHdrTestHook] != 0) {
+            a0.have = false;  // withhold every item: nothing published, nothing loaded
+        } else
+#endif
+        {
+            next_piece(a0);
+            next_piece(a1);
+        }
         uint32_t pc = 0, pub[2] = {0, 0};
         bool ok = true;
         while (ok && a0.have) {

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
         hdr[kHdrEmpty] = bad ? 0 : s_empty;
         hdr[kHdrMode] = chained ? kModeChained : kModePrepass;
         hdr[kHdrEpoch] = 0;
+        hdr[kHdrTestHook] = 0;
     }
     if (bad) return;  // forward kernels see zero segments and write nothing
     __syncthreads();
