@@ -42,9 +42,11 @@ METRIC = "SSD varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
 DECODE_METRIC = "SSD decode step tokens/s per layer (bf16, 1×GB300); % of roofline"
 CONV_METRIC = "varlen causal conv1d tokens/s per layer (bf16, 1×GB300); % of roofline"
 GDN_METRIC = "gated delta rule varlen prefill tokens/s per layer (bf16, 1×GB300); % of roofline"
-# The files the dominant (scan) kernel is compiled from; its DRAM-traffic figure in
-# profiles/traffic.txt is valid only for this exact source.
-KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
+# The files the forward's scan kernels (two heads per CTA for P = 64, one head per
+# CTA otherwise, the segment-state passes) are compiled from; a DRAM-traffic figure
+# in profiles/traffic.txt is valid only for this exact source.
+KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_pair.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu",
+                  "mamba2_ssd_varlen_gb300/csrc/tc_util.cuh", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
                   "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"]
 
 
@@ -698,6 +700,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--heads-div", type=int, default=1,
+                    help="profiling only: run the workload with H / d heads and G / d groups (at least 1), "
+                         "the same tokens and kernels, so an ncu capture of many passes stays small")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, local_rank, world = env_rank()
@@ -723,7 +728,11 @@ def main():
             dist.destroy_process_group()
         return
     peaks = load_peaks()
-    prob = workloads.make_problem(args.config, device="cuda")
+    spec = workloads.CONFIGS[args.config]
+    if args.heads_div > 1:
+        import dataclasses
+        spec = dataclasses.replace(spec, H=max(1, spec.H // args.heads_div), G=max(1, spec.G // args.heads_div))
+    prob = workloads.make_problem(spec, device="cuda")
     call = m.Call(prob)
     stream = torch.cuda.current_stream()
     n_rows, n_blocks = count_outputs(prob)
@@ -866,7 +875,7 @@ def main():
 
     khash = kernel_source_hash()
     roofline = roofline_of(cost["bytes"], cost["flops"], fwd_avg, peaks)
-    roofline.update({"traffic": read_traffic(khash, args.config), "peak_source": peaks["source"],
+    roofline.update({"traffic": read_traffic(khash, args.config + (f"/heads{args.heads_div}" if args.heads_div > 1 else "")), "peak_source": peaks["source"],
                      "algorithmic_bytes": cost["bytes"], "algorithmic_flops": cost["flops"],
                      "kernel": "ssd_varlen_forward", "kernel_ms_avg": round(fwd_avg, 5),
                      "tensor_frac_of_peak": round(cost["flops"] / (fwd_avg / 1e3) / 1e12 / peaks["bf16_tflops"], 4)})
@@ -874,8 +883,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob["dtype"] == "bf16" else "f32",
             "data": "synthetic",
-            "config": {"workload": args.config, "T": T, "R": prob["R"], "H": prob["H"],
-                       "P": prob["P"], "N": prob["N"], "G": prob["G"],
+            "config": {"workload": args.config + (f"/heads{args.heads_div}" if args.heads_div > 1 else ""),
+                       "T": T, "R": prob["R"], "H": prob["H"], "P": prob["P"], "N": prob["N"], "G": prob["G"],
                        "chunk_size": prob["chunk_size"], "global_batch": prob["R"], "seq_len": T // prob["R"],
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "l2": "inputs larger than L2 (no flush)"},
