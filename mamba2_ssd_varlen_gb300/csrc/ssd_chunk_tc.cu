@@ -1202,8 +1202,15 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, bool pair, c
     }
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_items));
-    ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
-    cudaError_t e = cudaGetLastError();
+    // the segment states from zero: one contraction per segment where supported,
+    // else this kernel's piece-by-piece state-only mode
+    cudaError_t e = cudaSuccess;
+    if (seg_state_supported(p)) {
+        e = launch_seg_state(p, max_items, stream);
+    } else {
+        ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const int pass_grid = (int)std::max<int64_t>(1, std::min<int64_t>(seg_ctas, 4LL * std::max(sms, 1)));
     seg_pass_kernel<P><<<pass_grid, 256, 0, stream>>>(p);

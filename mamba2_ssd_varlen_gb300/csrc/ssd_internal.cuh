@@ -116,5 +116,9 @@ cudaError_t launch_chunk_tc(const FwdParams &p, int64_t max_segs, cudaStream_t s
 // heads per group); launched by launch_chunk_tc after the segment-state passes.
 bool pair_supported(const FwdParams &p);
 cudaError_t launch_pair_scan(const FwdParams &p, int Qi, int64_t max_items, cudaStream_t stream);
+// The segment-state pre-pass as one contraction per segment (P = 64, N = 128);
+// launched by launch_chunk_tc first (it also rewinds the ticket and counts the forward).
+bool seg_state_supported(const FwdParams &p);
+cudaError_t launch_seg_state(const FwdParams &p, int64_t max_items, cudaStream_t stream);
 
 }  // namespace ssd
