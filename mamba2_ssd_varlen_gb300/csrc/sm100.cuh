@@ -30,6 +30,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ldmatrix, four 8x8 b16 matrices, transposed: thread 8 i + r gives the address of
+// row r of matrix i (16 bytes); thread T receives, for matrix i, the elements at
+// (row 2 (T % 4), column T / 4) and (row 2 (T % 4) + 1, column T / 4), the first in
+// the low half of d[i].
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t (&d)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(saddr)
+                 : "memory");
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -184,6 +195,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+// Shape 16x256b, two repetitions along the columns: 16 lanes from lane_base,
+// 16 columns.  Thread T holds lanes (T / 4) and (T / 4 + 8) at columns
+// 2 (T % 4) and 2 (T % 4) + 1 of each 8-column repetition: r[0], r[1] lane T/4,
+// r[2], r[3] lane T/4 + 8 for columns 0-7; r[4..7] likewise for columns 8-15.
+__device__ __forceinline__ void tmem_st16x256_x2(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
 }

@@ -245,15 +245,23 @@ __global__ void __launch_bounds__(kThreads, 1) seg_state_kernel(const FwdParams 
         }
     } else if (warp < kWarpW) {
         // ------------------------------------------------------------ A = (w o x)^T, hi | lo
-        // Thread (quadrant q, lane) owns TMEM lane 32 q + lane: head h = q / 2 of the
-        // pair, p = 32 (q % 2) + lane.  Half j of the warps takes tokens 64 j .. 64 j + 63
-        // of a piece: 16-token blocks kk = 4 j .. 4 j + 3, each 8 hi then 8 lo columns
-        // (two tokens per column, the earlier in the low half).
+        // Warp (quadrant q, half j) fills TMEM lanes 32 q .. 32 q + 31 (head h = q / 2 of
+        // the pair, p = 32 (q % 2) + lane offset) for tokens 64 j .. 64 j + 63 of a piece:
+        // per 16-token block kk, 8 hi then 8 lo columns (two tokens per column, the
+        // earlier in the low half).  Per block and 16-lane half, one transposed
+        // ldmatrix takes the x values straight into the 16x256b store fragment:
+        // matrices 0 and 1 are the tokens {0,1,4,5,8,9,12,13} and {2,3,6,7,10,11,14,15}
+        // of the block at p0 .. p0 + 7, matrices 2 and 3 the same at p0 + 8 .. p0 + 15,
+        // so thread T (g = T / 4, c = T % 4) receives the token pairs 2 c and 2 c + 1
+        // of lanes p0 + g and p0 + g + 8 -- the fragment's four registers.
         const int q = warp & 3;
         const int half = (warp - kWarpA) >> 2;
         const int hh = q >> 1;
-        const int pc_ = (q & 1) * 32 + lane;
-        const uint32_t chunk = (uint32_t)pc_ >> 3, sub = (uint32_t)(pc_ & 7) * 2;
+        const int c4 = lane & 3;
+        // this thread's ldmatrix row: matrix mi = lane / 8, row r = lane % 8
+        const int mi = lane >> 3, r8 = lane & 7;
+        const int row_tok = (r8 >> 1) * 4 + (r8 & 1) + ((mi & 1) ? 2 : 0);  // token within the block
+        const uint32_t row_chunk = (uint32_t)((q & 1) * 4 + ((mi >> 1) ? 1 : 0));  // 16-byte chunk of p0 (+ 8)
         const uint32_t tl = (uint32_t)(q * 32) << 16;
         uint32_t w = blockIdx.x, pc = 0, nitem = 0;
         Item it;
@@ -267,31 +275,25 @@ __global__ void __launch_bounds__(kThreads, 1) seg_state_kernel(const FwdParams 
                 if (!wait_bar_warp(&s.x_full[st], par(pc / kSt), abort_flag, p.hdr)) { ok = false; break; }
                 if (pc >= 2 && !wait_bar_warp(&s.a_empty[ab], par(pc / 2 - 1), abort_flag, p.hdr)) { ok = false; break; }
                 tc_fence_after();
-                const uint8_t *xs = s.x[st][hh];
+                const uint32_t xs = smem_u32(s.x[st][hh]);
                 // weights of this half's 64 tokens (zero past the segment's end)
                 const float *wv = s.w[wb][hh] + c * kRows + half * 64;
                 const uint32_t ta = tbase + tl + kColA + 128u * ab + (uint32_t)half * 64;
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk) {
-                    uint32_t hi[8], lo[8];
+                    const float4 w4 = *reinterpret_cast<const float4 *>(wv + blk * 16 + 4 * c4);
+                    const uint64_t wa = f2(w4.x, w4.y), wb2 = f2(w4.z, w4.w);
+                    const int t = half * 64 + blk * 16 + row_tok;
 #pragma unroll
-                    for (int e4 = 0; e4 < 4; ++e4) {
-                        const float4 w4 = *reinterpret_cast<const float4 *>(wv + blk * 16 + 4 * e4);
-                        const float wq[4] = {w4.x, w4.y, w4.z, w4.w};
+                    for (int sh = 0; sh < 2; ++sh) {
+                        uint32_t xv[4];
+                        ldmatrix_x4_trans(xs + (uint32_t)t * 128u + (((row_chunk + 2u * sh) ^ (uint32_t)(t & 7)) << 4), xv);
+                        uint32_t v[8];
 #pragma unroll
-                        for (int e2 = 0; e2 < 2; ++e2) {
-                            const int t = half * 64 + blk * 16 + 4 * e4 + 2 * e2;  // even token of the pair
-                            const uint32_t x0 =
-                                *reinterpret_cast<const uint16_t *>(xs + t * 128 + ((chunk ^ (uint32_t)(t & 7)) << 4) + sub);
-                            const uint32_t x1 = *reinterpret_cast<const uint16_t *>(
-                                xs + (t + 1) * 128 + ((chunk ^ (uint32_t)((t + 1) & 7)) << 4) + sub);
-                            split_pair(f2_mul(f2(__uint_as_float(x0 << 16), __uint_as_float(x1 << 16)),
-                                              f2(wq[2 * e2], wq[2 * e2 + 1])),
-                                       hi[2 * e4 + e2], lo[2 * e4 + e2]);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            split_pair(f2_mul(f2_bf16x2(xv[e]), (e & 1) ? wb2 : wa), v[e], v[4 + e]);
+                        tmem_st16x256_x2(ta + ((uint32_t)(16 * sh) << 16) + blk * 16, v);
                     }
-                    tmem_st8(ta + blk * 16, hi);
-                    tmem_st8(ta + blk * 16 + 8, lo);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -319,30 +321,45 @@ __global__ void __launch_bounds__(kThreads, 1) seg_state_kernel(const FwdParams 
         uint32_t w = blockIdx.x, nitem = 0;
         Item it, prev;
         bool ok = true;
-        // read-out of item m: D (lane 64 h + p, columns n) -> seg_state[seg - req][head][p][n]
+        // read-out of item m: D (lane 64 h + p, columns n) -> seg_state[seg - req][head][p][n].
+        // Each 32 x 32 block goes through shared memory (the item's weight buffer, free
+        // once its last MMA has completed: 1024 floats per warp, 16-byte chunks XOR-
+        // swizzled by row) so that every global store writes whole 128-byte lines.
         auto read_out = [&](const Item &pv, uint32_t m) -> bool {
             const int sb = m & 1;
             if (!wait_bar_warp(&s.s_full[sb], par(m / 2), abort_flag, p.hdr)) return false;
             tc_fence_after();
-            const int h = q >> 1, pp = (q & 1) * 32 + lane;
+            const int h = q >> 1;
             const size_t k = (size_t)(pv.seg - pv.req);
-            float *dst = p.seg_state + k * slot_elems + ((size_t)(pv.head0 + h) * kP + pp) * 128;
+            float *dst = p.seg_state + k * slot_elems + ((size_t)(pv.head0 + h) * kP + (q & 1) * 32) * 128;
             const uint32_t tS = tbase + ((uint32_t)(q * 32) << 16) + kColS + 128u * sb;
+            float *tr = &s.w[sb][0][0] + v * 1024;
+            const int rr = lane >> 3, kk = lane & 7;  // store phase: row 4 i + rr, chunk kk
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t r[32];
                 tmem_ld32(tS + cc * 32, r);
                 tmem_ld_wait();
+                if (cc == 3) {
+                    // D is free for the item two ahead
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.s_empty[sb]);
+                }
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    *reinterpret_cast<float4 *>(dst + cc * 32 + 4 * i) =
-                        make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                    __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4 *>(tr + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+                        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 4 * i + rr;
+                    const float4 val = *reinterpret_cast<const float4 *>(tr + row * 32 + ((kk ^ (row & 7)) << 2));
+                    *reinterpret_cast<float4 *>(dst + (size_t)row * 128 + cc * 32 + 4 * kk) = val;
+                }
+                __syncwarp();
             }
             if ((q & 1) == 0 && lane == 0) p.seg_decay[k * p.H + pv.head0 + h] = fast_exp2(s.cs_total[sb][h]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.s_empty[sb]);
             return true;
         };
         while (ok && next_item(p, w, n_work, it)) {
