@@ -1066,16 +1066,19 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     }
 }
 
-// Per (request, head): chains the segment end states of a long request,
+// Per (request, head, run of kSegPassChunk state elements): chains the segment
+// end states of a long request, element by element (the chains are independent),
 //   h <- initial state;  for every segment k but the last:
 //   h <- decay_k h + S_k  and store it in slot k (= entering state of segment k+1),
 // and writes an empty request's final state (its initial state).  The chain
 // loads kSegPassBatch segments' states and decays before it updates and stores
 // them, so a batch costs one memory round trip instead of one per segment.
-constexpr int kSegPassBatch = 8;
+constexpr int kSegPassBatch = 16;
+constexpr int kSegPassThreads = 256;
+constexpr int kSegPassChunk = kSegPassThreads * 4;  // one float4 per thread
 
 template <int P>
-__device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
+__device__ void seg_pass_one(const FwdParams &p, int i, int hh, int chunk) {
     const int first = p.req_first_seg[i], cnt = p.req_first_seg[i + 1] - first;
     const size_t pn = (size_t)P * 128, slot_elems = (size_t)p.H * pn;
     const float *init = nullptr;
@@ -1083,9 +1086,10 @@ __device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
         const int slot = p.init_slots[i];
         if (slot >= 0 && slot < p.num_slots) init = p.pool + (size_t)slot * slot_elems + hh * pn;
     }
+    const size_t e = (size_t)chunk * kSegPassChunk + threadIdx.x * 4;  // this thread's 4 elements
     if (p.segs[first].len == 0) {
         // An empty request: its final state is its initial state.
-        const bool reporter = threadIdx.x == 0;
+        const bool reporter = threadIdx.x == 0 && chunk == 0;
         if (reporter && p.init_slots && p.init_slots[i] >= p.num_slots) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INIT_SLOT);
         float *fd = p.final_states ? p.final_states + (size_t)i * slot_elems + hh * pn : nullptr;
         float *fs = nullptr;
@@ -1097,16 +1101,14 @@ __device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
                 fs = p.pool + (size_t)fslot * slot_elems + hh * pn;
             }
         }
-        for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
-            const float4 v = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (fd) *reinterpret_cast<float4 *>(fd + e) = v;
-            if (fs) *reinterpret_cast<float4 *>(fs + e) = v;
-        }
+        const float4 v = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (fd) *reinterpret_cast<float4 *>(fd + e) = v;
+        if (fs) *reinterpret_cast<float4 *>(fs + e) = v;
         return;
     }
     if (cnt <= 1 || p.hdr[kHdrMode] == kModeChained) return;  // chained mode: the scan carries the states
     const int nk = cnt - 1;
-    for (size_t e = threadIdx.x * 4; e < pn; e += blockDim.x * 4) {
+    {
         float4 h = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k0 = 0; k0 < nk; k0 += kSegPassBatch) {
             float4 sv[kSegPassBatch];
@@ -1137,11 +1139,15 @@ __device__ void seg_pass_one(const FwdParams &p, int i, int hh) {
 // A grid of at most a few CTAs per SM strides over the (request, head) pairs.
 // Batches with no multi-segment and no empty request leave at once.
 template <int P>
-__global__ void __launch_bounds__(256) seg_pass_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kSegPassThreads) seg_pass_kernel(const FwdParams p) {
     if (p.hdr[kHdrSegs] == 0) return;  // the plan rejected the batch
     if (p.hdr[kHdrEmpty] == 0 && (p.hdr[kHdrNonFinal] == 0 || p.hdr[kHdrMode] == kModeChained)) return;
-    const int64_t pairs = (int64_t)p.R * p.H;
-    for (int64_t w = blockIdx.x; w < pairs; w += gridDim.x) seg_pass_one<P>(p, (int)(w / p.H), (int)(w % p.H));
+    constexpr int kChunks = P * 128 / kSegPassChunk;
+    const int64_t work = (int64_t)p.R * p.H * kChunks;
+    for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
+        const int64_t rh = w / kChunks;
+        seg_pass_one<P>(p, (int)(rh / p.H), (int)(rh % p.H), (int)(w % kChunks));
+    }
 }
 
 // The driver's tensor-map encoder, looked up once per process (thread-safe).
@@ -1212,8 +1218,11 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, bool pair, c
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    const int pass_grid = (int)std::max<int64_t>(1, std::min<int64_t>(seg_ctas, 4LL * std::max(sms, 1)));
-    seg_pass_kernel<P><<<pass_grid, 256, 0, stream>>>(p);
+    constexpr int kPassChunks = P * 128 / kSegPassChunk;
+    static_assert(P * 128 % kSegPassChunk == 0, "state elements must split into whole chunks");
+    const int pass_grid =
+        (int)std::max<int64_t>(1, std::min<int64_t>(seg_ctas * kPassChunks, 8LL * std::max(sms, 1)));
+    seg_pass_kernel<P><<<pass_grid, kSegPassThreads, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (pair) return launch_pair_scan(p, Qi, max_items, stream);
