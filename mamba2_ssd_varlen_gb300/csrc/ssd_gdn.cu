@@ -622,6 +622,7 @@ extern "C" int ssd_varlen_gdn_forward(const ssd_gdn_dims *d, const int32_t *cu_s
                            io->block_table, io->device_err};
     for (const void *ptr : small)
         if (ptr && !aligned_to(ptr, 4)) return SSD_ERR_ALIGN;
+    if (gdn_tc_supported(d)) return launch_gdn_tc(d, cu_seqlens, io, stream);
     const int nvb = d->V / kBV;
     const int64_t ctas = (int64_t)d->R * d->Hv * nvb;
     if (ctas > 0x7fffffffLL) return SSD_ERR_DIMS;

@@ -1,0 +1,813 @@
+// ssd_gdn_tc.cu -- the gated delta rule (GDN) chunked prefill on the tcgen05
+// tensor cores, for key and value head dims K = V = 128 ("Automatic prefix
+// caching for GDN hybrid models (mamba_cache_mode=all) with MTP speculative
+// decoding", Purpose, Kernels/layers: the chunk kernel with intermediate-state
+// export and the block-aligned checkpoint scatter).
+//
+// The rule per value head (published gated delta rule; S a K x V matrix):
+//     S <- e^{g_t} S;  u = beta_t (v_t - S^T k_t);  S <- S + k_t u^T;  o_t = scale S^T q_t
+// with k, q optionally l2-normalised (row factors rk, rq).  Per chunk of L = 64
+// tokens from the state S0, with G the in-chunk prefix sums of g, gamma = e^G:
+//     A[s,r] = beta_s rk_s rk_r e^{G_s - G_r} k_s.k_r   (r < s)
+//     T = (I + A)^-1                                    (unit lower triangular)
+//     R = diag(beta) (V - diag(gamma rk) K S0),   U = T R
+//     O = diag(scale gamma rq) Q S0 + P U,   P[t,s] = scale rq_t rk_s e^{G_t - G_s} q_t.k_s  (s <= t)
+//     S = gamma_L S0 + K^T diag(rk e^{G_L - G}) U
+// The state-independent part of a chunk (its tiles, gates, l2 factors, A, P
+// and T) is prepared one chunk ahead of the state chain, whose products all run
+// on the tensor cores with their accumulators in TMEM:
+//     [K;Q] [K]^T -> [KK^T ; QK^T]   (M = 128: the 64 k rows over the 64 q rows)
+//     [K;Q] S0    -> [K S0 ; Q S0]   (S0 as bf16 hi + lo)
+//     U^T = R^T T^T                  (R and T as bf16 hi + lo: hi.hi + hi.lo + lo.hi)
+//     S  += K^T U'                   (U' = diag(rk e^{G_L - G}) U as hi + lo; S pre-scaled by gamma_L)
+//     O  += P U                      (onto the Q S0 rows scaled by scale gamma rq; P hi/lo in TMEM)
+// q, k, v enter exactly (bf16); every fp32 operand is split into a bf16 high part
+// and a bf16 remainder, about 16 significant bits.  T comes from A by forward
+// substitution in fp32 (one column per thread).
+//
+// One CTA per (request, value head); roles:
+//   warp 0      TMA: the K and Q tiles of each chunk (two buffers), the V tile;
+//   warp 1      MMA issuer and TMEM owner;
+//   warps 4-7   the state chain: S read-out (state outputs, S0 hi/lo, gamma_L S),
+//               R, the scaling of the Q S0 rows, U and U' hi/lo, the output rows;
+//   warps 8-11  the next chunk: gates and their prefix sums, l2 factors, A
+//               (to shared memory) and P (hi/lo in place in TMEM), then T.
+// Every wait is a bounded mbarrier wait; on a timeout the CTA records
+// SSD_DEVERR_TIMEOUT in the call's device error word, drains and exits.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstring>
+#include <mutex>
+
+#include "sm100.cuh"
+#include "ssd_internal.cuh"
+#include "tc_util.cuh"
+
+namespace ssd {
+namespace {
+using namespace sm100;
+using namespace tc;
+
+constexpr int kL = 64;    // chunk length
+constexpr int kK = 128;   // key head dim
+constexpr int kV = 128;   // value head dim
+constexpr int kThreads = 12 * 32;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpChain = 4, kWarpPrep = 8;
+constexpr int kLdA = kL + 4;  // fp32 row stride of A (float4 rows, conflict-free)
+constexpr uint64_t kWaitNs = 1000000000ull;
+// TMEM columns: S (128) | [K S0 ; Q S0] then O (128) | [KK^T ; QK^T] / P, two buffers (2 x 64) | U^T (64)
+constexpr uint32_t kColS = 0, kColKQ = 128, kColAP = 256, kColU = 384;
+
+struct GdnTcParams {
+    int64_t T;
+    int32_t R, Hk, Hv, bs, btw, num_slots, l2norm;
+    float scale;
+    const int32_t *cu;
+    ssd_gdn_io io;
+};
+
+struct GdnTcMaps {
+    CUtensorMap q, k, v;
+};
+
+// Per chunk: gate prefix sums (log2 units), write strengths, l2 factors (zero past the chunk's tokens).
+struct GdnVec {
+    float gl2[kL], beta[kL], rk[kL], rq[kL];
+};
+
+struct __align__(1024) GdnTcSmem {
+    uint8_t kq[2][32768];  // per chunk: k-half h at h*16384: 64 K rows (8 KB) then 64 Q rows (8 KB)
+    uint8_t s0[65536];     // S0 hi | lo [v-half][128 k rows][64 v]; then U' hi | lo [128 v rows][64 t]
+    uint8_t r[32768];      // R hi | lo [v-half][64 t rows][64 v]; then U hi | lo [128 v rows][64 s]
+    uint8_t v[16384];      // V tile [v-half][64 t rows][64 v]
+    uint8_t t[16384];      // T^T hi | lo [64 s rows][64 t]
+    float a[kL * kLdA];    // A, fp32
+    GdnVec vec[2];
+    uint64_t kq_full[2], kq_empty[2], ap_full[2], p_ready[2], vec_ready[2], vec_free[2];
+    uint64_t v_full, v_empty, a_ready, t_ready, t_free, s0_copy, kqs0_full, r_ready, o_scaled, u_full, u_copy,
+        s_ready, o_full, o_free, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(GdnTcSmem) <= 232448, "GDN tiles exceed the shared-memory limit");
+
+extern __shared__ __align__(1024) uint8_t gdn_tc_smem[];
+
+__device__ __noinline__ void gdn_record_timeout(int32_t *err) { atomicOr(err, SSD_DEVERR_TIMEOUT); }
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, kWaitNs)) return true;
+    *abort_flag = 1;
+    gdn_record_timeout(err);
+    return false;
+}
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *err) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err));
+}
+
+// The chunks of a request: cut at absolute multiples of kL (positions from s0).
+struct Chunks {
+    int64_t a, len, s0, pos;
+    __device__ __forceinline__ bool next(int64_t &t0, int &n, int64_t &abs_end) {
+        if (pos >= len) return false;
+        const int64_t abs0 = s0 + pos;
+        n = (int)min((abs0 / kL + 1) * kL - abs0, len - pos);
+        t0 = a + pos;
+        abs_end = abs0 + n;
+        pos += n;
+        return true;
+    }
+};
+
+// Where the state after a chunk ending at absolute position abs_end goes (export
+// row, block checkpoint), or the final destinations; at most four.
+struct Dests {
+    float *d[4];
+    int n;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_constant__ GdnTcParams p,
+                                                             const __grid_constant__ GdnTcMaps maps) {
+    const ssd_gdn_io &io = p.io;
+    int32_t *err = io.device_err;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i = (int)(blockIdx.x / p.Hv), hv = (int)(blockIdx.x % p.Hv);
+    const int kh = hv / (p.Hv / p.Hk);
+    const size_t state_elems = (size_t)kK * kV;
+
+    if (blockIdx.x == 0 && tid == 0 && (p.cu[0] != 0 || (int64_t)p.cu[p.R] != p.T)) atomicOr(err, SSD_DEVERR_CU_SEQLENS);
+    const int64_t a = p.cu[i], b = p.cu[i + 1];
+    if (a < 0 || b < a || b > p.T) {
+        if (tid == 0) atomicOr(err, SSD_DEVERR_CU_SEQLENS);
+        return;
+    }
+    int64_t s0 = io.num_computed ? io.num_computed[i] : 0;
+    if (s0 < 0 || s0 + (b - a) > 0x7fffffffLL) {
+        if (tid == 0) atomicOr(err, SSD_DEVERR_NUM_COMPUTED);
+        s0 = 0;
+    }
+    const float *init = nullptr;
+    if (io.init_slots && io.state_pool) {
+        const int sl = io.init_slots[i];
+        if (sl >= p.num_slots) {
+            if (tid == 0) atomicOr(err, SSD_DEVERR_INIT_SLOT);
+        } else if (sl >= 0) {
+            init = io.state_pool + ((size_t)sl * p.Hv + hv) * state_elems;
+        }
+    }
+    // final destinations (every CTA of the request checks the slot; thread 0 reports)
+    Dests fin{{nullptr, nullptr, nullptr, nullptr}, 0};
+    if (io.final_states) fin.d[fin.n++] = io.final_states + ((size_t)i * p.Hv + hv) * state_elems;
+    if (io.final_slots && io.state_pool) {
+        const int fs = io.final_slots[i];
+        if (fs >= p.num_slots) {
+            if (tid == 0) atomicOr(err, SSD_DEVERR_FINAL_SLOT);
+        } else if (fs >= 0) {
+            fin.d[fin.n++] = io.state_pool + ((size_t)fs * p.Hv + hv) * state_elems;
+        }
+    }
+    if (b == a) {
+        // An empty request: its final state is its initial state.
+        for (size_t e = (size_t)tid * 4; e < state_elems; e += kThreads * 4) {
+            const float4 val = init ? *reinterpret_cast<const float4 *>(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int f = 0; f < fin.n; ++f) *reinterpret_cast<float4 *>(fin.d[f] + e) = val;
+        }
+        return;
+    }
+    const int nch = (int)((s0 + (b - a) - 1) / kL - s0 / kL + 1);
+
+    if ((smem_u32(gdn_tc_smem) & 1023u) != 0) {
+        if (tid == 0) atomicOr(err, SSD_DEVERR_INTERNAL);
+        return;
+    }
+    GdnTcSmem &s = *reinterpret_cast<GdnTcSmem *>(gdn_tc_smem);
+    volatile int *abort_flag = &s.abort_flag;
+    if (tid == 0) {
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&s.kq_full[k], 1);
+            mbar_init(&s.kq_empty[k], 1);
+            mbar_init(&s.ap_full[k], 1);
+            mbar_init(&s.p_ready[k], 4);
+            mbar_init(&s.vec_ready[k], 4);
+            mbar_init(&s.vec_free[k], 4);
+        }
+        mbar_init(&s.v_full, 1);
+        mbar_init(&s.v_empty, 2);
+        mbar_init(&s.a_ready, 2);
+        mbar_init(&s.t_ready, 2);
+        mbar_init(&s.t_free, 1);
+        mbar_init(&s.s0_copy, 4);
+        mbar_init(&s.kqs0_full, 1);
+        mbar_init(&s.r_ready, 2);
+        mbar_init(&s.o_scaled, 2);
+        mbar_init(&s.u_full, 1);
+        mbar_init(&s.u_copy, 4);
+        mbar_init(&s.s_ready, 1);
+        mbar_init(&s.o_full, 1);
+        mbar_init(&s.o_free, 2);
+        mbar_init(&s.drain, 1);
+        s.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s.tmem_base;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ K, Q and V tiles
+        if (lane == 0) {
+            prefetch_tmap(&maps.q);
+            prefetch_tmap(&maps.k);
+            prefetch_tmap(&maps.v);
+            Chunks ch{a, b - a, s0, 0};
+            int64_t t0, ae;
+            int n;
+            uint32_t c = 0, nkq = 0, nv = 0;
+            bool ok = true;
+            while (ok && ch.next(t0, n, ae)) {
+                const int bb = c & 1;
+                if (c >= 2 && !wait_bar(&s.kq_empty[bb], par((c >> 1) - 1), abort_flag, err)) { ok = false; break; }
+                mbar_arrive_expect_tx(&s.kq_full[bb], 32768);
+                ++nkq;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tma_load_3d(s.kq[bb] + h * 16384, &maps.k, &s.kq_full[bb], 64 * h, kh, (int)t0);
+                    tma_load_3d(s.kq[bb] + h * 16384 + 8192, &maps.q, &s.kq_full[bb], 64 * h, kh, (int)t0);
+                }
+                if (c >= 1 && !wait_bar(&s.v_empty, par(c - 1), abort_flag, err)) { ok = false; break; }
+                mbar_arrive_expect_tx(&s.v_full, 16384);
+                ++nv;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tma_load_3d(s.v + h * 8192, &maps.v, &s.v_full, 64 * h, hv, (int)t0);
+                ++c;
+            }
+            // never leave a copy in flight
+            for (uint32_t k = nkq > 2 ? nkq - 2 : 0; k < nkq; ++k) mbar_wait(&s.kq_full[k & 1], par(k >> 1), kWaitNs);
+            if (nv > 0) mbar_wait(&s.v_full, par(nv - 1), kWaitNs);
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t i_kq = idesc_bf16_f32(128, 64, false, false);   // [K;Q] x K^T
+            constexpr uint32_t i_ks = idesc_bf16_f32(128, 128, false, true);   // [K;Q] x S0 (MN-major)
+            constexpr uint32_t i_u = idesc_bf16_f32(128, 64, true, true);      // R^T (MN) x T^T (MN)
+            constexpr uint32_t i_s = idesc_bf16_f32(128, 128, true, false);    // K^T (MN) x U' (K-major)
+            constexpr uint32_t i_o = idesc_bf16_f32(128, 128, false, false);   // P (TMEM) x U (K-major)
+            // descriptors built once; + offset / 16 addresses further into a tile
+            uint64_t dKQ[2], dKt[2];
+            for (int bb = 0; bb < 2; ++bb) {
+                dKQ[bb] = sdesc_sw128(smem_u32(s.kq[bb]), 16, 1024);     // K-major, k-halves 16 KB apart
+                dKt[bb] = sdesc_sw128(smem_u32(s.kq[bb]), 16384, 1024);  // K^T: MN-major, k-halves 16 KB apart
+            }
+            const uint64_t dS0 = sdesc_sw128(smem_u32(s.s0), 16384, 1024);  // MN-major, v-halves 16 KB apart
+            const uint64_t dUp = sdesc_sw128(smem_u32(s.s0), 16, 1024);     // U': K-major, 128 v rows
+            const uint64_t dR = sdesc_sw128(smem_u32(s.r), 8192, 1024);     // R^T: MN-major, v-halves 8 KB apart
+            const uint64_t dU = sdesc_sw128(smem_u32(s.r), 16, 1024);       // U: K-major, 128 v rows
+            const uint64_t dT = sdesc_sw128(smem_u32(s.t), 16, 1024);       // T^T: MN-major, one 64-wide atom
+            const uint32_t tS = tbase + kColS, tKQ = tbase + kColKQ, tU = tbase + kColU;
+            bool ok = true;
+            auto issue_kq = [&](uint32_t c) -> bool {
+                const int bb = c & 1;
+                if (!wait_bar(&s.kq_full[bb], par(c >> 1), abort_flag, err)) return false;
+                tc_fence_after();
+                const uint32_t tAP = tbase + kColAP + 64u * bb;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss(tAP, dKQ[bb] + ko, dKQ[bb] + ko, i_kq, kk > 0);
+                }
+                mma_commit(&s.ap_full[bb]);
+                return true;
+            };
+            ok = issue_kq(0);
+            for (uint32_t c = 0; ok && c < (uint32_t)nch; ++c) {
+                const int bb = c & 1;
+                // [K S0 ; Q S0], once S0 hi/lo is written and the last output rows were read
+                if (!wait_bar(&s.s0_copy, par(c), abort_flag, err)) { ok = false; break; }
+                if (c >= 1 && !wait_bar(&s.o_free, par(c - 1), abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ko = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        mma_ss(tKQ, dKQ[bb] + ko, dS0 + ((uint32_t)(part * 32768 + kk * 2048) >> 4), i_ks,
+                               (part | kk) != 0);
+                    }
+                }
+                mma_commit(&s.kqs0_full);
+                // U^T = R^T T^T: hi.hi + hi.lo + lo.hi
+                if (!wait_bar(&s.r_ready, par(c), abort_flag, err)) { ok = false; break; }
+                if (!wait_bar(&s.t_ready, par(c), abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int pass = 0; pass < 3; ++pass) {
+                    const uint32_t ro = pass == 2 ? 16384u : 0u, to = pass == 1 ? 8192u : 0u;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tU, dR + ((ro + kk * 2048) >> 4), dT + ((to + kk * 2048) >> 4), i_u, (pass | kk) != 0);
+                }
+                mma_commit(&s.u_full);
+                mma_commit(&s.t_free);
+                // the next chunk's [KK^T ; QK^T] for its preparation
+                if (c + 1 < (uint32_t)nch && !issue_kq(c + 1)) { ok = false; break; }
+                // S += K^T U' (hi, lo), then O += P U onto the scaled Q S0 rows
+                if (!wait_bar(&s.u_copy, par(c), abort_flag, err)) { ok = false; break; }
+                if (!wait_bar(&s.p_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+                if (!wait_bar(&s.o_scaled, par(c), abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tS, dKt[bb] + ((uint32_t)(kk * 2048) >> 4),
+                               dUp + ((uint32_t)(part * 16384 + kk * 32) >> 4), i_s, 1u);
+                }
+                mma_commit(&s.s_ready);
+                const uint32_t tAP = tbase + kColAP + 64u * bb;
+#pragma unroll
+                for (int pass = 0; pass < 3; ++pass) {
+                    const uint32_t pa = pass == 2 ? 8u : 0u, uo = pass == 1 ? 16384u : 0u;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tKQ, tAP + kk * 16 + pa, dU + ((uo + kk * 32) >> 4), i_o, 1u);
+                }
+                mma_commit(&s.o_full);
+                mma_commit(&s.kq_empty[bb]);
+            }
+            mma_commit(&s.drain);
+            mbar_wait(&s.drain, 0, kWaitNs);
+        }
+    } else if (warp >= kWarpChain && warp < kWarpPrep) {
+        // ------------------------------------------------------------ the state chain
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // TMEM lane: state row k / output row / value column v
+        const uint32_t tl = (uint32_t)(q * 32) << 16;
+        const uint32_t tS = tbase + tl + kColS, tKQ = tbase + tl + kColKQ, tU = tbase + tl + kColU;
+        // export row of this request's first chunk: the chunks of the requests before it
+        int64_t fc = 0;
+        if (io.chunk_states) {
+            for (int rr = 0; rr < i; ++rr) {
+                const int64_t lr = (int64_t)p.cu[rr + 1] - p.cu[rr];
+                int64_t sr = io.num_computed ? io.num_computed[rr] : 0;
+                if (sr < 0 || sr + lr > 0x7fffffffLL) sr = 0;
+                if (lr > 0) fc += (sr + lr - 1) / kL - sr / kL + 1;
+            }
+        }
+        auto chunk_dests = [&](int j, int64_t abs_end) {
+            Dests d{{nullptr, nullptr, nullptr, nullptr}, 0};
+            if (io.chunk_states) d.d[d.n++] = io.chunk_states + ((size_t)(fc + j) * p.Hv + hv) * state_elems;
+            if (io.block_table && p.bs > 0 && abs_end % p.bs == 0) {
+                const int64_t colb = abs_end / p.bs - 1;
+                if (colb >= p.btw) {
+                    if (r == 0) atomicOr(err, SSD_DEVERR_BLOCK_TABLE);
+                } else {
+                    const int slot = io.block_table[(size_t)i * p.btw + colb];
+                    if (slot >= p.num_slots || !io.state_pool) {
+                        if (r == 0 && slot >= 0) atomicOr(err, SSD_DEVERR_BLOCK_SLOT);
+                    } else if (slot >= 0) {
+                        d.d[d.n++] = io.state_pool + ((size_t)slot * p.Hv + hv) * state_elems;
+                    }
+                }
+            }
+            return d;
+        };
+        auto store_row = [&](const Dests &d, int cc, const uint32_t (&vals)[32]) {
+            for (int f = 0; f < d.n; ++f) {
+                float *dst = d.d[f] + (size_t)r * kV + cc * 32;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<uint4 *>(dst + 4 * e) =
+                        make_uint4(vals[4 * e], vals[4 * e + 1], vals[4 * e + 2], vals[4 * e + 3]);
+            }
+        };
+        __nv_bfloat16 *__restrict__ og = static_cast<__nv_bfloat16 *>(io.o);
+        Chunks ch{a, b - a, s0, 0};
+        int64_t t0 = 0, ae = 0, prev_ae = 0;
+        int n = 0;
+        bool ok = true;
+        for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
+            const int bb = c & 1;
+            const GdnVec &vc = s.vec[bb];
+            // ---- S: state outputs of the previous chunk, S0 hi/lo, gamma_L S
+            if (c >= 1 && !wait_bar_warp(&s.s_ready, par(c - 1), abort_flag, err)) { ok = false; break; }
+            if (!wait_bar_warp(&s.vec_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            {
+                const float gL = exp2f(vc.gl2[kL - 1]);
+                const Dests d = c >= 1 ? chunk_dests((int)c - 1, prev_ae) : Dests{{nullptr, nullptr, nullptr, nullptr}, 0};
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    if (c == 0) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = init ? __float_as_uint(init[(size_t)r * kV + cc * 32 + e]) : 0u;
+                    } else {
+                        tmem_ld32(tS + cc * 32, v);
+                        tmem_ld_wait();
+                        store_row(d, cc, v);
+                    }
+                    // S0 hi/lo: row k = r, v = 32 cc .. 32 cc + 31 (v-half cc / 2, chunks 4 (cc % 2) ..)
+                    uint8_t *hb = s.s0 + (cc >> 1) * 16384, *lb = hb + 32768;
+#pragma unroll
+                    for (int ch4 = 0; ch4 < 4; ++ch4) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split_pair(f2(__uint_as_float(v[8 * ch4 + 2 * e]), __uint_as_float(v[8 * ch4 + 2 * e + 1])),
+                                       hi[e], lo[e]);
+                        const uint32_t off = sw128_off((uint32_t)r, (uint32_t)((cc & 1) * 4 + ch4));
+                        *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(lb + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * gL);
+                    tmem_st32(tS + cc * 32, v);
+                }
+                tmem_st_wait();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.s0_copy);
+            // ---- R = diag(beta) (V - diag(gamma rk) K S0); the Q S0 rows scaled by scale gamma rq
+            if (!wait_bar_warp(&s.kqs0_full, par(c), abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            if (q < 2) {
+                if (!wait_bar_warp(&s.v_full, par(c), abort_flag, err)) { ok = false; break; }
+                const int t = r;
+                const float bt = vc.beta[t], w = exp2f(vc.gl2[t]) * vc.rk[t];
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tKQ + cc * 32, v);
+                    tmem_ld_wait();
+                    const uint8_t *vt = s.v + (cc >> 1) * 8192;
+                    uint8_t *hb = s.r + (cc >> 1) * 8192, *lb = hb + 16384;
+#pragma unroll
+                    for (int ch4 = 0; ch4 < 4; ++ch4) {
+                        const uint32_t off = sw128_off((uint32_t)t, (uint32_t)((cc & 1) * 4 + ch4));
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(vt + off);
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float v0, v1;
+                            f2_get(f2_bf16x2(xw[e]), v0, v1);
+                            const float r0 = bt * (v0 - w * __uint_as_float(v[8 * ch4 + 2 * e]));
+                            const float r1 = bt * (v1 - w * __uint_as_float(v[8 * ch4 + 2 * e + 1]));
+                            split_pair(f2(r0, r1), hi[e], lo[e]);
+                        }
+                        *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(lb + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s.v_empty);
+                    mbar_arrive(&s.r_ready);
+                }
+            } else {
+                const int t = r - 64;
+                const float wq = p.scale * vc.rq[t] * exp2f(vc.gl2[t]);
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tKQ + cc * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * wq);
+                    tmem_st32(tKQ + cc * 32, v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.o_scaled);
+            }
+            // ---- U and U' = diag(rk e^{G_L - G}) U as hi/lo, row v = r: [v][s]
+            if (!wait_bar_warp(&s.u_full, par(c), abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            {
+                const float gLl = vc.gl2[kL - 1];
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tU + cc * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int ch4 = 0; ch4 < 4; ++ch4) {
+                        uint32_t hi[4], lo[4], hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int sidx = cc * 32 + 8 * ch4 + 2 * e;
+                            const float u0 = __uint_as_float(v[8 * ch4 + 2 * e]);
+                            const float u1 = __uint_as_float(v[8 * ch4 + 2 * e + 1]);
+                            split_pair(f2(u0, u1), hi[e], lo[e]);
+                            const float w0 = vc.rk[sidx] * exp2f(fminf(gLl - vc.gl2[sidx], 0.f));
+                            const float w1 = vc.rk[sidx + 1] * exp2f(fminf(gLl - vc.gl2[sidx + 1], 0.f));
+                            split_pair(f2(w0 * u0, w1 * u1), hw[e], lw[e]);
+                        }
+                        const uint32_t off = sw128_off((uint32_t)r, (uint32_t)(cc * 4 + ch4));
+                        *reinterpret_cast<uint4 *>(s.r + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(s.r + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        *reinterpret_cast<uint4 *>(s.s0 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4 *>(s.s0 + 16384 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.u_copy);
+            // ---- output rows: O (rows 64..127 of the [K S0 ; Q S0] accumulator) -> bf16
+            if (q >= 2) {
+                if (!wait_bar_warp(&s.o_full, par(c), abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                const int t = r - 64;
+                __nv_bfloat16 *orow = og + ((size_t)(t0 + t) * p.Hv + hv) * kV;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tKQ + cc * 32, v);
+                    tmem_ld_wait();
+                    if (t < n) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                pk[j] = pack_bf16x2(__uint_as_float(v[8 * e + 2 * j]), __uint_as_float(v[8 * e + 2 * j + 1]));
+                            *reinterpret_cast<uint4 *>(orow + cc * 32 + 8 * e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.o_free);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.vec_free[bb]);
+            prev_ae = ae;
+        }
+        // ---- the state after the last chunk: its outputs and the final states
+        if (ok && wait_bar_warp(&s.s_ready, par((uint32_t)nch - 1), abort_flag, err)) {
+            tc_fence_after();
+            const Dests d = chunk_dests(nch - 1, prev_ae);
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tS + cc * 32, v);
+                tmem_ld_wait();
+                store_row(d, cc, v);
+                store_row(fin, cc, v);
+            }
+        }
+    } else if (warp >= kWarpPrep) {
+        // ------------------------------------------------------------ the next chunk's A, P and T
+        const int q = warp & 3;
+        const uint32_t tl = (uint32_t)(q * 32) << 16;
+        const float *__restrict__ gg = io.g;
+        const float *__restrict__ gb = io.beta;
+        Chunks ch{a, b - a, s0, 0};
+        int64_t t0, ae;
+        int n;
+        bool ok = true;
+        for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
+            const int bb = c & 1;
+            GdnVec &vc = s.vec[bb];
+            if (c >= 2 && !wait_bar_warp(&s.vec_free[bb], par((c >> 1) - 1), abort_flag, err)) { ok = false; break; }
+            if (!wait_bar_warp(&s.kq_full[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            // gates: inclusive prefix sums of g log2(e) over the chunk (zero past its tokens)
+            if (q == 0) {
+                const int tA = 2 * lane, tB = 2 * lane + 1;
+                const float x0 = tA < n ? gg[(size_t)(t0 + tA) * p.Hv + hv] * kLog2e : 0.f;
+                const float x1 = tB < n ? gg[(size_t)(t0 + tB) * p.Hv + hv] * kLog2e : 0.f;
+                vc.beta[tA] = tA < n ? gb[(size_t)(t0 + tA) * p.Hv + hv] : 0.f;
+                vc.beta[tB] = tB < n ? gb[(size_t)(t0 + tB) * p.Hv + hv] : 0.f;
+                float incl = x0 + x1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const float excl = incl - (x0 + x1);
+                vc.gl2[tA] = excl + x0;
+                vc.gl2[tB] = incl;
+            }
+            // l2 factors: warps q = 0, 1 the k rows 32 q + lane, q = 2, 3 the q rows 32 (q - 2) + lane
+            {
+                const int t = (q & 1) * 32 + lane;
+                float f = 0.f;
+                if (t < n) {
+                    f = 1.f;
+                    if (p.l2norm) {
+                        float ss = 0.f;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint8_t *row = s.kq[bb] + h * 16384 + (q >= 2 ? 8192 : 0) + t * 128;
+#pragma unroll
+                            for (int c16 = 0; c16 < 8; ++c16) {
+                                const uint4 raw = *reinterpret_cast<const uint4 *>(row + c16 * 16);
+                                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float lo = bf16lo_to_f32(w4[e]), hi = bf16hi_to_f32(w4[e]);
+                                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                                }
+                            }
+                        }
+                        f = rsqrtf(ss + 1e-6f);
+                    }
+                }
+                if (q < 2) vc.rk[t] = f;
+                else vc.rq[t] = f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.vec_ready[bb]);
+            if (!wait_bar_warp(&s.vec_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            // ---- A rows (to shared memory) and P rows (hi/lo in place in TMEM)
+            if (!wait_bar_warp(&s.ap_full[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t tAP = tbase + tl + kColAP + 64u * bb;
+            if (q < 2) {
+                const int sr = q * 32 + lane;
+                const float ws = vc.beta[sr] * vc.rk[sr], gs = vc.gl2[sr];
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tAP + cc * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        float av[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int rc = cc * 32 + 4 * e4 + e;
+                            av[e] = rc < sr ? ws * vc.rk[rc] * exp2f(fminf(gs - vc.gl2[rc], 0.f)) * __uint_as_float(v[4 * e4 + e])
+                                            : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(s.a + sr * kLdA + cc * 32 + 4 * e4) = make_float4(av[0], av[1], av[2], av[3]);
+                    }
+                }
+            } else {
+                const int t = (q - 2) * 32 + lane;
+                const float wt = p.scale * vc.rq[t], gt = vc.gl2[t];
+                uint32_t v[2][32];
+                tmem_ld32(tAP, v[0]);
+                tmem_ld32(tAP + 32, v[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s0i = kk * 16 + 2 * e;
+                        const float q0 = __uint_as_float(v[kk >> 1][(kk & 1) * 16 + 2 * e]);
+                        const float q1 = __uint_as_float(v[kk >> 1][(kk & 1) * 16 + 2 * e + 1]);
+                        const float p0 = s0i <= t ? wt * vc.rk[s0i] * exp2f(fminf(gt - vc.gl2[s0i], 0.f)) * q0 : 0.f;
+                        const float p1 = s0i + 1 <= t ? wt * vc.rk[s0i + 1] * exp2f(fminf(gt - vc.gl2[s0i + 1], 0.f)) * q1 : 0.f;
+                        split_pair(f2(p0, p1), hi[e], lo[e]);
+                    }
+                    tmem_st8(tAP + kk * 16, hi);
+                    tmem_st8(tAP + kk * 16 + 8, lo);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.p_ready[bb]);
+            if (q >= 2) continue;
+            // ---- T = (I + A)^-1 by forward substitution, column j per thread; written
+            // as T^T (row j = column j of T) hi/lo, once the last U product has read T
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.a_ready);
+            if (!wait_bar_warp(&s.a_ready, par(c), abort_flag, err)) { ok = false; break; }
+            const int j = q * 32 + lane;
+            float x[kL];
+#pragma unroll
+            for (int rr = 0; rr < kL; ++rr) x[rr] = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < kL; ++rr) {
+                float acc0 = 0.f, acc1 = 0.f;
+                const float *arow = s.a + rr * kLdA;
+#pragma unroll
+                for (int cc = 0; cc < rr; cc += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + cc);
+                    acc0 = fmaf(a4.x, x[cc], acc0);
+                    acc1 = fmaf(a4.y, x[cc + 1], acc1);
+                    acc0 = fmaf(a4.z, x[cc + 2], acc0);
+                    acc1 = fmaf(a4.w, x[cc + 3], acc1);
+                }
+                x[rr] = rr == j ? 1.f : (rr < j ? 0.f : -(acc0 + acc1));
+            }
+            if (c >= 1 && !wait_bar_warp(&s.t_free, par(c - 1), abort_flag, err)) { ok = false; break; }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split_pair(f2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1]), hi[e], lo[e]);
+                const uint32_t off = sw128_off((uint32_t)j, (uint32_t)c8);
+                *reinterpret_cast<uint4 *>(s.t + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(s.t + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.t_ready);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 gdn_encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D bf16 map over a row-major (d2, d1, d0 = 128) tensor; box = 64 x 1 x 64 rows, 128-byte swizzle.
+bool gdn_map(CUtensorMap *m, const void *g, uint64_t d1, uint64_t d2) {
+    auto fn = gdn_encode_fn();
+    if (!fn) return false;
+    const uint64_t dims[3] = {128, d1, d2 > 0 ? d2 : 1};
+    const uint64_t strides[2] = {128 * 2, 128 * d1 * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)kL};
+    const uint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(g), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gdn_tc_supported(const ssd_gdn_dims *d) {
+    return d->dtype == SSD_DTYPE_BF16 && d->K == kK && d->V == kV && d->chunk_size == kL;
+}
+
+// The tcgen05 GDN prefill: one CTA per (request, value head).  The caller has
+// validated the arguments (dims, pointers, alignment, slot tables).
+int launch_gdn_tc(const ssd_gdn_dims *d, const int32_t *cu_seqlens, const ssd_gdn_io *io, cudaStream_t stream) {
+    GdnTcParams p{};
+    p.T = d->T;
+    p.R = d->R;
+    p.Hk = d->Hk;
+    p.Hv = d->Hv;
+    p.bs = io->block_table ? d->block_size : 0;
+    p.btw = d->block_table_width;
+    p.num_slots = d->num_slots;
+    p.l2norm = d->l2norm ? 1 : 0;
+    p.scale = d->scale != 0.f ? d->scale : 1.f / sqrtf((float)d->K);
+    p.cu = cu_seqlens;
+    p.io = *io;
+    // with no tokens (every request empty) no tile is loaded and the maps stay zero
+    GdnTcMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (d->T > 0 && (!gdn_map(&maps.q, io->q, d->Hk, (uint64_t)d->T) || !gdn_map(&maps.k, io->k, d->Hk, (uint64_t)d->T) ||
+                     !gdn_map(&maps.v, io->v, d->Hv, (uint64_t)d->T)))
+        return SSD_ERR_CUDA;
+    const int smem = (int)sizeof(GdnTcSmem);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const bool known = dev >= 0 && dev < 64;
+        if (!known || !attr_done[dev]) {
+            if (cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return SSD_ERR_CUDA;
+            if (known) attr_done[dev] = true;
+        }
+    }
+    const int64_t ctas = (int64_t)d->R * d->Hv;
+    if (ctas > 0x7fffffffLL) return SSD_ERR_DIMS;
+    gdn_tc_kernel<<<(unsigned)ctas, kThreads, smem, stream>>>(p, maps);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace ssd

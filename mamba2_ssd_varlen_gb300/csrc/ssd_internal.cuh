@@ -120,5 +120,9 @@ cudaError_t launch_pair_scan(const FwdParams &p, int Qi, int64_t max_items, cuda
 // launched by launch_chunk_tc first (it also rewinds the ticket and counts the forward).
 bool seg_state_supported(const FwdParams &p);
 cudaError_t launch_seg_state(const FwdParams &p, int64_t max_items, cudaStream_t stream);
+// The gated delta rule prefill on the tcgen05 tensor cores (bf16, K = V = 128,
+// 64-token chunks); ssd_varlen_gdn_forward validates the call, then launches it.
+bool gdn_tc_supported(const ssd_gdn_dims *d);
+int launch_gdn_tc(const ssd_gdn_dims *d, const int32_t *cu_seqlens, const ssd_gdn_io *io, cudaStream_t stream);
 
 }  // namespace ssd

@@ -69,10 +69,17 @@ def test_small_config_every_output():
     run_full(workloads.make_gdn_problem("gdn_small", device="cuda", canary=-3.0))
 
 
-def test_resumed_requests_partial_first_chunks():
+# V = 128 runs the tcgen05 kernel (K = V = 128), other widths the mma.sync kernel.
+@pytest.mark.parametrize("V", [64, 128])
+def test_every_output_both_kernels(V):
+    run_full(workloads.make_gdn_problem(_spec(V=V), seed=30 + V, device="cuda", canary=-3.0))
+
+
+@pytest.mark.parametrize("V", [64, 128])
+def test_resumed_requests_partial_first_chunks(V):
     # num_computed not a multiple of the chunk: partial first chunks, block
     # boundaries at absolute positions, export rows per absolute chunk
-    prob = workloads.make_gdn_problem(_spec(), seed=5, device="cuda", num_computed=[3, 64, 0, 100, 5, 70],
+    prob = workloads.make_gdn_problem(_spec(V=V), seed=5, device="cuda", num_computed=[3, 64, 0, 100, 5, 70],
                                       canary=2.0)
     run_full(prob)
 
@@ -83,8 +90,9 @@ def test_head_shapes(V, Hk, Hv):
     run_full(workloads.make_gdn_problem(spec, seed=V + Hk, device="cuda", canary=1.5))
 
 
-def test_without_l2norm_and_explicit_scale():
-    spec = _spec(l2norm=False, lengths=[90, 64, 17])
+@pytest.mark.parametrize("V", [64, 128])
+def test_without_l2norm_and_explicit_scale(V):
+    spec = _spec(V=V, l2norm=False, lengths=[90, 64, 17])
     prob = workloads.make_gdn_problem(spec, seed=8, device="cuda", canary=0.5)
     prob["q"] = (prob["q"].float() / 12.0).to(torch.bfloat16)   # keep the un-normalised rule stable
     prob["k"] = (prob["k"].float() / 12.0).to(torch.bfloat16)
@@ -92,15 +100,17 @@ def test_without_l2norm_and_explicit_scale():
     run_full(prob)
 
 
-def test_long_request_many_chunks():
-    spec = _spec(lengths=[1500, 300], block_size=256)
+@pytest.mark.parametrize("V", [64, 128])
+def test_long_request_many_chunks(V):
+    spec = _spec(V=V, lengths=[1500, 300], block_size=256)
     run_full(workloads.make_gdn_problem(spec, seed=9, device="cuda", canary=-1.0))
 
 
+@pytest.mark.parametrize("V", [64, 128])
 @pytest.mark.parametrize("k", [1, 63, 64, 100])
-def test_split_state_resume(k):
+def test_split_state_resume(k, V):
     L = 333
-    spec = _spec(lengths=[L], export_chunks=False, block_size=0, final_slots=True)
+    spec = _spec(V=V, lengths=[L], export_chunks=False, block_size=0, final_slots=True)
     prob = workloads.make_gdn_problem(spec, seed=12, device="cuda")
     ref = gdn_forward(workloads.to_oracle_gdn(prob))
     first = dict(prob)
@@ -123,8 +133,9 @@ def test_split_state_resume(k):
     assert_close(host(c2.final_states), ref["final_states"], "split final")
 
 
-def test_device_error_bits_and_skipped_writes():
-    spec = _spec(lengths=[20, 70, 9], export_chunks=False, block_size=64)
+@pytest.mark.parametrize("V", [64, 128])
+def test_device_error_bits_and_skipped_writes(V):
+    spec = _spec(V=V, lengths=[20, 70, 9], export_chunks=False, block_size=64)
     prob = workloads.make_gdn_problem(spec, seed=13, device="cuda", canary=4.0)
     S = prob["state_pool"].shape[0]
     prob["init_slots"][1] = S + 2      # read as zeros
@@ -160,10 +171,11 @@ def test_full_uniform_8x2048_sampled():
     assert_close(host(call.final_states[reqs].index_select(1, hidx)), ref["final_states"], "final_states")
 
 
-def test_all_requests_empty():
+@pytest.mark.parametrize("V", [64, 128])
+def test_all_requests_empty(V):
     # T = 0: no chunk runs; every request's final state is its initial state
     # (zeros where the read slot is -1), in the dense output and the final slots.
-    spec = _spec(lengths=[0, 0, 0], export_chunks=False, block_size=0)
+    spec = _spec(V=V, lengths=[0, 0, 0], export_chunks=False, block_size=0)
     prob = workloads.make_gdn_problem(spec, seed=21, device="cuda", canary=0.75)
     prob["init_slots"][1] = -1
     run_full(prob)
