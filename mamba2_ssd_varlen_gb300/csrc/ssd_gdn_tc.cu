@@ -31,7 +31,8 @@
 //   warps 4-7   the state chain: S read-out (state outputs, S0 hi/lo, gamma_L S),
 //               R, the scaling of the Q S0 rows, U and U' hi/lo, the output rows;
 //   warps 8-11  the next chunk: gates and their prefix sums, l2 factors, A
-//               (to shared memory) and P (hi/lo in place in TMEM), then T.
+//               (to shared memory) and P (hi/lo in place in TMEM), then T by a
+//               right-looking substitution (independent updates of the later rows).
 // Every wait is a bounded mbarrier wait; on a timeout the CTA records
 // SSD_DEVERR_TIMEOUT in the call's device error word, drains and exits.
 #include <cudaTypedefs.h>
@@ -72,9 +73,13 @@ struct GdnTcMaps {
     CUtensorMap q, k, v;
 };
 
-// Per chunk: gate prefix sums (log2 units), write strengths, l2 factors (zero past the chunk's tokens).
+// Per chunk: gate prefix sums (log2 units), write strengths, l2 factors (zero past the
+// chunk's tokens), and what the state chain takes from them: gamma rk (R), scale gamma
+// rq (the Q S0 rows), rk e^{G_L - G} (U') and gamma_L.
 struct GdnVec {
     float gl2[kL], beta[kL], rk[kL], rq[kL];
+    float grk[kL], osc[kL], wu[kL];
+    float gL, pad[3];
 };
 
 struct __align__(1024) GdnTcSmem {
@@ -83,9 +88,9 @@ struct __align__(1024) GdnTcSmem {
     uint8_t r[32768];      // R hi | lo [v-half][64 t rows][64 v]; then U hi | lo [128 v rows][64 s]
     uint8_t v[16384];      // V tile [v-half][64 t rows][64 v]
     uint8_t t[16384];      // T^T hi | lo [64 s rows][64 t]
-    float a[kL * kLdA];    // A, fp32
+    float a[kL * kLdA];    // A^T (row c = column c of A), fp32
     GdnVec vec[2];
-    uint64_t kq_full[2], kq_empty[2], ap_full[2], p_ready[2], vec_ready[2], vec_free[2];
+    uint64_t kq_full[2], kq_empty[2], ap_full[2], p_ready[2], vec_ready[2], vec2_ready[2], vec_free[2];
     uint64_t v_full, v_empty, a_ready, t_ready, t_free, s0_copy, kqs0_full, r_ready, o_scaled, u_full, u_copy,
         s_ready, o_full, o_free, drain;
     uint32_t tmem_base;
@@ -193,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             mbar_init(&s.ap_full[k], 1);
             mbar_init(&s.p_ready[k], 4);
             mbar_init(&s.vec_ready[k], 4);
+            mbar_init(&s.vec2_ready[k], 4);
             mbar_init(&s.vec_free[k], 4);
         }
         mbar_init(&s.v_full, 1);
@@ -398,65 +404,92 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
             const int bb = c & 1;
             const GdnVec &vc = s.vec[bb];
-            // ---- S: state outputs of the previous chunk, S0 hi/lo, gamma_L S
+            // ---- S: state outputs of the previous chunk and S0 hi/lo (for the K S0 / Q S0
+            // product, published first), then gamma_L S in place (before the state product)
             if (c >= 1 && !wait_bar_warp(&s.s_ready, par(c - 1), abort_flag, err)) { ok = false; break; }
-            if (!wait_bar_warp(&s.vec_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            if (!wait_bar_warp(&s.vec2_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             {
-                const float gL = exp2f(vc.gl2[kL - 1]);
                 const Dests d = c >= 1 ? chunk_dests((int)c - 1, prev_ae) : Dests{{nullptr, nullptr, nullptr, nullptr}, 0};
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[2][32];
                     if (c == 0) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = init ? __float_as_uint(init[(size_t)r * kV + cc * 32 + e]) : 0u;
-                    } else {
-                        tmem_ld32(tS + cc * 32, v);
-                        tmem_ld_wait();
-                        store_row(d, cc, v);
-                    }
-                    // S0 hi/lo: row k = r, v = 32 cc .. 32 cc + 31 (v-half cc / 2, chunks 4 (cc % 2) ..)
-                    uint8_t *hb = s.s0 + (cc >> 1) * 16384, *lb = hb + 32768;
+                        for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int ch4 = 0; ch4 < 4; ++ch4) {
+                            for (int e = 0; e < 32; ++e)
+                                v[h][e] = init ? __float_as_uint(init[(size_t)r * kV + c2 * 64 + h * 32 + e]) : 0u;
+                    } else {
+                        tmem_ld32(tS + c2 * 64, v[0]);
+                        tmem_ld32(tS + c2 * 64 + 32, v[1]);
+                        tmem_ld_wait();
+                        store_row(d, 2 * c2, v[0]);
+                        store_row(d, 2 * c2 + 1, v[1]);
+                    }
+                    // S0 hi/lo: row k = r, v = 64 c2 .. 64 c2 + 63 (v-half c2)
+                    uint8_t *hb = s.s0 + c2 * 16384, *lb = hb + 32768;
+#pragma unroll
+                    for (int ch8 = 0; ch8 < 8; ++ch8) {
                         uint32_t hi[4], lo[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            split_pair(f2(__uint_as_float(v[8 * ch4 + 2 * e]), __uint_as_float(v[8 * ch4 + 2 * e + 1])),
+                            split_pair(f2(__uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e]),
+                                          __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e + 1])),
                                        hi[e], lo[e]);
-                        const uint32_t off = sw128_off((uint32_t)r, (uint32_t)((cc & 1) * 4 + ch4));
+                        const uint32_t off = sw128_off((uint32_t)r, (uint32_t)ch8);
                         *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4 *>(lb + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
+                    if (c == 0) {
+                        // the first chunk's state comes from memory: it goes to TMEM scaled here
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * gL);
-                    tmem_st32(tS + cc * 32, v);
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * vc.gL);
+                            tmem_st32(tS + c2 * 64 + h * 32, v[h]);
+                        }
+                    }
                 }
-                tmem_st_wait();
             }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.s0_copy);
+            if (c >= 1) {
+#pragma unroll 1
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tS + c2 * 64, v[0]);
+                    tmem_ld32(tS + c2 * 64 + 32, v[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * vc.gL);
+                        tmem_st32(tS + c2 * 64 + h * 32, v[h]);
+                    }
+                }
+            }
+            tmem_st_wait();
             // ---- R = diag(beta) (V - diag(gamma rk) K S0); the Q S0 rows scaled by scale gamma rq
             if (!wait_bar_warp(&s.kqs0_full, par(c), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             if (q < 2) {
                 if (!wait_bar_warp(&s.v_full, par(c), abort_flag, err)) { ok = false; break; }
                 const int t = r;
-                const float bt = vc.beta[t], w = exp2f(vc.gl2[t]) * vc.rk[t];
+                const float bt = vc.beta[t], w = vc.grk[t];
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tKQ + cc * 32, v);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tKQ + c2 * 64, v[0]);
+                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
                     tmem_ld_wait();
-                    const uint8_t *vt = s.v + (cc >> 1) * 8192;
-                    uint8_t *hb = s.r + (cc >> 1) * 8192, *lb = hb + 16384;
+                    const uint8_t *vt = s.v + c2 * 8192;
+                    uint8_t *hb = s.r + c2 * 8192, *lb = hb + 16384;
 #pragma unroll
-                    for (int ch4 = 0; ch4 < 4; ++ch4) {
-                        const uint32_t off = sw128_off((uint32_t)t, (uint32_t)((cc & 1) * 4 + ch4));
+                    for (int ch8 = 0; ch8 < 8; ++ch8) {
+                        const uint32_t off = sw128_off((uint32_t)t, (uint32_t)ch8);
                         const uint4 xv = *reinterpret_cast<const uint4 *>(vt + off);
                         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
                         uint32_t hi[4], lo[4];
@@ -464,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                         for (int e = 0; e < 4; ++e) {
                             float v0, v1;
                             f2_get(f2_bf16x2(xw[e]), v0, v1);
-                            const float r0 = bt * (v0 - w * __uint_as_float(v[8 * ch4 + 2 * e]));
-                            const float r1 = bt * (v1 - w * __uint_as_float(v[8 * ch4 + 2 * e + 1]));
+                            const float r0 = bt * (v0 - w * __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e]));
+                            const float r1 = bt * (v1 - w * __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e + 1]));
                             split_pair(f2(r0, r1), hi[e], lo[e]);
                         }
                         *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -480,16 +513,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                     mbar_arrive(&s.r_ready);
                 }
             } else {
-                const int t = r - 64;
-                const float wq = p.scale * vc.rq[t] * exp2f(vc.gl2[t]);
+                const float wq = vc.osc[r - 64];
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tKQ + cc * 32, v);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tKQ + c2 * 64, v[0]);
+                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * wq);
-                    tmem_st32(tKQ + cc * 32, v);
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * wq);
+                        tmem_st32(tKQ + c2 * 64 + h * 32, v[h]);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -500,31 +536,28 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             if (!wait_bar_warp(&s.u_full, par(c), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             {
-                const float gLl = vc.gl2[kL - 1];
-#pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tU + cc * 32, v);
-                    tmem_ld_wait();
+                uint32_t v[2][32];
+                tmem_ld32(tU, v[0]);
+                tmem_ld32(tU + 32, v[1]);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int ch4 = 0; ch4 < 4; ++ch4) {
-                        uint32_t hi[4], lo[4], hw[4], lw[4];
+                for (int ch8 = 0; ch8 < 8; ++ch8) {
+                    uint32_t hi[4], lo[4], hw[4], lw[4];
+                    const float4 wa = *reinterpret_cast<const float4 *>(&vc.wu[8 * ch8]);
+                    const float4 wb = *reinterpret_cast<const float4 *>(&vc.wu[8 * ch8 + 4]);
+                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int sidx = cc * 32 + 8 * ch4 + 2 * e;
-                            const float u0 = __uint_as_float(v[8 * ch4 + 2 * e]);
-                            const float u1 = __uint_as_float(v[8 * ch4 + 2 * e + 1]);
-                            split_pair(f2(u0, u1), hi[e], lo[e]);
-                            const float w0 = vc.rk[sidx] * exp2f(fminf(gLl - vc.gl2[sidx], 0.f));
-                            const float w1 = vc.rk[sidx + 1] * exp2f(fminf(gLl - vc.gl2[sidx + 1], 0.f));
-                            split_pair(f2(w0 * u0, w1 * u1), hw[e], lw[e]);
-                        }
-                        const uint32_t off = sw128_off((uint32_t)r, (uint32_t)(cc * 4 + ch4));
-                        *reinterpret_cast<uint4 *>(s.r + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(s.r + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        *reinterpret_cast<uint4 *>(s.s0 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4 *>(s.s0 + 16384 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float u0 = __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e]);
+                        const float u1 = __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e + 1]);
+                        split_pair(f2(u0, u1), hi[e], lo[e]);
+                        split_pair(f2(wv[2 * e] * u0, wv[2 * e + 1] * u1), hw[e], lw[e]);
                     }
+                    const uint32_t off = sw128_off((uint32_t)r, (uint32_t)ch8);
+                    *reinterpret_cast<uint4 *>(s.r + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(s.r + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(s.s0 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(s.s0 + 16384 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
             fence_async_smem();
@@ -538,18 +571,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                 const int t = r - 64;
                 __nv_bfloat16 *orow = og + ((size_t)(t0 + t) * p.Hv + hv) * kV;
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tKQ + cc * 32, v);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tKQ + c2 * 64, v[0]);
+                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
                     tmem_ld_wait();
                     if (t < n) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
+                        for (int e = 0; e < 8; ++e) {
                             uint32_t pk[4];
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                pk[j] = pack_bf16x2(__uint_as_float(v[8 * e + 2 * j]), __uint_as_float(v[8 * e + 2 * j + 1]));
-                            *reinterpret_cast<uint4 *>(orow + cc * 32 + 8 * e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                                pk[j] = pack_bf16x2(__uint_as_float(v[e >> 2][8 * (e & 3) + 2 * j]),
+                                                    __uint_as_float(v[e >> 2][8 * (e & 3) + 2 * j + 1]));
+                            *reinterpret_cast<uint4 *>(orow + c2 * 64 + 8 * e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
                     }
                 }
@@ -580,43 +615,55 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         const uint32_t tl = (uint32_t)(q * 32) << 16;
         const float *__restrict__ gg = io.g;
         const float *__restrict__ gb = io.beta;
-        Chunks ch{a, b - a, s0, 0};
-        int64_t t0, ae;
-        int n;
+        Chunks ch{a, b - a, s0, 0}, ahead{a, b - a, s0, 0};
+        int64_t t0, ae, ta0 = 0, tae;
+        int n, na = 0;
+        // warp q = 0 loads each chunk's gates a chunk ahead (lane l: tokens 2l, 2l + 1)
+        float g_nx[2] = {0.f, 0.f}, b_nx[2] = {0.f, 0.f};
+        auto load_gates = [&]() {
+            if (q == 0 && ahead.next(ta0, na, tae)) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = 2 * lane + e;
+                    g_nx[e] = t < na ? gg[(size_t)(ta0 + t) * p.Hv + hv] : 0.f;
+                    b_nx[e] = t < na ? gb[(size_t)(ta0 + t) * p.Hv + hv] : 0.f;
+                }
+            }
+        };
+        load_gates();
         bool ok = true;
         for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
             const int bb = c & 1;
             GdnVec &vc = s.vec[bb];
+            const float gx[2] = {g_nx[0], g_nx[1]}, bx[2] = {b_nx[0], b_nx[1]};
+            load_gates();  // the next chunk's, in flight while this one is prepared
             if (c >= 2 && !wait_bar_warp(&s.vec_free[bb], par((c >> 1) - 1), abort_flag, err)) { ok = false; break; }
             if (!wait_bar_warp(&s.kq_full[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
             // gates: inclusive prefix sums of g log2(e) over the chunk (zero past its tokens)
             if (q == 0) {
-                const int tA = 2 * lane, tB = 2 * lane + 1;
-                const float x0 = tA < n ? gg[(size_t)(t0 + tA) * p.Hv + hv] * kLog2e : 0.f;
-                const float x1 = tB < n ? gg[(size_t)(t0 + tB) * p.Hv + hv] * kLog2e : 0.f;
-                vc.beta[tA] = tA < n ? gb[(size_t)(t0 + tA) * p.Hv + hv] : 0.f;
-                vc.beta[tB] = tB < n ? gb[(size_t)(t0 + tB) * p.Hv + hv] : 0.f;
+                const float x0 = gx[0] * kLog2e, x1 = gx[1] * kLog2e;
+                vc.beta[2 * lane] = bx[0];
+                vc.beta[2 * lane + 1] = bx[1];
                 float incl = x0 + x1;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, incl, o);
                     if (lane >= o) incl += y;
                 }
-                const float excl = incl - (x0 + x1);
-                vc.gl2[tA] = excl + x0;
-                vc.gl2[tB] = incl;
+                vc.gl2[2 * lane] = incl - x1;
+                vc.gl2[2 * lane + 1] = incl;
             }
             // l2 factors: warps q = 0, 1 the k rows 32 q + lane, q = 2, 3 the q rows 32 (q - 2) + lane
+            const int tq = (q & 1) * 32 + lane;
             {
-                const int t = (q & 1) * 32 + lane;
                 float f = 0.f;
-                if (t < n) {
+                if (tq < n) {
                     f = 1.f;
                     if (p.l2norm) {
-                        float ss = 0.f;
+                        float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const uint8_t *row = s.kq[bb] + h * 16384 + (q >= 2 ? 8192 : 0) + t * 128;
+                            const uint8_t *row = s.kq[bb] + h * 16384 + (q >= 2 ? 8192 : 0) + tq * 128;
 #pragma unroll
                             for (int c16 = 0; c16 < 8; ++c16) {
                                 const uint4 raw = *reinterpret_cast<const uint4 *>(row + c16 * 16);
@@ -624,45 +671,55 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const float lo = bf16lo_to_f32(w4[e]), hi = bf16hi_to_f32(w4[e]);
-                                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                                    ss0 = fmaf(lo, lo, ss0);
+                                    ss1 = fmaf(hi, hi, ss1);
                                 }
                             }
                         }
-                        f = rsqrtf(ss + 1e-6f);
+                        f = rsqrtf(ss0 + ss1 + 1e-6f);
                     }
                 }
-                if (q < 2) vc.rk[t] = f;
-                else vc.rq[t] = f;
+                if (q < 2) vc.rk[tq] = f;
+                else vc.rq[tq] = f;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.vec_ready[bb]);
             if (!wait_bar_warp(&s.vec_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
-            // ---- A rows (to shared memory) and P rows (hi/lo in place in TMEM)
+            // what the state chain takes: gamma rk and rk e^{G_L - G} (q = 0, 1), scale gamma rq
+            // (q = 2, 3), gamma_L
+            {
+                const float gLl = vc.gl2[kL - 1], gt = vc.gl2[tq];
+                if (q < 2) {
+                    vc.grk[tq] = fast_exp2(gt) * vc.rk[tq];
+                    vc.wu[tq] = vc.rk[tq] * fast_exp2(fminf(gLl - gt, 0.f));
+                } else {
+                    vc.osc[tq] = p.scale * vc.rq[tq] * fast_exp2(gt);
+                }
+                if (q == 0 && lane == 0) vc.gL = fast_exp2(gLl);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.vec2_ready[bb]);
+            // ---- A (to shared memory, transposed) and P rows (hi/lo in place in TMEM)
             if (!wait_bar_warp(&s.ap_full[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             const uint32_t tAP = tbase + tl + kColAP + 64u * bb;
             if (q < 2) {
-                const int sr = q * 32 + lane;
+                const int sr = tq;
                 const float ws = vc.beta[sr] * vc.rk[sr], gs = vc.gl2[sr];
-#pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tAP + cc * 32, v);
-                    tmem_ld_wait();
+                uint32_t v[2][32];
+                tmem_ld32(tAP, v[0]);
+                tmem_ld32(tAP + 32, v[1]);
+                tmem_ld_wait();
+                // A^T[rc][sr] = A[sr][rc]: for each rc the lanes store consecutive words
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        float av[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int rc = cc * 32 + 4 * e4 + e;
-                            av[e] = rc < sr ? ws * vc.rk[rc] * exp2f(fminf(gs - vc.gl2[rc], 0.f)) * __uint_as_float(v[4 * e4 + e])
-                                            : 0.f;
-                        }
-                        *reinterpret_cast<float4 *>(s.a + sr * kLdA + cc * 32 + 4 * e4) = make_float4(av[0], av[1], av[2], av[3]);
-                    }
+                for (int rc = 0; rc < kL; ++rc) {
+                    const float av = rc < sr ? ws * vc.rk[rc] * fast_exp2(fminf(gs - vc.gl2[rc], 0.f)) *
+                                                   __uint_as_float(v[rc >> 5][rc & 31])
+                                             : 0.f;
+                    s.a[rc * kLdA + sr] = av;
                 }
             } else {
-                const int t = (q - 2) * 32 + lane;
+                const int t = tq;
                 const float wt = p.scale * vc.rq[t], gt = vc.gl2[t];
                 uint32_t v[2][32];
                 tmem_ld32(tAP, v[0]);
@@ -676,8 +733,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                         const int s0i = kk * 16 + 2 * e;
                         const float q0 = __uint_as_float(v[kk >> 1][(kk & 1) * 16 + 2 * e]);
                         const float q1 = __uint_as_float(v[kk >> 1][(kk & 1) * 16 + 2 * e + 1]);
-                        const float p0 = s0i <= t ? wt * vc.rk[s0i] * exp2f(fminf(gt - vc.gl2[s0i], 0.f)) * q0 : 0.f;
-                        const float p1 = s0i + 1 <= t ? wt * vc.rk[s0i + 1] * exp2f(fminf(gt - vc.gl2[s0i + 1], 0.f)) * q1 : 0.f;
+                        const float p0 = s0i <= t ? wt * vc.rk[s0i] * fast_exp2(fminf(gt - vc.gl2[s0i], 0.f)) * q0 : 0.f;
+                        const float p1 =
+                            s0i + 1 <= t ? wt * vc.rk[s0i + 1] * fast_exp2(fminf(gt - vc.gl2[s0i + 1], 0.f)) * q1 : 0.f;
                         split_pair(f2(p0, p1), hi[e], lo[e]);
                     }
                     tmem_st8(tAP + kk * 16, hi);
@@ -689,28 +747,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.p_ready[bb]);
             if (q >= 2) continue;
-            // ---- T = (I + A)^-1 by forward substitution, column j per thread; written
-            // as T^T (row j = column j of T) hi/lo, once the last U product has read T
+            // ---- T = (I + A)^-1, column j per thread, by a right-looking substitution: once
+            // x[c] is final, every later row takes its term -A[r][c] x[c] (independent
+            // updates, A^T row c read four entries at a time); T^T row j = column j of T
+            // is then written as hi/lo, once the last U product has read T
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.a_ready);
             if (!wait_bar_warp(&s.a_ready, par(c), abort_flag, err)) { ok = false; break; }
-            const int j = q * 32 + lane;
+            const int j = tq;
             float x[kL];
 #pragma unroll
-            for (int rr = 0; rr < kL; ++rr) x[rr] = 0.f;
+            for (int rr = 0; rr < kL; ++rr) x[rr] = rr == j ? 1.f : 0.f;
 #pragma unroll
-            for (int rr = 0; rr < kL; ++rr) {
-                float acc0 = 0.f, acc1 = 0.f;
-                const float *arow = s.a + rr * kLdA;
+            for (int cc = 0; cc < kL - 1; ++cc) {
+                const float xc = x[cc];
+                const float *arow = s.a + cc * kLdA;
 #pragma unroll
-                for (int cc = 0; cc < rr; cc += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + cc);
-                    acc0 = fmaf(a4.x, x[cc], acc0);
-                    acc1 = fmaf(a4.y, x[cc + 1], acc1);
-                    acc0 = fmaf(a4.z, x[cc + 2], acc0);
-                    acc1 = fmaf(a4.w, x[cc + 3], acc1);
+                for (int rr = (cc + 1) & ~3; rr < kL; rr += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + rr);
+                    // entries rr <= cc of A^T row cc are zero (A is strictly lower)
+                    x[rr] = fmaf(-a4.x, xc, x[rr]);
+                    x[rr + 1] = fmaf(-a4.y, xc, x[rr + 1]);
+                    x[rr + 2] = fmaf(-a4.z, xc, x[rr + 2]);
+                    x[rr + 3] = fmaf(-a4.w, xc, x[rr + 3]);
                 }
-                x[rr] = rr == j ? 1.f : (rr < j ? 0.f : -(acc0 + acc1));
             }
             if (c >= 1 && !wait_bar_warp(&s.t_free, par(c - 1), abort_flag, err)) { ok = false; break; }
 #pragma unroll
