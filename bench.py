@@ -102,7 +102,9 @@ def load_peaks():
 ROW_KERNEL_SOURCES = {
     "conv": ["mamba2_ssd_varlen_gb300/csrc/ssd_conv1d.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
     "decode": ["mamba2_ssd_varlen_gb300/csrc/ssd_decode.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
-    "gdn": ["mamba2_ssd_varlen_gb300/csrc/ssd_gdn.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
+    "gdn": ["mamba2_ssd_varlen_gb300/csrc/ssd_gdn_tc.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_gdn.cu",
+            "mamba2_ssd_varlen_gb300/csrc/tc_util.cuh", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
+            "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
 }
 
 
