@@ -16,9 +16,10 @@
 //       first segments later (the k-th segments of all requests are taken
 //       after every (k-1)-th one), picks it up -- one pass over the data;
 //       pre-pass: every segment's state from zero and its total decay are
-//       computed first and chained (ssd_chunk_tc.cu), for batches whose
-//       longest request would otherwise be a serial chain longer than the
-//       work of a CTA (a few long requests);
+//       computed first (ssd_segstate.cu for headdim 64, the state-only mode of
+//       ssd_chunk_tc.cu otherwise) and chained (seg_pass_kernel), for batches
+//       whose longest request would otherwise be a serial chain longer than
+//       the work of a CTA (a few long requests);
 //   * validation bits for the device error word.
 // One CTA of 1024 threads; no host synchronisation.
 #include "ssd_internal.cuh"
