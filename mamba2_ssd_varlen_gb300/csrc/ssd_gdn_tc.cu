@@ -22,8 +22,8 @@
 //     S  += K^T U'                   (U' = diag(rk e^{G_L - G}) U as hi + lo; S pre-scaled by gamma_L)
 //     O  += P U                      (onto the Q S0 rows scaled by scale gamma rq; P hi/lo in TMEM)
 // q, k, v enter exactly (bf16); every fp32 operand is split into a bf16 high part
-// and a bf16 remainder, about 16 significant bits.  T comes from A by forward
-// substitution in fp32 (one column per thread).
+// and a bf16 remainder, about 16 significant bits.  T comes from A in fp32 by
+// 32 x 32 blocks (substitution for the diagonal blocks, products for the other).
 //
 // One CTA per (request, value head); roles:
 //   warp 0      TMA: the K and Q tiles of each chunk (two buffers), the V tile;
@@ -31,8 +31,9 @@
 //   warps 4-7   the state chain: S read-out (state outputs, S0 hi/lo, gamma_L S),
 //               R, the scaling of the Q S0 rows, U and U' hi/lo, the output rows;
 //   warps 8-11  the next chunk: gates and their prefix sums, l2 factors, A
-//               (to shared memory) and P (hi/lo in place in TMEM), then T by a
-//               right-looking substitution (independent updates of the later rows).
+//               (to shared memory) and P (hi/lo in place in TMEM), then T by 32 x 32
+//               blocks: the two diagonal blocks by right-looking substitutions in
+//               parallel, the off-diagonal one by two small products.
 // Every wait is a bounded mbarrier wait; on a timeout the CTA records
 // SSD_DEVERR_TIMEOUT in the call's device error word, drains and exits.
 #include <cudaTypedefs.h>
@@ -88,11 +89,12 @@ struct __align__(1024) GdnTcSmem {
     uint8_t r[32768];      // R hi | lo [v-half][64 t rows][64 v]; then U hi | lo [128 v rows][64 s]
     uint8_t v[16384];      // V tile [v-half][64 t rows][64 v]
     uint8_t t[16384];      // T^T hi | lo [64 s rows][64 t]
-    float a[kL * kLdA];    // A^T (row c = column c of A), fp32
+    float a[kL * kLdA];    // A^T (row c = column c of A), fp32; rows 32..63, columns 0..31: T22^T
+    float t11[32 * 33], m1[32 * 33], t21[32 * 33];  // blocks of T = (I + A)^-1, column-major
     GdnVec vec[2];
     uint64_t kq_full[2], kq_empty[2], ap_full[2], p_ready[2], vec_ready[2], vec2_ready[2], vec_free[2];
-    uint64_t v_full, v_empty, a_ready, t_ready, t_free, s0_copy, kqs0_full, r_ready, o_scaled, u_full, u_copy,
-        s_ready, o_full, o_free, drain;
+    uint64_t v_full, v_empty, a_ready, inv1, inv2, inv3, t_ready, t_free, s0_copy, kqs0_full, r_ready, o_scaled,
+        u_full, u_copy, s_ready, o_full, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -204,6 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         mbar_init(&s.v_full, 1);
         mbar_init(&s.v_empty, 2);
         mbar_init(&s.a_ready, 2);
+        mbar_init(&s.inv1, 2);
+        mbar_init(&s.inv2, 4);
+        mbar_init(&s.inv3, 4);
         mbar_init(&s.t_ready, 2);
         mbar_init(&s.t_free, 1);
         mbar_init(&s.s0_copy, 4);
@@ -703,39 +708,43 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             if (!wait_bar_warp(&s.ap_full[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             const uint32_t tAP = tbase + tl + kColAP + 64u * bb;
+            // one 16-column block of TMEM per round (a short loop body: the code stays small)
             if (q < 2) {
                 const int sr = tq;
                 const float ws = vc.beta[sr] * vc.rk[sr], gs = vc.gl2[sr];
-                uint32_t v[2][32];
-                tmem_ld32(tAP, v[0]);
-                tmem_ld32(tAP + 32, v[1]);
-                tmem_ld_wait();
-                // A^T[rc][sr] = A[sr][rc]: for each rc the lanes store consecutive words
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t v[16];
+                    tmem_ld16(tAP + cb * 16, v);
+                    tmem_ld_wait();
+                    // A^T[rc][sr] = A[sr][rc]: for each rc the lanes store consecutive words
 #pragma unroll
-                for (int rc = 0; rc < kL; ++rc) {
-                    const float av = rc < sr ? ws * vc.rk[rc] * fast_exp2(fminf(gs - vc.gl2[rc], 0.f)) *
-                                                   __uint_as_float(v[rc >> 5][rc & 31])
-                                             : 0.f;
-                    s.a[rc * kLdA + sr] = av;
+                    for (int e = 0; e < 16; ++e) {
+                        const int rc = cb * 16 + e;
+                        const float av = rc < sr ? ws * vc.rk[rc] * fast_exp2(fminf(gs - vc.gl2[rc], 0.f)) *
+                                                       __uint_as_float(v[e])
+                                                 : 0.f;
+                        s.a[rc * kLdA + sr] = av;
+                    }
                 }
             } else {
                 const int t = tq;
                 const float wt = p.scale * vc.rq[t], gt = vc.gl2[t];
-                uint32_t v[2][32];
-                tmem_ld32(tAP, v[0]);
-                tmem_ld32(tAP + 32, v[1]);
-                tmem_ld_wait();
-#pragma unroll
+                // in place per block: the 16 fp32 columns read become 8 hi + 8 lo columns
+#pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk) {
+                    uint32_t v[16];
+                    tmem_ld16(tAP + kk * 16, v);
+                    tmem_ld_wait();
                     uint32_t hi[8], lo[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s0i = kk * 16 + 2 * e;
-                        const float q0 = __uint_as_float(v[kk >> 1][(kk & 1) * 16 + 2 * e]);
-                        const float q1 = __uint_as_float(v[kk >> 1][(kk & 1) * 16 + 2 * e + 1]);
-                        const float p0 = s0i <= t ? wt * vc.rk[s0i] * fast_exp2(fminf(gt - vc.gl2[s0i], 0.f)) * q0 : 0.f;
-                        const float p1 =
-                            s0i + 1 <= t ? wt * vc.rk[s0i + 1] * fast_exp2(fminf(gt - vc.gl2[s0i + 1], 0.f)) * q1 : 0.f;
+                        const float p0 =
+                            s0i <= t ? wt * vc.rk[s0i] * fast_exp2(fminf(gt - vc.gl2[s0i], 0.f)) * __uint_as_float(v[2 * e]) : 0.f;
+                        const float p1 = s0i + 1 <= t ? wt * vc.rk[s0i + 1] * fast_exp2(fminf(gt - vc.gl2[s0i + 1], 0.f)) *
+                                                            __uint_as_float(v[2 * e + 1])
+                                                      : 0.f;
                         split_pair(f2(p0, p1), hi[e], lo[e]);
                     }
                     tmem_st8(tAP + kk * 16, hi);
@@ -746,41 +755,117 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.p_ready[bb]);
-            if (q >= 2) continue;
-            // ---- T = (I + A)^-1, column j per thread, by a right-looking substitution: once
-            // x[c] is final, every later row takes its term -A[r][c] x[c] (independent
-            // updates, A^T row c read four entries at a time); T^T row j = column j of T
-            // is then written as hi/lo, once the last U product has read T
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.a_ready);
-            if (!wait_bar_warp(&s.a_ready, par(c), abort_flag, err)) { ok = false; break; }
-            const int j = tq;
-            float x[kL];
+            // ---- T = (I + A)^-1 by 32 x 32 blocks:
+            //   T11 = (I + A11)^-1, T22 = (I + A22)^-1   (warps q = 0 and 1, in parallel: one
+            //        column per thread by a right-looking substitution over 32 rows)
+            //   M1  = A21 T11,  T21 = -T22 M1           (all four warps: 8 rows x 1 column each)
+            // T11, M1, T21 are kept column by column (stride 33, lane-indexed reads); T22
+            // as rows of T22^T in the A^T rows 32..63, columns 0..31 (that block, A12^T, is
+            // zero and never read).  T^T (row j = column j of T) is then written as hi/lo,
+            // once the last U product has read T.
+            const int j = lane;
+            if (q < 2) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.a_ready);
+                if (!wait_bar_warp(&s.a_ready, par(c), abort_flag, err)) { ok = false; break; }
+                const int o = 32 * q;  // the diagonal block's first row / column
+                float x[32];
 #pragma unroll
-            for (int rr = 0; rr < kL; ++rr) x[rr] = rr == j ? 1.f : 0.f;
+                for (int rr = 0; rr < 32; ++rr) x[rr] = rr == j ? 1.f : 0.f;
 #pragma unroll
-            for (int cc = 0; cc < kL - 1; ++cc) {
-                const float xc = x[cc];
-                const float *arow = s.a + cc * kLdA;
+                for (int cc = 0; cc < 31; ++cc) {
+                    const float xc = x[cc];
+                    const float *arow = s.a + (o + cc) * kLdA + o;
 #pragma unroll
-                for (int rr = (cc + 1) & ~3; rr < kL; rr += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + rr);
-                    // entries rr <= cc of A^T row cc are zero (A is strictly lower)
-                    x[rr] = fmaf(-a4.x, xc, x[rr]);
-                    x[rr + 1] = fmaf(-a4.y, xc, x[rr + 1]);
-                    x[rr + 2] = fmaf(-a4.z, xc, x[rr + 2]);
-                    x[rr + 3] = fmaf(-a4.w, xc, x[rr + 3]);
+                    for (int rr = (cc + 1) & ~3; rr < 32; rr += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(arow + rr);
+                        // entries rr <= cc of A^T row cc are zero (A is strictly lower)
+                        x[rr] = fmaf(-a4.x, xc, x[rr]);
+                        x[rr + 1] = fmaf(-a4.y, xc, x[rr + 1]);
+                        x[rr + 2] = fmaf(-a4.z, xc, x[rr + 2]);
+                        x[rr + 3] = fmaf(-a4.w, xc, x[rr + 3]);
+                    }
                 }
+                if (q == 0) {
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr) s.t11[j * 33 + rr] = x[rr];
+                } else {
+#pragma unroll
+                    for (int rr = 0; rr < 32; rr += 4)
+                        *reinterpret_cast<float4 *>(s.a + (32 + j) * kLdA + rr) = make_float4(x[rr], x[rr + 1], x[rr + 2], x[rr + 3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.inv1);
             }
+            if (!wait_bar_warp(&s.inv1, par(c), abort_flag, err)) { ok = false; break; }
+            const int r0 = 8 * q;  // this warp's 8 rows of M1 and T21
+            {
+                // M1[r][j] = sum_c A[32 + r][c] T11[c][j] = sum_c A^T[c][32 + r] T11[c][j]
+                float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int cc = 0; cc < 32; ++cc) {
+                    const float tv = s.t11[j * 33 + cc];
+                    const float4 a0 = *reinterpret_cast<const float4 *>(s.a + cc * kLdA + 32 + r0);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(s.a + cc * kLdA + 36 + r0);
+                    m[0] = fmaf(a0.x, tv, m[0]);
+                    m[1] = fmaf(a0.y, tv, m[1]);
+                    m[2] = fmaf(a0.z, tv, m[2]);
+                    m[3] = fmaf(a0.w, tv, m[3]);
+                    m[4] = fmaf(a1.x, tv, m[4]);
+                    m[5] = fmaf(a1.y, tv, m[5]);
+                    m[6] = fmaf(a1.z, tv, m[6]);
+                    m[7] = fmaf(a1.w, tv, m[7]);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s.m1[j * 33 + r0 + e] = m[e];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.inv2);
+            if (!wait_bar_warp(&s.inv2, par(c), abort_flag, err)) { ok = false; break; }
+            {
+                // T21[r][j] = -sum_k T22[r][k] M1[k][j]; T22[r][k] = (T22^T row k)[r]
+                float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int kk = 0; kk < 32; ++kk) {
+                    const float mv = s.m1[j * 33 + kk];
+                    const float4 t0v = *reinterpret_cast<const float4 *>(s.a + (32 + kk) * kLdA + r0);
+                    const float4 t1v = *reinterpret_cast<const float4 *>(s.a + (32 + kk) * kLdA + r0 + 4);
+                    m[0] = fmaf(-t0v.x, mv, m[0]);
+                    m[1] = fmaf(-t0v.y, mv, m[1]);
+                    m[2] = fmaf(-t0v.z, mv, m[2]);
+                    m[3] = fmaf(-t0v.w, mv, m[3]);
+                    m[4] = fmaf(-t1v.x, mv, m[4]);
+                    m[5] = fmaf(-t1v.y, mv, m[5]);
+                    m[6] = fmaf(-t1v.z, mv, m[6]);
+                    m[7] = fmaf(-t1v.w, mv, m[7]);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s.t21[j * 33 + r0 + e] = m[e];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.inv3);
+            if (q >= 2) continue;
+            if (!wait_bar_warp(&s.inv3, par(c), abort_flag, err)) { ok = false; break; }
             if (c >= 1 && !wait_bar_warp(&s.t_free, par(c - 1), abort_flag, err)) { ok = false; break; }
+            {
+                // row sj of T^T = column sj of T: rows 0..31 then 32..63
+                const int sj = 32 * q + j;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t hi[4], lo[4];
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float col[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) split_pair(f2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1]), hi[e], lo[e]);
-                const uint32_t off = sw128_off((uint32_t)j, (uint32_t)c8);
-                *reinterpret_cast<uint4 *>(s.t + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(s.t + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int e = 0; e < 8; ++e) {
+                        const int t = 8 * c8 + e;
+                        if (q == 0) col[e] = t < 32 ? s.t11[j * 33 + t] : s.t21[j * 33 + (t - 32)];
+                        else col[e] = t < 32 ? 0.f : s.a[(32 + j) * kLdA + (t - 32)];
+                    }
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split_pair(f2(col[2 * e], col[2 * e + 1]), hi[e], lo[e]);
+                    const uint32_t off = sw128_off((uint32_t)sj, (uint32_t)c8);
+                    *reinterpret_cast<uint4 *>(s.t + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(s.t + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
             }
             fence_async_smem();
             __syncwarp();
