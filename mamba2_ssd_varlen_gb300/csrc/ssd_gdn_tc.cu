@@ -28,8 +28,9 @@
 // One CTA per (request, value head); roles:
 //   warp 0      TMA: the K and Q tiles of each chunk (two buffers), the V tile;
 //   warp 1      MMA issuer and TMEM owner;
+//   warps 2, 3  the output rows (O, in TMEM lane quadrants 2 and 3) -> bf16;
 //   warps 4-7   the state chain: S read-out (state outputs, S0 hi/lo, gamma_L S),
-//               R, the scaling of the Q S0 rows, U and U' hi/lo, the output rows;
+//               R, the scaling of the Q S0 rows, U and U' hi/lo;
 //   warps 8-11  the next chunk: gates and their prefix sums, l2 factors, A
 //               (to shared memory) and P (hi/lo in place in TMEM), then T by 32 x 32
 //               blocks: the two diagonal blocks by right-looking substitutions in
@@ -56,7 +57,7 @@ constexpr int kL = 64;    // chunk length
 constexpr int kK = 128;   // key head dim
 constexpr int kV = 128;   // value head dim
 constexpr int kThreads = 12 * 32;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpChain = 4, kWarpPrep = 8;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpOut = 2, kWarpChain = 4, kWarpPrep = 8;
 constexpr int kLdA = kL + 4;  // fp32 row stride of A (float4 rows, conflict-free)
 constexpr uint64_t kWaitNs = 1000000000ull;
 // TMEM columns: S (128) | [K S0 ; Q S0] then O (128) | [KK^T ; QK^T] / P, two buffers (2 x 64) | U^T (64)
@@ -80,6 +81,7 @@ struct GdnTcMaps {
 struct GdnVec {
     float gl2[kL], beta[kL], rk[kL], rq[kL];
     float grk[kL], osc[kL], wu[kL];
+    float wb[kL];  // rk_r e^{G_b - G_r}, b = the last row of r's 16-row block (the masks' column factor)
     float gL, pad[3];
 };
 
@@ -401,7 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                         make_uint4(vals[4 * e], vals[4 * e + 1], vals[4 * e + 2], vals[4 * e + 3]);
             }
         };
-        __nv_bfloat16 *__restrict__ og = static_cast<__nv_bfloat16 *>(io.o);
         Chunks ch{a, b - a, s0, 0};
         int64_t t0 = 0, ae = 0, prev_ae = 0;
         int n = 0;
@@ -409,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
             const int bb = c & 1;
             const GdnVec &vc = s.vec[bb];
-            // ---- S: state outputs of the previous chunk and S0 hi/lo (for the K S0 / Q S0
-            // product, published first), then gamma_L S in place (before the state product)
+            // ---- S: state outputs of the previous chunk, S0 hi/lo (for the K S0 / Q S0
+            // product) and gamma_L S in place, in one pass
             if (c >= 1 && !wait_bar_warp(&s.s_ready, par(c - 1), abort_flag, err)) { ok = false; break; }
             if (!wait_bar_warp(&s.vec2_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
@@ -446,28 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                         *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4 *>(lb + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
-                    if (c == 0) {
-                        // the first chunk's state comes from memory: it goes to TMEM scaled here
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * vc.gL);
-                            tmem_st32(tS + c2 * 64 + h * 32, v[h]);
-                        }
-                    }
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.s0_copy);
-            if (c >= 1) {
-#pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t v[2][32];
-                    tmem_ld32(tS + c2 * 64, v[0]);
-                    tmem_ld32(tS + c2 * 64 + 32, v[1]);
-                    tmem_ld_wait();
+                    // gamma_L S back to TMEM in the same pass (the state product adds to it)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -477,6 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                 }
             }
             tmem_st_wait();
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.s0_copy);
             // ---- R = diag(beta) (V - diag(gamma rk) K S0); the Q S0 rows scaled by scale gamma rq
             if (!wait_bar_warp(&s.kqs0_full, par(c), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
@@ -569,34 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.u_copy);
-            // ---- output rows: O (rows 64..127 of the [K S0 ; Q S0] accumulator) -> bf16
-            if (q >= 2) {
-                if (!wait_bar_warp(&s.o_full, par(c), abort_flag, err)) { ok = false; break; }
-                tc_fence_after();
-                const int t = r - 64;
-                __nv_bfloat16 *orow = og + ((size_t)(t0 + t) * p.Hv + hv) * kV;
-#pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t v[2][32];
-                    tmem_ld32(tKQ + c2 * 64, v[0]);
-                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
-                    tmem_ld_wait();
-                    if (t < n) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                pk[j] = pack_bf16x2(__uint_as_float(v[e >> 2][8 * (e & 3) + 2 * j]),
-                                                    __uint_as_float(v[e >> 2][8 * (e & 3) + 2 * j + 1]));
-                            *reinterpret_cast<uint4 *>(orow + c2 * 64 + 8 * e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.o_free);
-            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.vec_free[bb]);
             prev_ae = ae;
@@ -612,6 +568,48 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                 tmem_ld_wait();
                 store_row(d, cc, v);
                 store_row(fin, cc, v);
+            }
+        }
+    } else if (warp == kWarpOut || warp == kWarpOut + 1) {
+        // ------------------------------------------------------------ output rows
+        // O = rows 64..127 of the [K S0 ; Q S0] accumulator (warps 2, 3: TMEM lane
+        // quadrants 2, 3) -> bf16, so that the chain warps of those quadrants go on to
+        // the next chunk's state read-out meanwhile.
+        const int q = warp & 3;
+        const int t = (q - 2) * 32 + lane;  // token row of the chunk
+        const uint32_t tKQ = tbase + ((uint32_t)(q * 32) << 16) + kColKQ;
+        __nv_bfloat16 *__restrict__ og = static_cast<__nv_bfloat16 *>(io.o);
+        Chunks ch{a, b - a, s0, 0};
+        int64_t t0, ae;
+        int n;
+        bool ok = true;
+        for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
+            if (!wait_bar_warp(&s.o_full, par(c), abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            __nv_bfloat16 *orow = og + ((size_t)(t0 + t) * p.Hv + hv) * kV;
+#pragma unroll 1
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t v[2][32];
+                tmem_ld32(tKQ + c2 * 64, v[0]);
+                tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
+                tmem_ld_wait();
+                if (c2 == 1) {
+                    // the accumulator is free for the next chunk's K S0 / Q S0 product
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.o_free);
+                }
+                if (t < n) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            pk[jj] = pack_bf16x2(__uint_as_float(v[e >> 2][8 * (e & 3) + 2 * jj]),
+                                                 __uint_as_float(v[e >> 2][8 * (e & 3) + 2 * jj + 1]));
+                        *reinterpret_cast<uint4 *>(orow + c2 * 64 + 8 * e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
             }
         }
     } else if (warp >= kWarpPrep) {
@@ -697,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                 if (q < 2) {
                     vc.grk[tq] = fast_exp2(gt) * vc.rk[tq];
                     vc.wu[tq] = vc.rk[tq] * fast_exp2(fminf(gLl - gt, 0.f));
+                    vc.wb[tq] = vc.rk[tq] * fast_exp2(fminf(vc.gl2[tq | 15] - gt, 0.f));
                 } else {
                     vc.osc[tq] = p.scale * vc.rq[tq] * fast_exp2(gt);
                 }
@@ -704,31 +703,45 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.vec2_ready[bb]);
-            // ---- A (to shared memory, transposed) and P rows (hi/lo in place in TMEM)
+            if (!wait_bar_warp(&s.vec2_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            // ---- A (to shared memory, transposed) and P rows (hi/lo in place in TMEM).  Below
+            // the diagonal 16-row block the decay splits around the column block's last row
+            // b: e^{G_s - G_r} = e^{G_s - G_b} e^{G_b - G_r}, both factors <= 1, the second
+            // (times rk_r) precomputed per column; the diagonal block is evaluated directly.
             if (!wait_bar_warp(&s.ap_full[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             const uint32_t tAP = tbase + tl + kColAP + 64u * bb;
             // one 16-column block of TMEM per round (a short loop body: the code stays small)
             if (q < 2) {
-                const int sr = tq;
+                const int sr = tq, bs = sr >> 4;
                 const float ws = vc.beta[sr] * vc.rk[sr], gs = vc.gl2[sr];
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t v[16];
                     tmem_ld16(tAP + cb * 16, v);
                     tmem_ld_wait();
+                    float av[16];
+                    if (cb < bs) {
+                        const float f = ws * fast_exp2(fminf(gs - vc.gl2[16 * cb + 15], 0.f));
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) av[e] = f * vc.wb[cb * 16 + e] * __uint_as_float(v[e]);
+                    } else if (cb == bs) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int rc = cb * 16 + e;
+                            av[e] = rc < sr ? ws * vc.rk[rc] * fast_exp2(fminf(gs - vc.gl2[rc], 0.f)) * __uint_as_float(v[e])
+                                            : 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) av[e] = 0.f;
+                    }
                     // A^T[rc][sr] = A[sr][rc]: for each rc the lanes store consecutive words
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int rc = cb * 16 + e;
-                        const float av = rc < sr ? ws * vc.rk[rc] * fast_exp2(fminf(gs - vc.gl2[rc], 0.f)) *
-                                                       __uint_as_float(v[e])
-                                                 : 0.f;
-                        s.a[rc * kLdA + sr] = av;
-                    }
+                    for (int e = 0; e < 16; ++e) s.a[(cb * 16 + e) * kLdA + sr] = av[e];
                 }
             } else {
-                const int t = tq;
+                const int t = tq, bt = t >> 4;
                 const float wt = p.scale * vc.rq[t], gt = vc.gl2[t];
                 // in place per block: the 16 fp32 columns read become 8 hi + 8 lo columns
 #pragma unroll 1
@@ -736,17 +749,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                     uint32_t v[16];
                     tmem_ld16(tAP + kk * 16, v);
                     tmem_ld_wait();
+                    float pv[16];
+                    if (kk < bt) {
+                        const float f = wt * fast_exp2(fminf(gt - vc.gl2[16 * kk + 15], 0.f));
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pv[e] = f * vc.wb[kk * 16 + e] * __uint_as_float(v[e]);
+                    } else if (kk == bt) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int sc = kk * 16 + e;
+                            pv[e] = sc <= t ? wt * vc.rk[sc] * fast_exp2(fminf(gt - vc.gl2[sc], 0.f)) * __uint_as_float(v[e])
+                                            : 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pv[e] = 0.f;
+                    }
                     uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s0i = kk * 16 + 2 * e;
-                        const float p0 =
-                            s0i <= t ? wt * vc.rk[s0i] * fast_exp2(fminf(gt - vc.gl2[s0i], 0.f)) * __uint_as_float(v[2 * e]) : 0.f;
-                        const float p1 = s0i + 1 <= t ? wt * vc.rk[s0i + 1] * fast_exp2(fminf(gt - vc.gl2[s0i + 1], 0.f)) *
-                                                            __uint_as_float(v[2 * e + 1])
-                                                      : 0.f;
-                        split_pair(f2(p0, p1), hi[e], lo[e]);
-                    }
+                    for (int e = 0; e < 8; ++e) split_pair(f2(pv[2 * e], pv[2 * e + 1]), hi[e], lo[e]);
                     tmem_st8(tAP + kk * 16, hi);
                     tmem_st8(tAP + kk * 16 + 8, lo);
                 }
