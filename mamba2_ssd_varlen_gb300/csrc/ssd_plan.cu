@@ -21,18 +21,22 @@
 //       whose longest request would otherwise be a serial chain longer than
 //       the work of a CTA (a few long requests);
 //   * validation bits for the device error word.
-// One CTA of 1024 threads; no host synchronisation.
+// One CTA of up to 1024 threads (one per request, at least 64); no host
+// synchronisation.
+#include <algorithm>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;  // at most; the launch sizes the block to the batch
 
-// Block-wide exclusive scan of two counters; returns the block totals.
+// Block-wide exclusive scan of two counters; returns the block totals.  Any block
+// of whole warps (at most 32).
 __device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
     __shared__ int wa[32], wb[32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
     int ia = a, ib = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -42,7 +46,7 @@ __device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
     if (lane == 31) { wa[warp] = ia; wb[warp] = ib; }
     __syncthreads();
     if (warp == 0) {
-        int sa = wa[lane], sb = wb[lane];
+        int sa = lane < nw ? wa[lane] : 0, sb = lane < nw ? wb[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int va = __shfl_up_sync(0xffffffffu, sa, o), vb = __shfl_up_sync(0xffffffffu, sb, o);
@@ -55,8 +59,8 @@ __device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
     const int pa = warp ? wa[warp - 1] : 0, pb = warp ? wb[warp - 1] : 0;
     ea = pa + ia - a;
     eb = pb + ib - b;
-    ta = wa[31];
-    tb = wb[31];
+    ta = wa[nw - 1];
+    tb = wb[nw - 1];
     __syncthreads();
 }
 
@@ -89,7 +93,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     int err = 0, n_empty = 0, my_max_segs = 0;
     long long my_max_len = 0;
     int carry_c = 0, carry_s = 0;
-    for (int base = 0; base < R; base += kPlanThreads) {
+    const int nt = (int)blockDim.x;
+    for (int base = 0; base < R; base += nt) {
         const int i = base + threadIdx.x;
         int nc = 0, ns = 0;
         if (i < R) {
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     if (chained) {
         int base = 0;
         for (int k = 0; k < maxk; ++k) {
-            for (int b0 = 0; b0 < R; b0 += kPlanThreads) {
+            for (int b0 = 0; b0 < R; b0 += nt) {
                 const int i = b0 + threadIdx.x;
                 const int has = (i < R && segs_of(cu, ncomp, i, seg_len) > k) ? 1 : 0;
                 int e1, e2, t1, t2;
@@ -167,12 +172,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
             }
         }
         const int64_t nflags = (int64_t)(carry_s - R) * a.H;
-        for (int64_t j = threadIdx.x; j < nflags; j += kPlanThreads) a.seg_flags[j] = 0;
+        for (int64_t j = threadIdx.x; j < nflags; j += nt) a.seg_flags[j] = 0;
     } else {
-        for (int j = threadIdx.x; j < carry_s; j += kPlanThreads) a.seg_order[j] = j;
+        for (int j = threadIdx.x; j < carry_s; j += nt) a.seg_order[j] = j;
     }
     // Fill the segment list (one thread per request; long requests loop).
-    for (int i = threadIdx.x; i < R; i += kPlanThreads) {
+    for (int i = threadIdx.x; i < R; i += nt) {
         const int64_t a = cu[i], L = (int64_t)cu[i + 1] - a;
         const int64_t s = ncomp ? (int64_t)ncomp[i] : 0;
         const int first = req_first_seg[i], cnt = req_first_seg[i + 1] - first;
@@ -192,7 +197,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
 }  // namespace
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
+    // one warp per 32 requests, at least two (the flag zeroing), at most 32
+    const int threads = (int)std::min<int64_t>(kPlanThreads, std::max<int64_t>(64, ((int64_t)a.R + 31) / 32 * 32));
+    plan_kernel<<<1, threads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
