@@ -17,8 +17,10 @@
 // and T) is prepared one chunk ahead of the state chain, whose products all run
 // on the tensor cores with their accumulators in TMEM:
 //     [K;Q] [K]^T -> [KK^T ; QK^T]   (M = 128: the 64 k rows over the 64 q rows)
-//     [K;Q] S0    -> [K S0 ; Q S0]   (S0 as bf16 hi + lo)
-//     U^T = R^T T^T                  (R and T as bf16 hi + lo: hi.hi + hi.lo + lo.hi)
+//     S0^T K^T    -> (K S0)^T        (S0 as bf16 hi + lo; value columns on the TMEM lanes)
+//     [K;Q] S0    -> [K S0 ; Q S0]   (only the Q S0 rows are used: the output)
+//     U^T = R^T T^T                  (R^T hi/lo formed in TMEM over (K S0)^T, T hi/lo:
+//                                     hi.hi + hi.lo + lo.hi)
 //     S  += K^T U'                   (U' = diag(rk e^{G_L - G}) U as hi + lo; S pre-scaled by gamma_L)
 //     O  += P U                      (onto the Q S0 rows scaled by scale gamma rq; P hi/lo in TMEM)
 // q, k, v enter exactly (bf16); every fp32 operand is split into a bf16 high part
@@ -28,9 +30,10 @@
 // One CTA per (request, value head); roles:
 //   warp 0      TMA: the K and Q tiles of each chunk (two buffers), the V tile;
 //   warp 1      MMA issuer and TMEM owner;
-//   warps 2, 3  the output rows (O, in TMEM lane quadrants 2 and 3) -> bf16;
+//   warps 2, 3  the output rows (TMEM lane quadrants 2 and 3): the Q S0 rows
+//               scaled, then O -> bf16;
 //   warps 4-7   the state chain: S read-out (state outputs, S0 hi/lo, gamma_L S),
-//               R, the scaling of the Q S0 rows, U and U' hi/lo;
+//               R^T (one value column per thread), U and U' hi/lo;
 //   warps 8-11  the next chunk: gates and their prefix sums, l2 factors, A
 //               (to shared memory) and P (hi/lo in place in TMEM), then T by 32 x 32
 //               blocks: the two diagonal blocks by right-looking substitutions in
@@ -61,7 +64,8 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpOut = 2, kWarpChain = 4, kWarpPre
 constexpr int kLdA = kL + 4;  // fp32 row stride of A (float4 rows, conflict-free)
 constexpr uint64_t kWaitNs = 1000000000ull;
 // TMEM columns: S (128) | [K S0 ; Q S0] then O (128) | [KK^T ; QK^T] / P, two buffers (2 x 64) | U^T (64)
-constexpr uint32_t kColS = 0, kColKQ = 128, kColAP = 256, kColU = 384;
+// | (K S0)^T, then R^T hi/lo in place (64)
+constexpr uint32_t kColS = 0, kColKQ = 128, kColAP = 256, kColU = 384, kColKT = 448;
 
 struct GdnTcParams {
     int64_t T;
@@ -88,14 +92,14 @@ struct GdnVec {
 struct __align__(1024) GdnTcSmem {
     uint8_t kq[2][32768];  // per chunk: k-half h at h*16384: 64 K rows (8 KB) then 64 Q rows (8 KB)
     uint8_t s0[65536];     // S0 hi | lo [v-half][128 k rows][64 v]; then U' hi | lo [128 v rows][64 t]
-    uint8_t r[32768];      // R hi | lo [v-half][64 t rows][64 v]; then U hi | lo [128 v rows][64 s]
+    uint8_t r[32768];      // U hi | lo [128 v rows][64 s]
     uint8_t v[16384];      // V tile [v-half][64 t rows][64 v]
     uint8_t t[16384];      // T^T hi | lo [64 s rows][64 t]
     float a[kL * kLdA];    // A^T (row c = column c of A), fp32; rows 32..63, columns 0..31: T22^T
     float t11[32 * 33], m1[32 * 33], t21[32 * 33];  // blocks of T = (I + A)^-1, column-major
     GdnVec vec[2];
     uint64_t kq_full[2], kq_empty[2], ap_full[2], p_ready[2], vec_ready[2], vec2_ready[2], vec_free[2];
-    uint64_t v_full, v_empty, a_ready, inv1, inv2, inv3, t_ready, t_free, s0_copy, kqs0_full, r_ready, o_scaled,
+    uint64_t v_full, v_empty, a_ready, inv1, inv2, inv3, t_ready, t_free, s0_copy, kt_full, kqs0_full, r_ready, o_scaled,
         u_full, u_copy, s_ready, o_full, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -203,10 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             mbar_init(&s.p_ready[k], 4);
             mbar_init(&s.vec_ready[k], 4);
             mbar_init(&s.vec2_ready[k], 4);
-            mbar_init(&s.vec_free[k], 4);
+            mbar_init(&s.vec_free[k], 6);
         }
         mbar_init(&s.v_full, 1);
-        mbar_init(&s.v_empty, 2);
+        mbar_init(&s.v_empty, 4);
         mbar_init(&s.a_ready, 2);
         mbar_init(&s.inv1, 2);
         mbar_init(&s.inv2, 4);
@@ -214,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         mbar_init(&s.t_ready, 2);
         mbar_init(&s.t_free, 1);
         mbar_init(&s.s0_copy, 4);
+        mbar_init(&s.kt_full, 1);
         mbar_init(&s.kqs0_full, 1);
-        mbar_init(&s.r_ready, 2);
+        mbar_init(&s.r_ready, 4);
         mbar_init(&s.o_scaled, 2);
         mbar_init(&s.u_full, 1);
         mbar_init(&s.u_copy, 4);
@@ -272,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         if (lane == 0) {
             constexpr uint32_t i_kq = idesc_bf16_f32(128, 64, false, false);   // [K;Q] x K^T
             constexpr uint32_t i_ks = idesc_bf16_f32(128, 128, false, true);   // [K;Q] x S0 (MN-major)
-            constexpr uint32_t i_u = idesc_bf16_f32(128, 64, true, true);      // R^T (MN) x T^T (MN)
+            constexpr uint32_t i_kt = idesc_bf16_f32(128, 64, true, false);    // S0^T (MN) x K^T (K-major)
+            constexpr uint32_t i_u = idesc_bf16_f32(128, 64, false, true);     // R^T (TMEM) x T^T (MN)
             constexpr uint32_t i_s = idesc_bf16_f32(128, 128, true, false);    // K^T (MN) x U' (K-major)
             constexpr uint32_t i_o = idesc_bf16_f32(128, 128, false, false);   // P (TMEM) x U (K-major)
             // descriptors built once; + offset / 16 addresses further into a tile
@@ -283,10 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             }
             const uint64_t dS0 = sdesc_sw128(smem_u32(s.s0), 16384, 1024);  // MN-major, v-halves 16 KB apart
             const uint64_t dUp = sdesc_sw128(smem_u32(s.s0), 16, 1024);     // U': K-major, 128 v rows
-            const uint64_t dR = sdesc_sw128(smem_u32(s.r), 8192, 1024);     // R^T: MN-major, v-halves 8 KB apart
             const uint64_t dU = sdesc_sw128(smem_u32(s.r), 16, 1024);       // U: K-major, 128 v rows
             const uint64_t dT = sdesc_sw128(smem_u32(s.t), 16, 1024);       // T^T: MN-major, one 64-wide atom
-            const uint32_t tS = tbase + kColS, tKQ = tbase + kColKQ, tU = tbase + kColU;
+            const uint32_t tS = tbase + kColS, tKQ = tbase + kColKQ, tU = tbase + kColU, tKT = tbase + kColKT;
             bool ok = true;
             auto issue_kq = [&](uint32_t c) -> bool {
                 const int bb = c & 1;
@@ -304,8 +309,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             ok = issue_kq(0);
             for (uint32_t c = 0; ok && c < (uint32_t)nch; ++c) {
                 const int bb = c & 1;
-                // [K S0 ; Q S0], once S0 hi/lo is written and the last output rows were read
+                // (K S0)^T = S0^T K^T (v lanes: R^T is then formed by all four chain warps),
+                // once S0 hi/lo is written
                 if (!wait_bar(&s.s0_copy, par(c), abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ko = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        mma_ss(tKT, dS0 + ((uint32_t)(part * 32768 + kk * 2048) >> 4), dKQ[bb] + ko, i_kt,
+                               (part | kk) != 0);
+                    }
+                }
+                mma_commit(&s.kt_full);
+                // [K S0 ; Q S0] for the Q S0 rows of the output, once the last output rows were
+                // read (it runs while the chain forms R^T)
                 if (c >= 1 && !wait_bar(&s.o_free, par(c - 1), abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -318,16 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                     }
                 }
                 mma_commit(&s.kqs0_full);
-                // U^T = R^T T^T: hi.hi + hi.lo + lo.hi
+                // U^T = R^T T^T with R^T (hi/lo) read from TMEM: hi.hi + hi.lo + lo.hi
                 if (!wait_bar(&s.r_ready, par(c), abort_flag, err)) { ok = false; break; }
                 if (!wait_bar(&s.t_ready, par(c), abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t ro = pass == 2 ? 16384u : 0u, to = pass == 1 ? 8192u : 0u;
+                    const uint32_t ra = pass == 2 ? 8u : 0u, to = pass == 1 ? 8192u : 0u;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tU, dR + ((ro + kk * 2048) >> 4), dT + ((to + kk * 2048) >> 4), i_u, (pass | kk) != 0);
+                        mma_ts(tU, tKT + kk * 16 + ra, dT + ((to + kk * 2048) >> 4), i_u, (pass | kk) != 0);
                 }
                 mma_commit(&s.u_full);
                 mma_commit(&s.t_free);
@@ -335,8 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                 if (c + 1 < (uint32_t)nch && !issue_kq(c + 1)) { ok = false; break; }
                 // S += K^T U' (hi, lo), then O += P U onto the scaled Q S0 rows
                 if (!wait_bar(&s.u_copy, par(c), abort_flag, err)) { ok = false; break; }
-                if (!wait_bar(&s.p_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
-                if (!wait_bar(&s.o_scaled, par(c), abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
@@ -346,6 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
                                dUp + ((uint32_t)(part * 16384 + kk * 32) >> 4), i_s, 1u);
                 }
                 mma_commit(&s.s_ready);
+                if (!wait_bar(&s.p_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+                if (!wait_bar(&s.o_scaled, par(c), abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
                 const uint32_t tAP = tbase + kColAP + 64u * bb;
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
@@ -365,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         const int q = warp & 3;
         const int r = q * 32 + lane;  // TMEM lane: state row k / output row / value column v
         const uint32_t tl = (uint32_t)(q * 32) << 16;
-        const uint32_t tS = tbase + tl + kColS, tKQ = tbase + tl + kColKQ, tU = tbase + tl + kColU;
+        const uint32_t tS = tbase + tl + kColS, tU = tbase + tl + kColU, tKT = tbase + tl + kColKT;
         // export row of this request's first chunk: the chunks of the requests before it
         int64_t fc = 0;
         if (io.chunk_states) {
@@ -461,67 +481,45 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.s0_copy);
-            // ---- R = diag(beta) (V - diag(gamma rk) K S0); the Q S0 rows scaled by scale gamma rq
-            if (!wait_bar_warp(&s.kqs0_full, par(c), abort_flag, err)) { ok = false; break; }
+            // ---- R^T[v][t] = beta_t (V[t][v] - gamma_t rk_t (K S0)^T[v][t]) by all four warps
+            // (thread = value column v = r), written over (K S0)^T as bf16 hi/lo -- per
+            // 16-token block 8 hi then 8 lo columns -- the A operand of the U product
+            if (!wait_bar_warp(&s.kt_full, par(c), abort_flag, err)) { ok = false; break; }
+            if (!wait_bar_warp(&s.v_full, par(c), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
-            if (q < 2) {
-                if (!wait_bar_warp(&s.v_full, par(c), abort_flag, err)) { ok = false; break; }
-                const int t = r;
-                const float bt = vc.beta[t], w = vc.grk[t];
+            {
+                const uint8_t *vt = s.v + (r >> 6) * 8192;  // this column's v-half of the V tile
+                const uint32_t vch = (uint32_t)((r & 63) >> 3), vsub = (uint32_t)(r & 7) * 2;
 #pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t v[2][32];
-                    tmem_ld32(tKQ + c2 * 64, v[0]);
-                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint32_t v[16];
+                    tmem_ld16(tKT + kk * 16, v);
                     tmem_ld_wait();
-                    const uint8_t *vt = s.v + c2 * 8192;
-                    uint8_t *hb = s.r + c2 * 8192, *lb = hb + 16384;
+                    uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int ch8 = 0; ch8 < 8; ++ch8) {
-                        const uint32_t off = sw128_off((uint32_t)t, (uint32_t)ch8);
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(vt + off);
-                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float v0, v1;
-                            f2_get(f2_bf16x2(xw[e]), v0, v1);
-                            const float r0 = bt * (v0 - w * __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e]));
-                            const float r1 = bt * (v1 - w * __uint_as_float(v[ch8 >> 2][8 * (ch8 & 3) + 2 * e + 1]));
-                            split_pair(f2(r0, r1), hi[e], lo[e]);
-                        }
-                        *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4 *>(lb + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int e = 0; e < 8; ++e) {
+                        const int t = kk * 16 + 2 * e;
+                        const uint32_t x0 = *reinterpret_cast<const uint16_t *>(vt + t * 128 + ((vch ^ (uint32_t)(t & 7)) << 4) + vsub);
+                        const uint32_t x1 =
+                            *reinterpret_cast<const uint16_t *>(vt + (t + 1) * 128 + ((vch ^ (uint32_t)((t + 1) & 7)) << 4) + vsub);
+                        const float r0 = vc.beta[t] * (__uint_as_float(x0 << 16) - vc.grk[t] * __uint_as_float(v[2 * e]));
+                        const float r1 =
+                            vc.beta[t + 1] * (__uint_as_float(x1 << 16) - vc.grk[t + 1] * __uint_as_float(v[2 * e + 1]));
+                        split_pair(f2(r0, r1), hi[e], lo[e]);
                     }
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&s.v_empty);
-                    mbar_arrive(&s.r_ready);
-                }
-            } else {
-                const float wq = vc.osc[r - 64];
-#pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t v[2][32];
-                    tmem_ld32(tKQ + c2 * 64, v[0]);
-                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * wq);
-                        tmem_st32(tKQ + c2 * 64 + h * 32, v[h]);
-                    }
+                    tmem_st8(tKT + kk * 16, hi);
+                    tmem_st8(tKT + kk * 16 + 8, lo);
                 }
                 tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.o_scaled);
             }
-            // ---- U and U' = diag(rk e^{G_L - G}) U as hi/lo, row v = r: [v][s]
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s.v_empty);
+                mbar_arrive(&s.r_ready);
+            }
+            // ---- U and U' = diag(rk e^{G_L - G}) U as hi/lo, row v = r: [v][s] (U' over S0
+            // hi/lo: both products that read S0 were issued before U)
             if (!wait_bar_warp(&s.u_full, par(c), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             {
@@ -572,9 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         }
     } else if (warp == kWarpOut || warp == kWarpOut + 1) {
         // ------------------------------------------------------------ output rows
-        // O = rows 64..127 of the [K S0 ; Q S0] accumulator (warps 2, 3: TMEM lane
-        // quadrants 2, 3) -> bf16, so that the chain warps of those quadrants go on to
-        // the next chunk's state read-out meanwhile.
+        // Rows 64..127 of the [K S0 ; Q S0] accumulator (warps 2, 3: TMEM lane quadrants
+        // 2, 3): the Q S0 rows scaled by scale gamma rq, then, once P U has been added,
+        // O -> bf16; off the state chain, whose warps go on to the next chunk.
         const int q = warp & 3;
         const int t = (q - 2) * 32 + lane;  // token row of the chunk
         const uint32_t tKQ = tbase + ((uint32_t)(q * 32) << 16) + kColKQ;
@@ -584,6 +582,34 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_consta
         int n;
         bool ok = true;
         for (uint32_t c = 0; ok && ch.next(t0, n, ae); ++c) {
+            const int bb = c & 1;
+            // the Q S0 rows scaled by scale gamma rq before the P U product adds to them
+            if (!wait_bar_warp(&s.vec2_ready[bb], par(c >> 1), abort_flag, err)) { ok = false; break; }
+            if (!wait_bar_warp(&s.kqs0_full, par(c), abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            {
+                const float wq = s.vec[bb].osc[t];
+#pragma unroll 1
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tKQ + c2 * 64, v[0]);
+                    tmem_ld32(tKQ + c2 * 64 + 32, v[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * wq);
+                        tmem_st32(tKQ + c2 * 64 + h * 32, v[h]);
+                    }
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s.o_scaled);
+                mbar_arrive(&s.vec_free[bb]);
+            }
             if (!wait_bar_warp(&s.o_full, par(c), abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             __nv_bfloat16 *orow = og + ((size_t)(t0 + t) * p.Hv + hv) * kV;
