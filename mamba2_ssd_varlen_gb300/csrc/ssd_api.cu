@@ -34,11 +34,15 @@ static int check_dims(const ssd_dims *d) {
 
 // Tokens per work segment: long requests are cut into segments that CTAs walk
 // in parallel (the state chain between them is resolved by the forward path).
-// Batches of requests averaging at most 2048 tokens take 1024-token segments,
-// so that a batch has enough (segment, head) items to keep every SM busy to
-// the end; others 2048.
+// Batches of requests averaging at most 1024 tokens take 1024-token segments,
+// batches averaging up to 2048 tokens 768-token ones, others 2048: shorter
+// segments give a batch of mid-length requests more (segment, head) items, so
+// that fewer SMs sit idle while the last items finish (requests of 2048 tokens
+// in 1024-token halves leave most of the GPU idle for the last round of equal
+// items); every length is a multiple of the largest chunk size (256).
 static int32_t pick_seg_len(const ssd_dims *d) {
-    return d->T <= 2048LL * d->R ? 1024 : 2048;
+    if (d->T <= 1024LL * d->R) return 1024;
+    return d->T <= 2048LL * d->R ? 768 : 2048;
 }
 
 // The longest request the chained mode takes: its segments form one serial

@@ -132,6 +132,27 @@ def test_chained_segment_states(P):
     assert plan_mode(call) == MODE_CHAINED
 
 
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("H,mode", [(64, 1), (8, 0)])
+def test_mid_length_batch_768_token_segments(P, H, mode):
+    # Requests averaging between 1024 and 2048 tokens are cut into 768-token
+    # segments; resume offsets put segment, chunk and block boundaries (1024-token
+    # checkpoints, 256-token chunks) at different places.  With 64 heads the plan
+    # chains the segment states, with 8 (the longest request then outlasts a CTA's
+    # share of the work) it takes the pre-pass.  Every output of sampled requests
+    # and heads against the oracle.
+    spec = workloads.Spec("mid", H=H, P=P, N=128, G=4, chunk_size=256, dtype="bf16", has_D=True,
+                          has_z=True, init="all", pool_slots=120, final_slots=True, export_chunks=True,
+                          block_size=1024)
+    lengths = [2048, 1300, 1700, 900, 2048, 1536, 1100, 1900]
+    ncomp = [0, 256, 700, 0, 1024, 5, 0, 2047]
+    prob = workloads.make_problem(spec, seed=90 + P + H, device="cuda", lengths=lengths, num_computed=ncomp,
+                                  canary=0.5)
+    call = _sampled_check(prob, [0, 2, 5, 7], [0, 3, H - 1])
+    assert plan_mode(call) == (MODE_CHAINED if mode else MODE_PREPASS)
+    assert call.plan.seg_len == 768
+
+
 def test_long_request_uses_the_state_pre_pass():
     # One request far longer than the rest of the batch: chaining its segments
     # would make it one serial chain, so the plan computes the segment states
