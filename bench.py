@@ -47,7 +47,7 @@ GDN_METRIC = "gated delta rule varlen prefill tokens/s per layer (bf16, 1×GB300
 # in profiles/traffic.txt is valid only for this exact source.
 KERNEL_SOURCES = ["mamba2_ssd_varlen_gb300/csrc/ssd_pair.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_chunk_tc.cu",
                   "mamba2_ssd_varlen_gb300/csrc/tc_util.cuh", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
-                  "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh",
+                  "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh", "mamba2_ssd_varlen_gb300/csrc/pdl.cuh",
                   # how a batch is cut into segments decides the scan's traffic too
                   "mamba2_ssd_varlen_gb300/csrc/ssd_api.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_plan.cu"]
 

@@ -61,6 +61,7 @@
 #include <mutex>
 
 #include "sm100.cuh"
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 #include "tc_util.cuh"
 
@@ -336,7 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int Qi) {
     using Cfg = TcCfg<P>;
     using Smem = TcSmem<P>;
-    // The first kernel of a forward rewinds the scan's work ticket.
+    // The state-only pass is the first kernel of a forward: it waits for the plan
+    // (or the previous forward) before anything else; the scan waits after its
+    // shared-memory and TMEM set-up.
+    if (STATE_ONLY) pdl_wait();
     // The first kernel of a forward rewinds the scan's work ticket and counts the
     // forward (the chained mode's publication counters grow by one round per forward).
     if (STATE_ONLY && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -349,6 +353,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     // one segment: leave before setting up barriers and TMEM.
     if (STATE_ONLY && (p.hdr[kHdrNonFinal] == 0 || p.hdr[kHdrMode] == kModeChained)) return;
     if ((smem_u32(tc_smem) & 1023u) != 0) {
+        pdl_wait();
         if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
         return;
     }
@@ -403,6 +408,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (!STATE_ONLY) pdl_wait();  // the segment-state passes have finished
     const uint32_t tbase = s.tmem_base;
     const uint32_t n_work = (uint32_t)p.hdr[kHdrSegs] * (uint32_t)p.H;
 
@@ -1140,6 +1146,7 @@ __device__ void seg_pass_one(const FwdParams &p, int i, int hh, int chunk) {
 // Batches with no multi-segment and no empty request leave at once.
 template <int P>
 __global__ void __launch_bounds__(kSegPassThreads) seg_pass_kernel(const FwdParams p) {
+    pdl_wait();  // the segment states from zero are written
     if (p.hdr[kHdrSegs] == 0) return;  // the plan rejected the batch
     if (p.hdr[kHdrEmpty] == 0 && (p.hdr[kHdrNonFinal] == 0 || p.hdr[kHdrMode] == kModeChained)) return;
     constexpr int kChunks = P * 128 / kSegPassChunk;
@@ -1214,20 +1221,17 @@ cudaError_t launch_p(const FwdParams &p, int Qi, int64_t max_items, bool pair, c
     if (seg_state_supported(p)) {
         e = launch_seg_state(p, max_items, stream);
     } else {
-        ssd_chunk_tc_kernel<P, true><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
-        e = cudaGetLastError();
+        e = launch_after_prev(ssd_chunk_tc_kernel<P, true>, dim3(grid), dim3(kThreads), smem, stream, p, maps, Qi);
     }
     if (e != cudaSuccess) return e;
     constexpr int kPassChunks = P * 128 / kSegPassChunk;
     static_assert(P * 128 % kSegPassChunk == 0, "state elements must split into whole chunks");
     const int pass_grid =
         (int)std::max<int64_t>(1, std::min<int64_t>(seg_ctas * kPassChunks, 8LL * std::max(sms, 1)));
-    seg_pass_kernel<P><<<pass_grid, kSegPassThreads, 0, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_after_prev(seg_pass_kernel<P>, dim3(pass_grid), dim3(kSegPassThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
     if (pair) return launch_pair_scan(p, Qi, max_items, stream);
-    ssd_chunk_tc_kernel<P, false><<<grid, kThreads, smem, stream>>>(p, maps, Qi);
-    return cudaGetLastError();
+    return launch_after_prev(ssd_chunk_tc_kernel<P, false>, dim3(grid), dim3(kThreads), smem, stream, p, maps, Qi);
 }
 
 }  // namespace

@@ -45,6 +45,7 @@
 #include <mutex>
 
 #include "sm100.cuh"
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 #include "tc_util.cuh"
 
@@ -292,6 +293,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
     // The tiles need 1024-byte alignment (swizzle atoms); the dynamic shared
     // window starts there on this architecture.  Refuse to run otherwise.
     if ((smem_u32(pair_smem) & 1023u) != 0) {
+        pdl_wait();
         if (threadIdx.x == 0) atomicOr(p.hdr + kHdrErr, SSD_DEVERR_INTERNAL);
         return;
     }
@@ -336,6 +338,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();  // the segment-state passes have finished
     const uint32_t tbase = s.tmem_base;
     const uint32_t n_work = (uint32_t)p.hdr[kHdrSegs] * (uint32_t)(p.H >> 1);
 
@@ -1003,8 +1006,7 @@ cudaError_t launch_pair_scan(const FwdParams &p, int Qi, int64_t max_items, cuda
     }
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_items / 2));
-    ssd_pair_kernel<<<grid, kThreads, smem, stream>>>(p, maps, Qi);
-    return cudaGetLastError();
+    return launch_after_prev(ssd_pair_kernel, dim3(grid), dim3(kThreads), smem, stream, p, maps, Qi);
 }
 
 }  // namespace ssd

@@ -25,6 +25,7 @@
 // synchronisation.
 #include <algorithm>
 
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     int32_t *__restrict__ req_first_chunk = a.req_first_chunk;
     int32_t *__restrict__ req_first_seg = a.req_first_seg;
     Seg *__restrict__ segs = a.segs;
+    // the forward's first kernel may be scheduled now; it waits for this one
+    pdl_launch_dependents();
     __shared__ int s_err, s_empty, s_max_segs;
     __shared__ long long s_max_len;
     if (threadIdx.x == 0) {

@@ -42,6 +42,7 @@
 #include <mutex>
 
 #include "sm100.cuh"
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 #include "tc_util.cuh"
 
@@ -130,6 +131,7 @@ __device__ __forceinline__ bool next_item(const FwdParams &p, uint32_t &w, uint3
 __device__ __forceinline__ int pieces_of(int len) { return (len + kRows - 1) / kRows; }
 
 __global__ void __launch_bounds__(kThreads, 1) seg_state_kernel(const FwdParams p, const __grid_constant__ SegMaps maps) {
+    pdl_wait();  // the plan (or the previous forward) has finished
     // The first kernel of a forward rewinds the scan's work ticket and counts the
     // forward (the chained mode's publication counters grow by one round per forward).
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -507,8 +509,7 @@ cudaError_t launch_seg_state(const FwdParams &p, int64_t max_items, cudaStream_t
     }
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, max_items));
-    seg_state_kernel<<<grid, kThreads, smem, stream>>>(p, maps);
-    return cudaGetLastError();
+    return launch_after_prev(seg_state_kernel, dim3(grid), dim3(kThreads), smem, stream, p, maps);
 }
 
 }  // namespace ssd
