@@ -163,7 +163,15 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
 /* One SSD varlen prefill over the planned batch, launched on `stream`
  * (normally the plan's stream; another stream must be ordered after it).
  * Writes y and whichever state outputs are non-NULL.  Write slots must not
- * alias slots read in the same call. */
+ * alias slots read in the same call.
+ *
+ * Its kernels are programmatic dependent launches: each may become resident
+ * before the stream's previous kernel has finished, but waits
+ * (griddepcontrol.wait) for it, and for its writes to be visible, before
+ * touching global memory, so stream order holds as for plain launches.  The
+ * plan's kernel lets the next kernel on its stream be scheduled at its start;
+ * a caller kernel launched there with the same attribute must wait likewise.
+ * Both calls can be captured into a CUDA graph. */
 int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out,
                        cudaStream_t stream);
 
