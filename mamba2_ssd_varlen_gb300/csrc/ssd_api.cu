@@ -32,18 +32,31 @@ static int check_dims(const ssd_dims *d) {
     return SSD_OK;
 }
 
-// Tokens per work segment: long requests are cut into segments that CTAs walk
-// in parallel (the state chain between them is resolved by the forward path).
-// Batches of requests averaging at most 1024 tokens take 1024-token segments,
-// batches averaging up to 2048 tokens 768-token ones, others 2048: shorter
-// segments give a batch of mid-length requests more (segment, head) items, so
-// that fewer SMs sit idle while the last items finish (requests of 2048 tokens
-// in 1024-token halves leave most of the GPU idle for the last round of equal
-// items); every length is a multiple of the largest chunk size (256).
-static int32_t pick_seg_len(const ssd_dims *d) {
-    if (d->T <= 1024LL * d->R) return 1024;
-    return d->T <= 2048LL * d->R ? 768 : 2048;
+// How requests are cut into work segments, which CTAs walk in parallel (the
+// state chain between the segments of a request is resolved by the forward
+// path).  Every cut is at an absolute position that is a multiple of 256 (the
+// largest chunk size), every segment holds at most 2048 tokens.
+//   * Batches of requests averaging at most 1024 tokens: cuts at the multiples
+//     of 1024 (most requests stay one segment: few items, little start-up).
+//   * Averaging 1024-2048 tokens: tail-shortened segments (the plan's rule): a
+//     request ends with a short segment (129-384 tokens) and a 512-token one
+//     before it, the rest in segments of up to 2048, so that the last rounds of
+//     the schedule hold short items and the SMs finish together (a 2048-token
+//     request: 1280 + 512 + 256).
+//   * Longer requests on average: cuts at the multiples of 2048.
+constexpr int32_t kPlanTailSegs = 1;  // ssd_plan.flags bit: tail-shortened segments
+
+struct SegRule {
+    int32_t len;  // longest segment
+    bool tail;    // tail-shortened segments
+};
+
+static SegRule pick_seg_rule(const ssd_dims *d) {
+    if (d->T <= 1024LL * d->R) return {1024, false};
+    return {2048, d->T <= 2048LL * d->R};
 }
+
+static SegRule rule_of(const ssd_plan *plan) { return {plan->seg_len, (plan->flags & kPlanTailSegs) != 0}; }
 
 // The longest request the chained mode takes: its segments form one serial
 // chain per head, which must not outlast the work a CTA does anyway
@@ -56,23 +69,25 @@ static int64_t chain_max_len_of(const ssd_dims *d) {
     return d->T * (int64_t)d->H / (2LL * sms);
 }
 
-// Work segments of a batch, at most.  Every request has exactly one final
-// segment (an empty request one empty segment); its other segments end on a
-// multiple of seg_len strictly inside its positions (s, s + L - 1].  Such
-// boundaries number at most ceil((L - 1) / seg_len) per request, so over the
-// batch at most floor((T + R (seg_len - 2)) / seg_len); and as every segment
-// holds a token, at most T - 1.
-static int64_t nonfinal_segs_of(const ssd_dims *d, int32_t seg_len) {
-    const int64_t by_len = (d->T + (int64_t)d->R * (seg_len - 2)) / seg_len;
+// Work segments of a batch that are not the last of their request, at most.
+// Every request has exactly one final segment (an empty request one empty
+// segment).  Cut at the multiples of len, its other segments end on such a
+// multiple strictly inside its positions (s, s + L - 1]: at most
+// ceil((L - 1) / len) per request, so over the batch at most
+// floor((T + R (len - 2)) / len).  Tail-shortened, a request of L tokens has at
+// most ceil(L / 2048) head segments and two tail segments, so at most
+// (L + 4095) / 2048 that are not its last: over the batch at most
+// floor((T + 4095 R) / 2048).  As every segment holds a token, at most T - 1.
+static int64_t nonfinal_segs_of(const ssd_dims *d, SegRule rule) {
+    const int64_t by_len = rule.tail ? (d->T + 4095LL * d->R) / 2048
+                                     : (d->T + (int64_t)d->R * (rule.len - 2)) / rule.len;
     const int64_t by_tokens = d->T - 1;
     return std::max<int64_t>(0, std::min(by_len, by_tokens));
 }
 
-static int64_t max_segs_of(const ssd_dims *d, int32_t seg_len) {
-    return nonfinal_segs_of(d, seg_len) + d->R;
-}
+static int64_t max_segs_of(const ssd_dims *d, SegRule rule) { return nonfinal_segs_of(d, rule) + d->R; }
 
-static WsLayout layout_of(const ssd_dims *d, int32_t seg_len) {
+static WsLayout layout_of(const ssd_dims *d, SegRule rule) {
     WsLayout w{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -80,7 +95,7 @@ static WsLayout layout_of(const ssd_dims *d, int32_t seg_len) {
         off = align_up(off + bytes, 256);
         return o;
     };
-    const int64_t ms = max_segs_of(d, seg_len);
+    const int64_t ms = max_segs_of(d, rule);
     w.hdr = take(sizeof(int32_t) * kHdrInts);
     w.req_first_chunk = take(sizeof(int32_t) * ((size_t)d->R + 1));
     w.req_first_seg = take(sizeof(int32_t) * ((size_t)d->R + 1));
@@ -88,7 +103,7 @@ static WsLayout layout_of(const ssd_dims *d, int32_t seg_len) {
     w.seg_order = take(sizeof(int32_t) * (size_t)ms);
     // one state (and one decay per head) for each segment that is not the last of
     // its request, indexed compactly: segment k of request i uses entry k - i
-    const int64_t nf = nonfinal_segs_of(d, seg_len);
+    const int64_t nf = nonfinal_segs_of(d, rule);
     w.seg_state = take(sizeof(float) * (size_t)nf * d->H * d->P * d->N);
     w.seg_decay = take(sizeof(float) * (size_t)nf * d->H);
     w.seg_flags = take(sizeof(int32_t) * (size_t)nf * d->H);
@@ -121,7 +136,7 @@ static int forward_params(const ssd_plan *plan, const ssd_inputs *in, const ssd_
     if (uses_pool && (!in->state_pool || d->num_slots < 1)) return SSD_ERR_NULL;
     if (out->block_table && (d->block_size <= 0 || d->block_table_width < 1)) return SSD_ERR_BLOCK_SIZE;
 
-    const WsLayout w = layout_of(d, plan->seg_len);
+    const WsLayout w = layout_of(d, rule_of(plan));
     if (plan->workspace_bytes < w.total) return SSD_ERR_WORKSPACE;
     char *ws = static_cast<char *>(plan->workspace);
     p->T = d->T;
@@ -180,7 +195,7 @@ extern "C" {
 
 size_t ssd_varlen_workspace_size(const ssd_dims *dims) {
     if (check_dims(dims) != SSD_OK) return 0;
-    return layout_of(dims, pick_seg_len(dims)).total;
+    return layout_of(dims, pick_seg_rule(dims)).total;
 }
 
 int64_t ssd_varlen_count_chunks(const int32_t *cu, const int32_t *ncomp, int32_t R, int32_t Q) {
@@ -202,8 +217,8 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
     if (rc != SSD_OK) return rc;
     if (!cu_seqlens || !workspace || !out) return SSD_ERR_NULL;
     if (!aligned4(cu_seqlens) || (num_computed && !aligned4(num_computed))) return SSD_ERR_ALIGN;
-    const int32_t seg_len = pick_seg_len(dims);
-    const WsLayout w = layout_of(dims, seg_len);
+    const SegRule rule = pick_seg_rule(dims);
+    const WsLayout w = layout_of(dims, rule);
     if (!aligned16(workspace)) return SSD_ERR_WORKSPACE;
     if (workspace_bytes < w.total) return SSD_ERR_WORKSPACE;
     char *ws = static_cast<char *>(workspace);
@@ -213,9 +228,10 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
     a.R = dims->R;
     a.H = dims->H;
     a.Q = dims->chunk_size;
-    a.seg_len = seg_len;
+    a.seg_len = rule.len;
+    a.seg_tail = rule.tail ? 1 : 0;
     a.T = dims->T;
-    a.max_segs = max_segs_of(dims, seg_len);
+    a.max_segs = max_segs_of(dims, rule);
     a.chain_max_len = chain_max_len_of(dims);
     a.hdr = (int32_t *)(ws + w.hdr);
     a.req_first_chunk = (int32_t *)(ws + w.req_first_chunk);
@@ -232,8 +248,9 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
     out->cu_seqlens = cu_seqlens;
     out->num_computed = num_computed;
     out->max_chunks = (dims->T + dims->chunk_size - 1) / dims->chunk_size + dims->R;
-    out->max_segs = max_segs_of(dims, seg_len);
-    out->seg_len = seg_len;
+    out->max_segs = max_segs_of(dims, rule);
+    out->seg_len = rule.len;
+    out->flags = rule.tail ? kPlanTailSegs : 0;
     out->magic = kPlanMagic;
     out->stream = stream;
     return SSD_OK;
@@ -265,7 +282,7 @@ int ssd_varlen_forward_path(const ssd_plan *plan, const ssd_inputs *in, const ss
 int ssd_varlen_status(const ssd_plan *plan, int *device_err) {
     if (!plan || !device_err) return SSD_ERR_NULL;
     if (plan->magic != kPlanMagic) return SSD_ERR_PLAN;
-    const WsLayout w = layout_of(&plan->dims, plan->seg_len);
+    const WsLayout w = layout_of(&plan->dims, rule_of(plan));
     int32_t *hdr = (int32_t *)((char *)plan->workspace + w.hdr);
     // Only the plan's stream is synchronised (its work, then the read and the
     // clear, in stream order); other streams of the device keep running.

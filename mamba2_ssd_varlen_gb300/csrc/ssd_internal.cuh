@@ -98,6 +98,7 @@ __device__ __forceinline__ void set_err(int32_t *hdr, int bits) { atomicOr(hdr +
 struct PlanArgs {
     const int32_t *cu, *ncomp;
     int32_t R, H, Q, seg_len;
+    int32_t seg_tail;  // nonzero: tail-shortened segments (ssd_plan.cu), else cuts at multiples of seg_len
     int64_t T, max_segs;
     int64_t chain_max_len;  // longest request (tokens) the chained mode takes
     int32_t *hdr, *req_first_chunk, *req_first_seg;

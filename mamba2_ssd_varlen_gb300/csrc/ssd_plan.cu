@@ -7,8 +7,9 @@
 //   * req_first_chunk[i]: the request's first row in the chunk-state export
 //     (exclusive prefix sum of chunk counts; chunks cut at absolute multiples
 //     of chunk_size, so a resumed request's first chunk may be partial);
-//   * req_first_seg[i] and the segment list: runs of at most seg_len tokens,
-//     cut at absolute multiples of seg_len, that the forward kernels walk;
+//   * req_first_seg[i] and the segment list: runs of at most 2048 tokens that
+//     the forward kernels walk, cut at absolute multiples of seg_len or, for
+//     batches of mid-length requests, tail-shortened (SegCuts below);
 //   * how the state is carried from one segment of a request to the next, and
 //     the order in which the forward kernels take the segments (seg_order):
 //       chained: the kernel that finishes a segment publishes its end state,
@@ -68,17 +69,60 @@ __device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
 // Segments per request at most for the chained mode (one ordering pass each).
 constexpr int kMaxChainSegs = 16;
 
-__device__ __forceinline__ int segs_of(const int32_t *cu, const int32_t *ncomp, int i, int32_t seg_len) {
+// How a request at absolute positions [s, s + L), L >= 1, is cut into work
+// segments: segment k spans [lo(k), lo(k + 1)), lo(0) = s, lo(count()) = s + L.
+//   Multiples (tail false): cuts at the multiples of len strictly inside.
+//   Tail-shortened (tail true): the last segment starts at t1, the last multiple
+//   of 256 at least 129 tokens before the end (so it holds 129-384 tokens),
+//   provided t1 - s >= 256; the one before it at t2 = t1 - 512, provided
+//   t2 - s >= 512; the part before the first of these cuts, the head, is cut
+//   from its end backwards into n = ceil(length / 2048) segments of one stride,
+//   the smallest multiple of 256 not below length / n (the first segment takes
+//   the rest).  Every cut is a multiple of 256; every segment holds 1-2048 tokens.
+struct SegCuts {
+    int64_t s, e, head_end, stride, t1;
+    int32_t len;
+    int n_head, n_tail;
+    bool tail;
+    __device__ SegCuts(int64_t s_, int64_t L, int32_t len_, bool tail_)
+        : s(s_), e(s_ + L), head_end(s_ + L), stride(0), t1(0), len(len_), n_head(1), n_tail(0), tail(tail_) {
+        if (!tail) return;
+        if (L >= 385) {
+            t1 = (e - 129) / 256 * 256;
+            if (t1 - s >= 256) {
+                n_tail = t1 - 512 - s >= 512 ? 2 : 1;
+                head_end = n_tail == 2 ? t1 - 512 : t1;
+            }
+        }
+        const int64_t hlen = head_end - s;
+        n_head = (int)((hlen + 2047) / 2048);
+        stride = n_head > 1 ? ((hlen + n_head - 1) / n_head + 255) / 256 * 256 : hlen;
+    }
+    __device__ int count() const {
+        if (!tail) return (int)((e - 1) / len - s / len + 1);
+        return n_head + n_tail;
+    }
+    __device__ int64_t lo(int k) const {
+        if (k <= 0) return s;
+        if (k >= count()) return e;
+        if (!tail) return (s / len + k) * (int64_t)len;
+        if (k < n_head) return head_end - stride * (n_head - k);
+        return k == n_head ? head_end : t1;  // the tail cuts: head_end (t2 or t1), then t1
+    }
+};
+
+__device__ __forceinline__ int segs_of(const int32_t *cu, const int32_t *ncomp, int i, int32_t seg_len, bool tail) {
     const int64_t L = (int64_t)cu[i + 1] - cu[i];
     const int64_t s = ncomp ? (int64_t)ncomp[i] : 0;
     if (L <= 0) return 1;
-    return (int)((s + L - 1) / seg_len - s / seg_len + 1);
+    return SegCuts(s, L, seg_len, tail).count();
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     const int32_t *__restrict__ cu = a.cu;
     const int32_t *__restrict__ ncomp = a.ncomp;
     const int32_t R = a.R, Q = a.Q, seg_len = a.seg_len;
+    const bool tail = a.seg_tail != 0;
     const int64_t T = a.T;
     int32_t *hdr = a.hdr;
     int32_t *__restrict__ req_first_chunk = a.req_first_chunk;
@@ -108,7 +152,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
             if (s < 0 || s + L > 0x7fffffffLL) { err |= SSD_DEVERR_NUM_COMPUTED; s = 0; }
             if (L > 0) {
                 nc = (int)((s + L - 1) / Q - s / Q + 1);
-                ns = (int)((s + L - 1) / seg_len - s / seg_len + 1);
+                ns = SegCuts(s, L, seg_len, tail).count();
             } else {
                 ns = 1;  // an empty request still gets one (empty) segment: final = initial
                 ++n_empty;
@@ -167,7 +211,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
         for (int k = 0; k < maxk; ++k) {
             for (int b0 = 0; b0 < R; b0 += nt) {
                 const int i = b0 + threadIdx.x;
-                const int has = (i < R && segs_of(cu, ncomp, i, seg_len) > k) ? 1 : 0;
+                const int has = (i < R && segs_of(cu, ncomp, i, seg_len, tail) > k) ? 1 : 0;
                 int e1, e2, t1, t2;
                 block_scan2(has, 0, e1, e2, t1, t2);
                 if (has) a.seg_order[base + e1] = req_first_seg[i] + k;
@@ -188,10 +232,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
             segs[first] = Seg{i, (int32_t)a, 0, (int32_t)s};
             continue;
         }
-        const int64_t s0 = s / seg_len;
+        const SegCuts c(s, L, seg_len, tail);
         for (int k = 0; k < cnt; ++k) {
-            const int64_t lo = max(s, (s0 + k) * (int64_t)seg_len);
-            const int64_t hi = min(s + L, (s0 + k + 1) * (int64_t)seg_len);
+            const int64_t lo = c.lo(k), hi = c.lo(k + 1);
             segs[first + k] = Seg{i, (int32_t)(a + (lo - s)), (int32_t)(hi - lo), (int32_t)lo};
         }
     }

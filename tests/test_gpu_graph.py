@@ -44,7 +44,7 @@ def _same(a, b, what):
 
 @pytest.mark.parametrize("H,mode", [(64, MODE_CHAINED), (8, MODE_PREPASS)])
 def test_graph_replay_matches_direct_calls(H, mode):
-    # Requests of 900-2048 tokens with resume offsets (768-token segments, 256-token
+    # Requests of 900-2048 tokens with resume offsets (tail-shortened segments, 256-token
     # chunks exported, 1024-token block checkpoints, initial and final pool slots):
     # with 64 heads the scan chains the segment states itself, with 8 the pre-pass
     # and its chain kernel run first.

@@ -13,6 +13,7 @@ import torch
 
 import mamba2_ssd_varlen_gb300 as m
 import oracle
+import seg_rule
 import workloads
 from oracle import checkpoints
 
@@ -134,10 +135,11 @@ def test_chained_segment_states(P):
 
 @pytest.mark.parametrize("P", [64, 128])
 @pytest.mark.parametrize("H,mode", [(64, 1), (8, 0)])
-def test_mid_length_batch_768_token_segments(P, H, mode):
-    # Requests averaging between 1024 and 2048 tokens are cut into 768-token
-    # segments; resume offsets put segment, chunk and block boundaries (1024-token
-    # checkpoints, 256-token chunks) at different places.  With 64 heads the plan
+def test_mid_length_batch_tail_shortened_segments(P, H, mode):
+    # Requests averaging between 1024 and 2048 tokens are cut into tail-shortened
+    # segments (a 2048-token request: 1280 + 512 + 256); resume offsets put
+    # segment, chunk and block boundaries (1024-token checkpoints, 256-token
+    # chunks) at different places.  With 64 heads the plan
     # chains the segment states, with 8 (the longest request then outlasts a CTA's
     # share of the work) it takes the pre-pass.  Every output of sampled requests
     # and heads against the oracle.
@@ -150,7 +152,53 @@ def test_mid_length_batch_768_token_segments(P, H, mode):
                                   canary=0.5)
     call = _sampled_check(prob, [0, 2, 5, 7], [0, 3, H - 1])
     assert plan_mode(call) == (MODE_CHAINED if mode else MODE_PREPASS)
-    assert call.plan.seg_len == 768
+    assert call.plan.seg_len == 2048 and call.plan.flags & seg_rule.PLAN_TAIL_SEGS
+
+
+def plan_segments(call):
+    """(req_first_seg, segments) from the plan's workspace: the header (64 words),
+    then req_first_chunk and req_first_seg (R + 1 words each) and the segment
+    list (req, first token, length, absolute start), each region 256-byte aligned."""
+    R = call.dims.R
+    al = lambda v: (v + 255) // 256 * 256
+    off_rfs = al(256 + 4 * (R + 1))
+    off_segs = al(off_rfs + 4 * (R + 1))
+    ws = call.workspace
+    nsegs = int(ws[:64 * 4].view(torch.int32)[2].item())
+    rfs = ws[off_rfs:off_rfs + 4 * (R + 1)].view(torch.int32).cpu().tolist()
+    segs = ws[off_segs:off_segs + 16 * nsegs].view(torch.int32).view(-1, 4).cpu().tolist()
+    return rfs, segs
+
+
+@pytest.mark.parametrize("lengths,ncomp,rule", [
+    # mid-length (tail-shortened): a long request whose head is cut in three,
+    # resumes, a 1-token and a 300-token request
+    ([5000, 1100, 1500, 300, 2048, 600, 1700, 2600, 1, 1000], [0, 256, 700, 5, 1024, 0, 2047, 77, 3, 129],
+     (2048, True)),
+    # short on average: multiples of 1024
+    ([900, 300, 2500, 100], [0, 1000, 7, 0], (1024, False)),
+    # long on average: multiples of 2048
+    ([6000, 10], [100, 0], (2048, False)),
+])
+def test_plan_segments_follow_the_rule(lengths, ncomp, rule):
+    # The segment list the plan builds on the device, request by request, against
+    # the rule restated in seg_rule.py; sampled outputs against the oracle.
+    spec = workloads.Spec("segs", H=8, P=64, N=128, G=2, chunk_size=256, dtype="bf16", has_D=True,
+                          has_z=True, init="all", pool_slots=40, final_slots=True, export_chunks=True,
+                          block_size=1024)
+    prob = workloads.make_problem(spec, seed=500 + len(lengths), device="cuda", lengths=lengths, num_computed=ncomp)
+    assert seg_rule.rule_of(sum(lengths), len(lengths)) == rule
+    call = _sampled_check(prob, [0, len(lengths) - 1], [0, 7])
+    assert call.plan.seg_len == rule[0] and bool(call.plan.flags & seg_rule.PLAN_TAIL_SEGS) == rule[1]
+    rfs, segs = plan_segments(call)
+    cu = prob["cu_seqlens"].cpu().tolist()
+    for i, (L, s) in enumerate(zip(lengths, ncomp)):
+        mine = segs[rfs[i]:rfs[i + 1]]
+        assert all(sg[0] == i for sg in mine)
+        got = [mine[0][3]] + [sg[3] + sg[2] for sg in mine]
+        assert got == seg_rule.cuts(s, L, *rule), (i, got)
+        # first tokens are packed positions: request start + (absolute start - s)
+        assert [sg[1] for sg in mine] == [cu[i] + (c - s) for c in got[:-1]]
 
 
 def test_long_request_uses_the_state_pre_pass():
