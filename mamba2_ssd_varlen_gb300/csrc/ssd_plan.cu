@@ -203,10 +203,58 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     if (bad) return;  // forward kernels see zero segments and write nothing
     __syncthreads();
     // The order the forward kernels take the segments in: chained, the k-th
-    // segments of all requests (k = 0, 1, ...), each round in request order;
-    // otherwise the segment list itself.  Chained, the per-(segment, head)
-    // publication counters start from zero.
-    if (chained) {
+    // segments of all requests (k = 0, 1, ...), round by round; otherwise the
+    // segment list itself.  Within a round the requests with the most segments
+    // go first (their chains are the longest, and start first), ties in request
+    // order, when the batch fits one pass of the block; larger batches keep
+    // request order.  Chained, the per-(segment, head) publication counters
+    // start from zero.
+    if (chained && R <= nt) {
+        __shared__ int cnt_w[kPlanThreads / 32][kMaxChainSegs + 1];
+        __shared__ int bin_base[kMaxChainSegs + 1];
+        __shared__ int perm[kPlanThreads], segc[kPlanThreads];
+        const int t = threadIdx.x, lane = t & 31, w = t >> 5, nw = nt >> 5;
+        const int c = t < R ? segs_of(cu, ncomp, t, seg_len, tail) : 0;  // 1 .. maxk; 0: no request
+        for (int j = t; j < nw * (kMaxChainSegs + 1); j += nt) cnt_w[j / (kMaxChainSegs + 1)][j % (kMaxChainSegs + 1)] = 0;
+        segc[t] = c;
+        __syncthreads();
+        // the warp's requests with the same count, and how many of them come before this one
+        const unsigned same = __match_any_sync(0xffffffffu, c);
+        const int before = __popc(same & ((1u << lane) - 1u));
+        if (c > 0 && before == 0) cnt_w[w][c] = __popc(same);
+        __syncthreads();
+        if (t >= 1 && t <= kMaxChainSegs) {  // per count: exclusive prefix over the warps, total
+            int run = 0;
+            for (int ww = 0; ww < nw; ++ww) {
+                const int x = cnt_w[ww][t];
+                cnt_w[ww][t] = run;
+                run += x;
+            }
+            bin_base[t] = run;
+        }
+        __syncthreads();
+        if (t == 0) {  // counts from the largest down
+            int run = 0;
+            for (int v = kMaxChainSegs; v >= 1; --v) {
+                const int x = bin_base[v];
+                bin_base[v] = run;
+                run += x;
+            }
+        }
+        __syncthreads();
+        if (c > 0) perm[bin_base[c] + cnt_w[w][c] + before] = t;
+        __syncthreads();
+        const int ic = t < R ? perm[t] : 0;  // the request at place t of a round
+        const int cc = t < R ? segc[ic] : 0;
+        int base = 0;
+        for (int k = 0; k < maxk; ++k) {
+            const int has = cc > k ? 1 : 0;
+            int e1, e2, t1, t2;
+            block_scan2(has, 0, e1, e2, t1, t2);
+            if (has) a.seg_order[base + e1] = req_first_seg[ic] + k;
+            base += t1;
+        }
+    } else if (chained) {
         int base = 0;
         for (int k = 0; k < maxk; ++k) {
             for (int b0 = 0; b0 < R; b0 += nt) {
@@ -218,6 +266,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
                 base += t1;
             }
         }
+    }
+    if (chained) {
         const int64_t nflags = (int64_t)(carry_s - R) * a.H;
         for (int64_t j = threadIdx.x; j < nflags; j += nt) a.seg_flags[j] = 0;
     } else {

@@ -155,19 +155,46 @@ def test_mid_length_batch_tail_shortened_segments(P, H, mode):
     assert call.plan.seg_len == 2048 and call.plan.flags & seg_rule.PLAN_TAIL_SEGS
 
 
-def plan_segments(call):
-    """(req_first_seg, segments) from the plan's workspace: the header (64 words),
-    then req_first_chunk and req_first_seg (R + 1 words each) and the segment
-    list (req, first token, length, absolute start), each region 256-byte aligned."""
+def plan_segments(call, with_order=False):
+    """(req_first_seg, segments[, order]) from the plan's workspace: the header (64
+    words), then req_first_chunk and req_first_seg (R + 1 words each), the segment
+    list (req, first token, length, absolute start; plan.max_segs entries) and the
+    order the scan takes the segments in, each region 256-byte aligned."""
     R = call.dims.R
     al = lambda v: (v + 255) // 256 * 256
     off_rfs = al(256 + 4 * (R + 1))
     off_segs = al(off_rfs + 4 * (R + 1))
+    off_order = al(off_segs + 16 * call.plan.max_segs)
     ws = call.workspace
     nsegs = int(ws[:64 * 4].view(torch.int32)[2].item())
     rfs = ws[off_rfs:off_rfs + 4 * (R + 1)].view(torch.int32).cpu().tolist()
     segs = ws[off_segs:off_segs + 16 * nsegs].view(torch.int32).view(-1, 4).cpu().tolist()
-    return rfs, segs
+    if not with_order:
+        return rfs, segs
+    order = ws[off_order:off_order + 4 * nsegs].view(torch.int32).cpu().tolist()
+    return rfs, segs, order
+
+
+def test_chained_rounds_take_the_longest_chains_first():
+    # Chained mode on a batch whose requests have 1-4 segments (1024-token cuts):
+    # the scan takes every request's k-th segment after all (k-1)-th ones, and
+    # within a round the requests with more segments first, ties in request order.
+    spec = workloads.Spec("order", H=128, P=64, N=128, G=8, chunk_size=256, dtype="bf16", has_D=True,
+                          has_z=True, init="half_even", pool_slots=40, final_slots=True)
+    lengths = [2900, 100, 2100, 500, 1, 3300, 700, 1024, 50, 900, 300, 200]
+    ncomp = [0, 0, 300, 0, 0, 5, 1000, 0, 0, 200, 0, 0]
+    prob = workloads.make_problem(spec, seed=77, device="cuda", lengths=lengths, num_computed=ncomp)
+    call = _sampled_check(prob, [0, 5, 11], [0, 127])
+    assert plan_mode(call) == MODE_CHAINED
+    rfs, segs, order = plan_segments(call, with_order=True)
+    count = [rfs[i + 1] - rfs[i] for i in range(len(lengths))]
+    assert sorted(order) == list(range(len(segs)))
+    keys = []
+    for sid in order:
+        i = segs[sid][0]
+        keys.append((sid - rfs[i], -count[i], i))  # (round, longer chains first, request)
+    assert keys == sorted(keys), keys
+    assert max(count) == 4 and keys[0][2] == 5  # the 4-segment request opens the first round
 
 
 @pytest.mark.parametrize("lengths,ncomp,rule", [
