@@ -36,14 +36,13 @@ static int check_dims(const ssd_dims *d) {
 // state chain between the segments of a request is resolved by the forward
 // path).  Every cut is at an absolute position that is a multiple of 256 (the
 // largest chunk size), every segment holds at most 2048 tokens.
-//   * Batches of requests averaging at most 1024 tokens: cuts at the multiples
-//     of 1024 (most requests stay one segment: few items, little start-up).
-//   * Averaging 1024-2048 tokens: tail-shortened segments (the plan's rule): a
-//     request ends with a short segment (129-384 tokens) and a 512-token one
-//     before it, the rest in segments of up to 2048, so that the last rounds of
-//     the schedule hold short items and the SMs finish together (a 2048-token
-//     request: 1280 + 512 + 256).
-//   * Longer requests on average: cuts at the multiples of 2048.
+//   * Batches of requests averaging 1024-2048 tokens: tail-shortened segments
+//     (the plan's rule): a request ends with a short segment (129-384 tokens)
+//     and a 512-token one before it, the rest in segments of up to 2048, so that
+//     the last rounds of the schedule hold short items and the SMs finish
+//     together (a 2048-token request: 1280 + 512 + 256).
+//   * Others: cuts at the multiples of 2048 (few items, little start-up; the
+//     chained rounds take the longest chains first).
 constexpr int32_t kPlanTailSegs = 1;  // ssd_plan.flags bit: tail-shortened segments
 
 struct SegRule {
@@ -52,8 +51,7 @@ struct SegRule {
 };
 
 static SegRule pick_seg_rule(const ssd_dims *d) {
-    if (d->T <= 1024LL * d->R) return {1024, false};
-    return {2048, d->T <= 2048LL * d->R};
+    return {2048, d->T > 1024LL * d->R && d->T <= 2048LL * d->R};
 }
 
 static SegRule rule_of(const ssd_plan *plan) { return {plan->seg_len, (plan->flags & kPlanTailSegs) != 0}; }

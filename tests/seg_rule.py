@@ -2,8 +2,8 @@
 
 A request at absolute positions [s, s + L) is cut into work segments, given as
 their boundaries [s, c1, ..., e]:
-  * multiples of `len` (batches averaging at most 1024 tokens a request: len
-    1024; above 2048: len 2048): cuts at the multiples of len strictly inside;
+  * multiples of `len` (batches averaging at most 1024 or more than 2048 tokens
+    a request: len 2048): cuts at the multiples of len strictly inside;
   * tail-shortened (batches averaging 1024-2048 tokens): the last segment starts
     at t1, the last multiple of 256 at least 129 tokens before the end, if
     t1 - s >= 256; the one before at t2 = t1 - 512, if t2 - s >= 512; the head
@@ -38,6 +38,4 @@ def cuts(s, L, length, tail):
 
 def rule_of(T, R):
     """(len, tail) the plan picks for a batch of T tokens in R requests."""
-    if T <= 1024 * R:
-        return 1024, False
-    return 2048, T <= 2048 * R
+    return 2048, 1024 * R < T <= 2048 * R

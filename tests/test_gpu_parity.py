@@ -176,15 +176,15 @@ def plan_segments(call, with_order=False):
 
 
 def test_chained_rounds_take_the_longest_chains_first():
-    # Chained mode on a batch whose requests have 1-4 segments (1024-token cuts):
+    # Chained mode on a batch whose requests have 1-3 segments (2048-token cuts):
     # the scan takes every request's k-th segment after all (k-1)-th ones, and
     # within a round the requests with more segments first, ties in request order.
     spec = workloads.Spec("order", H=128, P=64, N=128, G=8, chunk_size=256, dtype="bf16", has_D=True,
                           has_z=True, init="half_even", pool_slots=40, final_slots=True)
-    lengths = [2900, 100, 2100, 500, 1, 3300, 700, 1024, 50, 900, 300, 200]
-    ncomp = [0, 0, 300, 0, 0, 5, 1000, 0, 0, 200, 0, 0]
+    lengths = [4100, 100, 2100, 500, 1, 5000, 700, 1024, 50, 900, 300, 200, 100, 100, 100, 100]
+    ncomp = [0, 0, 300, 0, 0, 5, 1000, 0, 0, 200, 0, 0, 0, 0, 0, 0]
     prob = workloads.make_problem(spec, seed=77, device="cuda", lengths=lengths, num_computed=ncomp)
-    call = _sampled_check(prob, [0, 5, 11], [0, 127])
+    call = _sampled_check(prob, [0, 5, 15], [0, 127])
     assert plan_mode(call) == MODE_CHAINED
     rfs, segs, order = plan_segments(call, with_order=True)
     count = [rfs[i + 1] - rfs[i] for i in range(len(lengths))]
@@ -194,7 +194,7 @@ def test_chained_rounds_take_the_longest_chains_first():
         i = segs[sid][0]
         keys.append((sid - rfs[i], -count[i], i))  # (round, longer chains first, request)
     assert keys == sorted(keys), keys
-    assert max(count) == 4 and keys[0][2] == 5  # the 4-segment request opens the first round
+    assert max(count) == 3 and [k[2] for k in keys[:3]] == [0, 5, 2]  # 3, 3, then 2 segments
 
 
 @pytest.mark.parametrize("lengths,ncomp,rule", [
@@ -202,8 +202,8 @@ def test_chained_rounds_take_the_longest_chains_first():
     # resumes, a 1-token and a 300-token request
     ([5000, 1100, 1500, 300, 2048, 600, 1700, 2600, 1, 1000], [0, 256, 700, 5, 1024, 0, 2047, 77, 3, 129],
      (2048, True)),
-    # short on average: multiples of 1024
-    ([900, 300, 2500, 100], [0, 1000, 7, 0], (1024, False)),
+    # short on average: multiples of 2048
+    ([900, 300, 2500, 100], [0, 1000, 7, 0], (2048, False)),
     # long on average: multiples of 2048
     ([6000, 10], [100, 0], (2048, False)),
 ])

@@ -34,7 +34,8 @@ def test_multiples_rule_cases():
 
 
 def test_rule_follows_the_average_request_length():
-    assert seg_rule.rule_of(8 * 1024, 8) == (1024, False)
+    assert seg_rule.rule_of(8 * 1024, 8) == (2048, False)
+    assert seg_rule.rule_of(8 * 1024 + 1, 8) == (2048, True)
     assert seg_rule.rule_of(8 * 2048, 8) == (2048, True)
     assert seg_rule.rule_of(8 * 2048 + 1, 8) == (2048, False)
 
@@ -42,7 +43,7 @@ def test_rule_follows_the_average_request_length():
 @pytest.mark.parametrize("tail", [True, False])
 def test_properties_over_random_requests(tail):
     rng = np.random.default_rng(7 if tail else 8)
-    length = 2048 if tail else 1024
+    length = 2048
     for _ in range(20000):
         s = int(rng.integers(0, 6000))
         L = int(rng.integers(1, 20000)) if rng.random() < 0.5 else int(rng.integers(1, 3000))
@@ -69,7 +70,7 @@ def test_workspace_bound_on_non_final_segments(tail):
         L = rng.integers(1, 5000, R)
         s = rng.integers(0, 3000, R)
         T = int(L.sum())
-        length = 2048 if tail else 1024
+        length = 2048
         nonfinal = sum(len(seg_rule.cuts(int(a), int(b), length, tail)) - 2 for a, b in zip(s, L))
         bound = (T + 4095 * R) // 2048 if tail else (T + R * (length - 2)) // length
         assert nonfinal <= min(bound, T - 1)
