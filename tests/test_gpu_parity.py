@@ -175,6 +175,31 @@ def plan_segments(call, with_order=False):
     return rfs, segs, order
 
 
+def test_more_requests_than_plan_threads():
+    # 1300 requests (the plan's CTA has at most 1024 threads, so every per-request
+    # pass loops): lengths 1-600 with every 97th request 2500 tokens long (two
+    # segments), chained.  The segment list against the rule, the order round by
+    # round in request order (batches past one pass of the block keep it), and
+    # sampled outputs against the oracle.
+    rng = np.random.default_rng(5)
+    R = 1300
+    lengths = [2500 if i % 97 == 3 else int(rng.integers(1, 600)) for i in range(R)]
+    ncomp = [int(rng.integers(0, 300)) if i % 5 == 0 else 0 for i in range(R)]
+    spec = workloads.Spec("many_req", H=8, P=64, N=128, G=2, chunk_size=128, dtype="bf16", has_D=True,
+                          has_z=True, init="half_even", pool_slots=2 * R, final_slots=True)
+    prob = workloads.make_problem(spec, seed=303, device="cuda", lengths=lengths, num_computed=ncomp)
+    rule = seg_rule.rule_of(sum(lengths), R)
+    assert rule == (2048, False)
+    call = _sampled_check(prob, [0, 3, 650, 1299], [0, 7])
+    assert plan_mode(call) == MODE_CHAINED
+    rfs, segs, order = plan_segments(call, with_order=True)
+    for i in range(R):
+        mine = segs[rfs[i]:rfs[i + 1]]
+        assert [mine[0][3]] + [sg[3] + sg[2] for sg in mine] == seg_rule.cuts(ncomp[i], lengths[i], *rule), i
+    keys = [(sid - rfs[segs[sid][0]], segs[sid][0]) for sid in order]
+    assert keys == sorted(keys) and len(keys) == len(segs)
+
+
 def test_chained_rounds_take_the_longest_chains_first():
     # Chained mode on a batch whose requests have 1-3 segments (2048-token cuts):
     # the scan takes every request's k-th segment after all (k-1)-th ones, and
@@ -206,6 +231,8 @@ def test_chained_rounds_take_the_longest_chains_first():
     ([900, 300, 2500, 100], [0, 1000, 7, 0], (2048, False)),
     # long on average: multiples of 2048
     ([6000, 10], [100, 0], (2048, False)),
+    # tail-shortened with an empty request (one empty segment: final = initial state)
+    ([2048, 0, 2048, 1500], [0, 0, 100, 7], (2048, True)),
 ])
 def test_plan_segments_follow_the_rule(lengths, ncomp, rule):
     # The segment list the plan builds on the device, request by request, against
