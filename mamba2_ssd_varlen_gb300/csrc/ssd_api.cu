@@ -41,8 +41,10 @@ static int check_dims(const ssd_dims *d) {
 //     and a 512-token one before it, the rest in segments of up to 2048, so that
 //     the last rounds of the schedule hold short items and the SMs finish
 //     together (a 2048-token request: 1280 + 512 + 256).
-//   * Others: cuts at the multiples of 2048 (few items, little start-up; the
-//     chained rounds take the longest chains first).
+//   * Others: cuts at the multiples of 2048 where the segment-state pre-pass is
+//     the two-head contraction (P = 64, N = 128, an even number of heads per
+//     group: its token weights hold 2048 tokens), 8192 otherwise -- few items,
+//     little start-up; the chained rounds take the longest chains first.
 constexpr int32_t kPlanTailSegs = 1;  // ssd_plan.flags bit: tail-shortened segments
 
 struct SegRule {
@@ -51,7 +53,9 @@ struct SegRule {
 };
 
 static SegRule pick_seg_rule(const ssd_dims *d) {
-    return {2048, d->T > 1024LL * d->R && d->T <= 2048LL * d->R};
+    if (d->T > 1024LL * d->R && d->T <= 2048LL * d->R) return {2048, true};
+    const bool two_head_prepass = d->P == 64 && d->N == 128 && d->G > 0 && (d->H / d->G) % 2 == 0;
+    return {two_head_prepass ? 2048 : 8192, false};
 }
 
 static SegRule rule_of(const ssd_plan *plan) { return {plan->seg_len, (plan->flags & kPlanTailSegs) != 0}; }

@@ -3,7 +3,9 @@
 A request at absolute positions [s, s + L) is cut into work segments, given as
 their boundaries [s, c1, ..., e]:
   * multiples of `len` (batches averaging at most 1024 or more than 2048 tokens
-    a request: len 2048): cuts at the multiples of len strictly inside;
+    a request: len 2048 when the segment-state pre-pass is the two-head kernel --
+    P = 64, N = 128, an even number of heads per group -- else 8192): cuts at the
+    multiples of len strictly inside;
   * tail-shortened (batches averaging 1024-2048 tokens): the last segment starts
     at t1, the last multiple of 256 at least 129 tokens before the end, if
     t1 - s >= 256; the one before at t2 = t1 - 512, if t2 - s >= 512; the head
@@ -36,6 +38,9 @@ def cuts(s, L, length, tail):
     return [s] + [head_end - stride * (n - k) for k in range(1, n)] + tail_cuts + [e]
 
 
-def rule_of(T, R):
+def rule_of(T, R, P=64, N=128, H=2, G=1):
     """(len, tail) the plan picks for a batch of T tokens in R requests."""
-    return 2048, 1024 * R < T <= 2048 * R
+    if 1024 * R < T <= 2048 * R:
+        return 2048, True
+    two_head_prepass = P == 64 and N == 128 and (H // G) % 2 == 0
+    return (2048 if two_head_prepass else 8192), False

@@ -116,8 +116,9 @@ def plan_mode(call):
 
 @pytest.mark.parametrize("P", [64, 128])
 def test_chained_segment_states(P):
-    # Twelve requests of 2000-2600 tokens, most crossing a 2048-token segment
-    # boundary (some from a resume offset), none long next to the batch: the
+    # Twelve requests of 2000-2600 tokens, most crossing a segment boundary
+    # (2048 tokens, 8192 on the one-head path; some from a resume offset), none
+    # long next to the batch: the
     # plan chains the segment states through the workspace -- the CTA that ends
     # a segment publishes its state, the one running the next segment picks it
     # up -- with no state pre-pass.  Every output of sampled requests and heads
@@ -127,6 +128,9 @@ def test_chained_segment_states(P):
                           block_size=256)
     lengths = [2600, 2100, 2500, 2300, 2450, 2000, 2550, 2200, 2350, 2400, 2150, 2250]
     ncomp = [0, 100, 1500, 0, 40, 2047, 0, 1000, 7, 0, 300, 1]
+    if P == 128:
+        # the one-head path cuts at multiples of 8192: resume just below one
+        ncomp = [c + 6144 for c in ncomp]
     prob = workloads.make_problem(spec, seed=61 + P, device="cuda", lengths=lengths, num_computed=ncomp,
                                   canary=0.75)
     call = _sampled_check(prob, [0, 2, 5, 7, 11], [0, 13, 31])
@@ -188,7 +192,7 @@ def test_more_requests_than_plan_threads():
     spec = workloads.Spec("many_req", H=8, P=64, N=128, G=2, chunk_size=128, dtype="bf16", has_D=True,
                           has_z=True, init="half_even", pool_slots=2 * R, final_slots=True)
     prob = workloads.make_problem(spec, seed=303, device="cuda", lengths=lengths, num_computed=ncomp)
-    rule = seg_rule.rule_of(sum(lengths), R)
+    rule = seg_rule.rule_of(sum(lengths), R, P=64, H=8, G=2)
     assert rule == (2048, False)
     call = _sampled_check(prob, [0, 3, 650, 1299], [0, 7])
     assert plan_mode(call) == MODE_CHAINED
@@ -222,26 +226,28 @@ def test_chained_rounds_take_the_longest_chains_first():
     assert max(count) == 3 and [k[2] for k in keys[:3]] == [0, 5, 2]  # 3, 3, then 2 segments
 
 
-@pytest.mark.parametrize("lengths,ncomp,rule", [
+@pytest.mark.parametrize("lengths,ncomp,P,rule", [
     # mid-length (tail-shortened): a long request whose head is cut in three,
     # resumes, a 1-token and a 300-token request
     ([5000, 1100, 1500, 300, 2048, 600, 1700, 2600, 1, 1000], [0, 256, 700, 5, 1024, 0, 2047, 77, 3, 129],
-     (2048, True)),
+     64, (2048, True)),
     # short on average: multiples of 2048
-    ([900, 300, 2500, 100], [0, 1000, 7, 0], (2048, False)),
+    ([900, 300, 2500, 100], [0, 1000, 7, 0], 64, (2048, False)),
     # long on average: multiples of 2048
-    ([6000, 10], [100, 0], (2048, False)),
+    ([6000, 10], [100, 0], 64, (2048, False)),
     # tail-shortened with an empty request (one empty segment: final = initial state)
-    ([2048, 0, 2048, 1500], [0, 0, 100, 7], (2048, True)),
+    ([2048, 0, 2048, 1500], [0, 0, 100, 7], 64, (2048, True)),
+    # the one-head path, long on average: multiples of 8192
+    ([9000, 3000, 17000], [0, 100, 5000], 128, (8192, False)),
 ])
-def test_plan_segments_follow_the_rule(lengths, ncomp, rule):
+def test_plan_segments_follow_the_rule(lengths, ncomp, P, rule):
     # The segment list the plan builds on the device, request by request, against
     # the rule restated in seg_rule.py; sampled outputs against the oracle.
-    spec = workloads.Spec("segs", H=8, P=64, N=128, G=2, chunk_size=256, dtype="bf16", has_D=True,
+    spec = workloads.Spec("segs", H=8, P=P, N=128, G=2, chunk_size=256, dtype="bf16", has_D=True,
                           has_z=True, init="all", pool_slots=40, final_slots=True, export_chunks=True,
                           block_size=1024)
     prob = workloads.make_problem(spec, seed=500 + len(lengths), device="cuda", lengths=lengths, num_computed=ncomp)
-    assert seg_rule.rule_of(sum(lengths), len(lengths)) == rule
+    assert seg_rule.rule_of(sum(lengths), len(lengths), P=P, H=8, G=2) == rule
     call = _sampled_check(prob, [0, len(lengths) - 1], [0, 7])
     assert call.plan.seg_len == rule[0] and bool(call.plan.flags & seg_rule.PLAN_TAIL_SEGS) == rule[1]
     rfs, segs = plan_segments(call)

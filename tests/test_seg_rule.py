@@ -38,6 +38,11 @@ def test_rule_follows_the_average_request_length():
     assert seg_rule.rule_of(8 * 1024 + 1, 8) == (2048, True)
     assert seg_rule.rule_of(8 * 2048, 8) == (2048, True)
     assert seg_rule.rule_of(8 * 2048 + 1, 8) == (2048, False)
+    # the one-head path (P = 128, or an odd number of heads per group) has no
+    # 2048-token pre-pass limit
+    assert seg_rule.rule_of(8 * 4000, 8, P=128) == (8192, False)
+    assert seg_rule.rule_of(8 * 4000, 8, P=64, H=6, G=2) == (8192, False)
+    assert seg_rule.rule_of(8 * 1500, 8, P=128) == (2048, True)
 
 
 @pytest.mark.parametrize("tail", [True, False])
