@@ -68,6 +68,9 @@ __device__ void block_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb) {
 
 // Segments per request at most for the chained mode (one ordering pass each).
 constexpr int kMaxChainSegs = 16;
+// Batches of at most this many requests rank them by segment count and length
+// (each thread counts over all of them); larger ones by segment count only.
+constexpr int kRankByLength = 256;
 
 // How a request at absolute positions [s, s + L), L >= 1, is cut into work
 // segments: segment k spans [lo(k), lo(k + 1)), lo(0) = s, lo(count()) = s + L.
@@ -205,18 +208,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     // The order the forward kernels take the segments in: chained, the k-th
     // segments of all requests (k = 0, 1, ...), round by round; otherwise the
     // segment list itself.  Within a round the requests with the most segments
-    // go first (their chains are the longest, and start first), ties in request
-    // order, when the batch fits one pass of the block; larger batches keep
-    // request order.  Chained, the per-(segment, head) publication counters
-    // start from zero.
+    // go first (their chains are the longest, and start first) and, among
+    // those, the longest (the longest items first: the last ones to finish are
+    // short), ties in request order -- by segment count alone past
+    // kRankByLength requests; batches past one pass of the block keep request
+    // order.  Chained, the per-(segment, head) publication counters start from
+    // zero.
     if (chained && R <= nt) {
         __shared__ int cnt_w[kPlanThreads / 32][kMaxChainSegs + 1];
         __shared__ int bin_base[kMaxChainSegs + 1];
-        __shared__ int perm[kPlanThreads], segc[kPlanThreads];
+        __shared__ int perm[kPlanThreads], segc[kPlanThreads], lens[kPlanThreads];
         const int t = threadIdx.x, lane = t & 31, w = t >> 5, nw = nt >> 5;
         const int c = t < R ? segs_of(cu, ncomp, t, seg_len, tail) : 0;  // 1 .. maxk; 0: no request
+        const int len_t = t < R ? cu[t + 1] - cu[t] : 0;
         for (int j = t; j < nw * (kMaxChainSegs + 1); j += nt) cnt_w[j / (kMaxChainSegs + 1)][j % (kMaxChainSegs + 1)] = 0;
         segc[t] = c;
+        lens[t] = len_t;
         __syncthreads();
         // the warp's requests with the same count, and how many of them come before this one
         const unsigned same = __match_any_sync(0xffffffffu, c);
@@ -242,7 +249,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
             }
         }
         __syncthreads();
-        if (c > 0) perm[bin_base[c] + cnt_w[w][c] + before] = t;
+        if (R <= kRankByLength) {
+            if (t < R) {  // place = the requests ahead of this one
+                int place = 0;
+                for (int j = 0; j < R; ++j) {
+                    const int cj = segc[j], lj = lens[j];
+                    place += (cj > c || (cj == c && (lj > len_t || (lj == len_t && j < t)))) ? 1 : 0;
+                }
+                perm[place] = t;
+            }
+        } else if (c > 0) {
+            perm[bin_base[c] + cnt_w[w][c] + before] = t;
+        }
         __syncthreads();
         const int ic = t < R ? perm[t] : 0;  // the request at place t of a round
         const int cc = t < R ? segc[ic] : 0;

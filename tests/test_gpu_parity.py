@@ -179,14 +179,14 @@ def plan_segments(call, with_order=False):
     return rfs, segs, order
 
 
-def test_more_requests_than_plan_threads():
-    # 1300 requests (the plan's CTA has at most 1024 threads, so every per-request
-    # pass loops): lengths 1-600 with every 97th request 2500 tokens long (two
-    # segments), chained.  The segment list against the rule, the order round by
-    # round in request order (batches past one pass of the block keep it), and
+@pytest.mark.parametrize("R", [400, 1300])
+def test_many_requests(R):
+    # 400 requests (ranked by segment count alone) and 1300 (the plan's CTA has
+    # at most 1024 threads, so every per-request pass loops; request order):
+    # lengths 1-600 with every 97th request 2500 tokens long (two segments),
+    # chained.  The segment list against the rule, the order round by round, and
     # sampled outputs against the oracle.
     rng = np.random.default_rng(5)
-    R = 1300
     lengths = [2500 if i % 97 == 3 else int(rng.integers(1, 600)) for i in range(R)]
     ncomp = [int(rng.integers(0, 300)) if i % 5 == 0 else 0 for i in range(R)]
     spec = workloads.Spec("many_req", H=8, P=64, N=128, G=2, chunk_size=128, dtype="bf16", has_D=True,
@@ -194,20 +194,25 @@ def test_more_requests_than_plan_threads():
     prob = workloads.make_problem(spec, seed=303, device="cuda", lengths=lengths, num_computed=ncomp)
     rule = seg_rule.rule_of(sum(lengths), R, P=64, H=8, G=2)
     assert rule == (2048, False)
-    call = _sampled_check(prob, [0, 3, 650, 1299], [0, 7])
+    call = _sampled_check(prob, [0, 3, R // 2, R - 1], [0, 7])
     assert plan_mode(call) == MODE_CHAINED
     rfs, segs, order = plan_segments(call, with_order=True)
     for i in range(R):
         mine = segs[rfs[i]:rfs[i + 1]]
         assert [mine[0][3]] + [sg[3] + sg[2] for sg in mine] == seg_rule.cuts(ncomp[i], lengths[i], *rule), i
-    keys = [(sid - rfs[segs[sid][0]], segs[sid][0]) for sid in order]
+    count = [rfs[i + 1] - rfs[i] for i in range(R)]
+    if R <= 1024:  # round, more segments first, then request order
+        keys = [(sid - rfs[segs[sid][0]], -count[segs[sid][0]], segs[sid][0]) for sid in order]
+    else:  # round, then request order
+        keys = [(sid - rfs[segs[sid][0]], segs[sid][0]) for sid in order]
     assert keys == sorted(keys) and len(keys) == len(segs)
 
 
 def test_chained_rounds_take_the_longest_chains_first():
     # Chained mode on a batch whose requests have 1-3 segments (2048-token cuts):
     # the scan takes every request's k-th segment after all (k-1)-th ones, and
-    # within a round the requests with more segments first, ties in request order.
+    # within a round the requests with more segments first, then the longer ones,
+    # ties in request order.
     spec = workloads.Spec("order", H=128, P=64, N=128, G=8, chunk_size=256, dtype="bf16", has_D=True,
                           has_z=True, init="half_even", pool_slots=40, final_slots=True)
     lengths = [4100, 100, 2100, 500, 1, 5000, 700, 1024, 50, 900, 300, 200, 100, 100, 100, 100]
@@ -221,9 +226,9 @@ def test_chained_rounds_take_the_longest_chains_first():
     keys = []
     for sid in order:
         i = segs[sid][0]
-        keys.append((sid - rfs[i], -count[i], i))  # (round, longer chains first, request)
+        keys.append((sid - rfs[i], -count[i], -lengths[i], i))  # (round, longer chains, longer, request)
     assert keys == sorted(keys), keys
-    assert max(count) == 3 and [k[2] for k in keys[:3]] == [0, 5, 2]  # 3, 3, then 2 segments
+    assert max(count) == 3 and [k[3] for k in keys[:3]] == [5, 0, 2]  # 3 (5000 tokens), 3, then 2 segments
 
 
 @pytest.mark.parametrize("lengths,ncomp,P,rule", [
