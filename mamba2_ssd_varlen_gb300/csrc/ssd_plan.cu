@@ -221,35 +221,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
         const int t = threadIdx.x, lane = t & 31, w = t >> 5, nw = nt >> 5;
         const int c = t < R ? segs_of(cu, ncomp, t, seg_len, tail) : 0;  // 1 .. maxk; 0: no request
         const int len_t = t < R ? cu[t + 1] - cu[t] : 0;
-        for (int j = t; j < nw * (kMaxChainSegs + 1); j += nt) cnt_w[j / (kMaxChainSegs + 1)][j % (kMaxChainSegs + 1)] = 0;
         segc[t] = c;
         lens[t] = len_t;
-        __syncthreads();
-        // the warp's requests with the same count, and how many of them come before this one
-        const unsigned same = __match_any_sync(0xffffffffu, c);
-        const int before = __popc(same & ((1u << lane) - 1u));
-        if (c > 0 && before == 0) cnt_w[w][c] = __popc(same);
-        __syncthreads();
-        if (t >= 1 && t <= kMaxChainSegs) {  // per count: exclusive prefix over the warps, total
-            int run = 0;
-            for (int ww = 0; ww < nw; ++ww) {
-                const int x = cnt_w[ww][t];
-                cnt_w[ww][t] = run;
-                run += x;
-            }
-            bin_base[t] = run;
-        }
-        __syncthreads();
-        if (t == 0) {  // counts from the largest down
-            int run = 0;
-            for (int v = kMaxChainSegs; v >= 1; --v) {
-                const int x = bin_base[v];
-                bin_base[v] = run;
-                run += x;
-            }
-        }
-        __syncthreads();
         if (R <= kRankByLength) {
+            __syncthreads();
             if (t < R) {  // place = the requests ahead of this one
                 int place = 0;
                 for (int j = 0; j < R; ++j) {
@@ -258,8 +233,36 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
                 }
                 perm[place] = t;
             }
-        } else if (c > 0) {
-            perm[bin_base[c] + cnt_w[w][c] + before] = t;
+        } else {
+            // stable counting sort by segment count: the warp's requests with the
+            // same count and how many of them come before this one, then per count
+            // an exclusive prefix over the warps, then the counts from the largest down
+            for (int j = t; j < nw * (kMaxChainSegs + 1); j += nt) cnt_w[j / (kMaxChainSegs + 1)][j % (kMaxChainSegs + 1)] = 0;
+            __syncthreads();
+            const unsigned same = __match_any_sync(0xffffffffu, c);
+            const int before = __popc(same & ((1u << lane) - 1u));
+            if (c > 0 && before == 0) cnt_w[w][c] = __popc(same);
+            __syncthreads();
+            if (t >= 1 && t <= kMaxChainSegs) {
+                int run = 0;
+                for (int ww = 0; ww < nw; ++ww) {
+                    const int x = cnt_w[ww][t];
+                    cnt_w[ww][t] = run;
+                    run += x;
+                }
+                bin_base[t] = run;
+            }
+            __syncthreads();
+            if (t == 0) {
+                int run = 0;
+                for (int v = kMaxChainSegs; v >= 1; --v) {
+                    const int x = bin_base[v];
+                    bin_base[v] = run;
+                    run += x;
+                }
+            }
+            __syncthreads();
+            if (c > 0) perm[bin_base[c] + cnt_w[w][c] + before] = t;
         }
         __syncthreads();
         const int ic = t < R ? perm[t] : 0;  // the request at place t of a round
