@@ -737,13 +737,45 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
             // H in TMEM (thread r: state column n = r) and its bf16 hi/lo copy for
             // the first y_inter.  The previous item's last state MMA and y_inter
             // have completed (waited for below), so both are free.
-#pragma unroll 1
-            for (int cs = 0; cs < kP; cs += 16) {
-                uint32_t v[16];
+            if (src) {
+                // the state (p rows of 128 floats, 32 KB) into the h^T tiles with one round of
+                // 16-byte loads by the slot's 128 threads (rows 0-31 to the hi tile, 32-63 to the
+                // lo tile); then all of it into H, and -- once every thread has read its
+                // column -- the hi/lo copy in place
+                const float4 *src4 = reinterpret_cast<const float4 *>(src);
+                float4 v4[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = src ? __float_as_uint(src[(size_t)(cs + e) * 128 + r]) : 0u;
-                tmem_st16(tH + cs, v);
-                write_h_copy16(hh_t, hl_t, r, cs, v);
+                for (int i = 0; i < 16; ++i) v4[i] = __ldg(src4 + i * 128 + r);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    reinterpret_cast<float4 *>(i < 8 ? hh_t : hl_t)[(i & 7) * 128 + r] = v4[i];
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + k) : "memory");
+#pragma unroll 1
+                for (int cs = 0; cs < kP; cs += 16) {
+                    const float *raw = reinterpret_cast<const float *>(cs < 32 ? hh_t : hl_t) + (size_t)(cs & 31) * 128;
+                    uint32_t v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(raw[(size_t)e * 128 + r]);
+                    tmem_st16(tH + cs, v);
+                }
+                tmem_st_wait();
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + k) : "memory");
+#pragma unroll 1
+                for (int cs = 0; cs < kP; cs += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tH + cs, v);
+                    tmem_ld_wait();
+                    write_h_copy16(hh_t, hl_t, r, cs, v);
+                }
+            } else {
+#pragma unroll 1
+                for (int cs = 0; cs < kP; cs += 16) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = 0u;
+                    tmem_st16(tH + cs, v);
+                    write_h_copy16(hh_t, hl_t, r, cs, v);
+                }
             }
             tmem_st_wait();
             fence_async_smem();
