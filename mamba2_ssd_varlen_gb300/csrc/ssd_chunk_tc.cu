@@ -137,6 +137,10 @@ SSD_TILE_ALIGNED(64, b); SSD_TILE_ALIGNED(64, c); SSD_TILE_ALIGNED(64, xd_hi); S
 SSD_TILE_ALIGNED(64, h_hi); SSD_TILE_ALIGNED(64, h_lo); SSD_TILE_ALIGNED(64, z); SSD_TILE_ALIGNED(64, ystage);
 SSD_TILE_ALIGNED(128, b); SSD_TILE_ALIGNED(128, c); SSD_TILE_ALIGNED(128, xd_hi); SSD_TILE_ALIGNED(128, xd_lo);
 SSD_TILE_ALIGNED(128, h_hi); SSD_TILE_ALIGNED(128, h_lo);
+// the h^T tiles also take a raw (P, 128) fp32 state, as one region
+static_assert(offsetof(TcSmem<64>, h_lo) == offsetof(TcSmem<64>, h_hi) + 128 * 64 * 2, "h^T tiles not adjacent");
+static_assert(offsetof(TcSmem<128>, h_lo) == offsetof(TcSmem<128>, h_hi) + 128 * 128 * 2, "h^T tiles not adjacent");
+static_assert(kWarpBC == 18, "G2 is warps 10-17 (its eight warps share the entering-state load)");
 static_assert(sizeof(TcSmem<64>) <= 232448, "P = 64 tiles exceed the 227 KB shared-memory limit");
 static_assert(sizeof(TcSmem<128>) <= 232448, "P = 128 tiles exceed the 227 KB shared-memory limit");
 #undef SSD_TILE_ALIGNED
@@ -785,13 +789,47 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 }
             }
             // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
-#pragma unroll 1
-            for (int cs = c0; cs < c0 + kHalf; cs += 16) {
-                uint32_t v[16];
+            if (!STATE_ONLY && src) {
+                // The state (P rows of 128 floats) into the h^T tiles (hi then lo, one
+                // region of P * 512 bytes) with one round of 16-byte loads by the eight
+                // warps; then this warp's columns into TMEM and -- once every warp has
+                // read its columns -- the hi/lo copy in place.
+                constexpr int kVec = P * 32 / 256;  // float4 per thread
+                const int g = (warp - 10) * 32 + lane;
+                const float4 *src4 = reinterpret_cast<const float4 *>(src);
+                float4 *raw4 = reinterpret_cast<float4 *>(s.h_hi);
+                float4 v4[kVec];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = src ? __float_as_uint(src[(size_t)(cs + k) * 128 + r]) : 0u;
-                tmem_st16(tl + Cfg::kColH + cs, v);
-                if (!STATE_ONLY) write_h_copy16<P>(s, r, cs, v);
+                for (int i = 0; i < kVec; ++i) v4[i] = __ldg(src4 + i * 256 + g);
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) raw4[i * 256 + g] = v4[i];
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                const float *raw = reinterpret_cast<const float *>(s.h_hi);
+#pragma unroll 1
+                for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(raw[(size_t)(cs + k) * 128 + r]);
+                    tmem_st16(tl + Cfg::kColH + cs, v);
+                }
+                tmem_st_wait();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+#pragma unroll 1
+                for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tl + Cfg::kColH + cs, v);
+                    tmem_ld_wait();
+                    write_h_copy16<P>(s, r, cs, v);
+                }
+            } else {
+#pragma unroll 1
+                for (int cs = c0; cs < c0 + kHalf; cs += 16) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = src ? __float_as_uint(src[(size_t)(cs + k) * 128 + r]) : 0u;
+                    tmem_st16(tl + Cfg::kColH + cs, v);
+                    if (!STATE_ONLY) write_h_copy16<P>(s, r, cs, v);
+                }
             }
             tmem_st_wait();
             if (!STATE_ONLY) fence_async_smem();
