@@ -169,8 +169,9 @@ int ssd_varlen_plan(const ssd_dims *dims, const int32_t *cu_seqlens, const int32
  * before the stream's previous kernel has finished, but waits
  * (griddepcontrol.wait) for it, and for its writes to be visible, before
  * touching global memory, so stream order holds as for plain launches.  The
- * plan's kernel lets the next kernel on its stream be scheduled at its start;
- * a caller kernel launched there with the same attribute must wait likewise.
+ * plan's kernel is launched the same way, and lets the next kernel on its
+ * stream be scheduled at its start; a caller kernel launched there with the
+ * same attribute must wait likewise.
  * Both calls can be captured into a CUDA graph. */
 int ssd_varlen_forward(const ssd_plan *plan, const ssd_inputs *in, const ssd_outputs *out,
                        cudaStream_t stream);

@@ -6,9 +6,9 @@
 namespace ssd {
 
 // ---- programmatic dependent launch ------------------------------------------
-// The kernels of a forward are launched with programmatic stream serialisation
-// (launch_after_prev): such a kernel may be scheduled while the stream's previous
-// kernel still runs, once every CTA of that kernel has called
+// The plan and the kernels of a forward are launched with programmatic stream
+// serialisation (launch_after_prev): such a kernel may be scheduled while the
+// stream's previous kernel still runs, once every CTA of that kernel has called
 // pdl_launch_dependents or exited.  Every thread of it calls pdl_wait before its
 // first global-memory access; the wait returns once the previous kernels have
 // completed and their writes are visible.  Only shared-memory and TMEM set-up

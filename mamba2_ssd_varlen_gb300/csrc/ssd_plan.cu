@@ -131,8 +131,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     int32_t *__restrict__ req_first_chunk = a.req_first_chunk;
     int32_t *__restrict__ req_first_seg = a.req_first_seg;
     Seg *__restrict__ segs = a.segs;
-    // the forward's first kernel may be scheduled now; it waits for this one
+    // the forward's first kernel may be scheduled now; it waits for this one.
+    // This kernel is itself a dependent launch: it waits for the stream's previous
+    // kernel (which may have written cu_seqlens) before reading anything.
     pdl_launch_dependents();
+    pdl_wait();
     __shared__ int s_err, s_empty, s_max_segs;
     __shared__ long long s_max_len;
     if (threadIdx.x == 0) {
@@ -316,8 +319,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream) {
     // one warp per 32 requests, at least two (the flag zeroing), at most 32
     const int threads = (int)std::min<int64_t>(kPlanThreads, std::max<int64_t>(64, ((int64_t)a.R + 31) / 32 * 32));
-    plan_kernel<<<1, threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_after_prev(plan_kernel, dim3(1), dim3(threads), 0, stream, a);
 }
 
 }  // namespace ssd
