@@ -102,11 +102,13 @@ def load_peaks():
 
 # The same for the kernels of the other rows (each bench line reports its own).
 ROW_KERNEL_SOURCES = {
-    "conv": ["mamba2_ssd_varlen_gb300/csrc/ssd_conv1d.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
-    "decode": ["mamba2_ssd_varlen_gb300/csrc/ssd_decode.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
+    "conv": ["mamba2_ssd_varlen_gb300/csrc/ssd_conv1d.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh",
+             "mamba2_ssd_varlen_gb300/csrc/pdl.cuh"],
+    "decode": ["mamba2_ssd_varlen_gb300/csrc/ssd_decode.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh",
+               "mamba2_ssd_varlen_gb300/csrc/pdl.cuh"],
     "gdn": ["mamba2_ssd_varlen_gb300/csrc/ssd_gdn_tc.cu", "mamba2_ssd_varlen_gb300/csrc/ssd_gdn.cu",
             "mamba2_ssd_varlen_gb300/csrc/tc_util.cuh", "mamba2_ssd_varlen_gb300/csrc/sm100.cuh",
-            "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh"],
+            "mamba2_ssd_varlen_gb300/csrc/ssd_internal.cuh", "mamba2_ssd_varlen_gb300/csrc/pdl.cuh"],
 }
 
 

@@ -15,6 +15,7 @@
 // coalesced vector access and every input is read once (plus a W-1 halo per
 // strip).  Request boundaries inside a strip restart the window from the next
 // request's conv state.
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -161,6 +162,7 @@ constexpr int kUnroll = 6;   // a multiple of W-1 for every W, so the window shi
 // registers.
 template <typename T, int W, bool kSilu>
 __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const __grid_constant__ ConvParams p) {
+    pdl_wait();  // a dependent launch: the stream's previous kernel has finished
     constexpr int kN = Vec<T>::kN;
     __shared__ __align__(16) uint4 ring[kStages][kConvThreads];
     const ssd_conv_io &io = p.io;
@@ -331,8 +333,7 @@ cudaError_t launch_conv_k(const ConvParams &p, int64_t units, cudaStream_t strea
     if (e != cudaSuccess) return e;
     const int64_t warps = (units + kMinStrip - 1) / kMinStrip;
     const int64_t ctas = std::max<int64_t>(1, std::min(resident, (warps + kConvThreads / 32 - 1) / (kConvThreads / 32)));
-    conv1d_kernel<T, W, kSilu><<<dim3((unsigned)ctas), kConvThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_after_prev(conv1d_kernel<T, W, kSilu>, dim3((unsigned)ctas), dim3(kConvThreads), 0, stream, p);
 }
 
 template <typename T, int W>

@@ -23,6 +23,7 @@
 // state rows that read the same values do so from shared memory and the
 // global load path carries each value once.  The step is bound by the state
 // traffic (4 P N bytes read, 4 P N per written anchor).
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -131,6 +132,7 @@ template <typename T, int KV>
 // Four CTAs per SM up to KV = 32 (64 registers a thread: the bf16 instance fits,
 // the fp32 one spills 12 bytes); KV = 64 keeps all the registers it needs.
 __global__ void __launch_bounds__(kDecThreads, KV <= 32 ? 4 : 1) decode_kernel(const __grid_constant__ DecParams p) {
+    pdl_wait();  // a dependent launch: the stream's previous kernel has finished
     const int i = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     const int g = hh / (p.H / p.G);
     const int rowlanes = p.N / KV;                   // threads per state row (power of 2, <= 32)
@@ -237,16 +239,15 @@ cudaError_t launch_decode_t(const DecParams &p, int kv, cudaStream_t stream) {
     const dim3 grid((unsigned)((int64_t)p.R * p.H)), block(kDecThreads);
     const size_t smem = (size_t)DecStage(p.N, p.P, (int)sizeof(T)).bytes;
     switch (kv) {
-        case 1: decode_kernel<T, 1><<<grid, block, smem, stream>>>(p); break;
-        case 2: decode_kernel<T, 2><<<grid, block, smem, stream>>>(p); break;
-        case 4: decode_kernel<T, 4><<<grid, block, smem, stream>>>(p); break;
-        case 8: decode_kernel<T, 8><<<grid, block, smem, stream>>>(p); break;
-        case 16: decode_kernel<T, 16><<<grid, block, smem, stream>>>(p); break;
-        case 32: decode_kernel<T, 32><<<grid, block, smem, stream>>>(p); break;
-        case 64: decode_kernel<T, 64><<<grid, block, smem, stream>>>(p); break;
+        case 1: return launch_after_prev(decode_kernel<T, 1>, grid, block, smem, stream, p);
+        case 2: return launch_after_prev(decode_kernel<T, 2>, grid, block, smem, stream, p);
+        case 4: return launch_after_prev(decode_kernel<T, 4>, grid, block, smem, stream, p);
+        case 8: return launch_after_prev(decode_kernel<T, 8>, grid, block, smem, stream, p);
+        case 16: return launch_after_prev(decode_kernel<T, 16>, grid, block, smem, stream, p);
+        case 32: return launch_after_prev(decode_kernel<T, 32>, grid, block, smem, stream, p);
+        case 64: return launch_after_prev(decode_kernel<T, 64>, grid, block, smem, stream, p);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 // State elements per thread: the smallest power of two that spreads the (P, N)

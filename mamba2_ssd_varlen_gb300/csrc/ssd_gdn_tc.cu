@@ -48,6 +48,7 @@
 #include <mutex>
 
 #include "sm100.cuh"
+#include "pdl.cuh"
 #include "ssd_internal.cuh"
 #include "tc_util.cuh"
 
@@ -145,6 +146,7 @@ struct Dests {
 
 __global__ void __launch_bounds__(kThreads, 1) gdn_tc_kernel(const __grid_constant__ GdnTcParams p,
                                                              const __grid_constant__ GdnTcMaps maps) {
+    pdl_wait();  // a dependent launch: the stream's previous kernel has finished
     const ssd_gdn_io &io = p.io;
     int32_t *err = io.device_err;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -998,8 +1000,9 @@ int launch_gdn_tc(const ssd_gdn_dims *d, const int32_t *cu_seqlens, const ssd_gd
     }
     const int64_t ctas = (int64_t)d->R * d->Hv;
     if (ctas > 0x7fffffffLL) return SSD_ERR_DIMS;
-    gdn_tc_kernel<<<(unsigned)ctas, kThreads, smem, stream>>>(p, maps);
-    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    return launch_after_prev(gdn_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), smem, stream, p, maps) == cudaSuccess
+               ? SSD_OK
+               : SSD_ERR_CUDA;
 }
 
 }  // namespace ssd
