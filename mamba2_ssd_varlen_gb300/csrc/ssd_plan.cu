@@ -7,9 +7,10 @@
 //   * req_first_chunk[i]: the request's first row in the chunk-state export
 //     (exclusive prefix sum of chunk counts; chunks cut at absolute multiples
 //     of chunk_size, so a resumed request's first chunk may be partial);
-//   * req_first_seg[i] and the segment list: runs of at most 2048 tokens that
-//     the forward kernels walk, cut at absolute multiples of seg_len or, for
-//     batches of mid-length requests, tail-shortened (SegCuts below);
+//   * req_first_seg[i] and the segment list: runs of at most seg_len tokens
+//     (2048, or 8192 on the one-head path) that the forward kernels walk, cut at
+//     absolute multiples of seg_len or, for batches of mid-length requests,
+//     tail-shortened (SegCuts below);
 //   * how the state is carried from one segment of a request to the next, and
 //     the order in which the forward kernels take the segments (seg_order):
 //       chained: the kernel that finishes a segment publishes its end state,
@@ -81,7 +82,8 @@ constexpr int kRankByLength = 256;
 //   t2 - s >= 512; the part before the first of these cuts, the head, is cut
 //   from its end backwards into n = ceil(length / 2048) segments of one stride,
 //   the smallest multiple of 256 not below length / n (the first segment takes
-//   the rest).  Every cut is a multiple of 256; every segment holds 1-2048 tokens.
+//   the rest).  Every cut is a multiple of 256; every segment holds 1 to len
+//   tokens (len = 2048 for the tail-shortened rule).
 struct SegCuts {
     int64_t s, e, head_end, stride, t1;
     int32_t len;
