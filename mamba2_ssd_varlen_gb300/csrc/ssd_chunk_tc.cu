@@ -125,6 +125,7 @@ struct __align__(1024) TcSmem {
     uint64_t cb_full, m_full, m_done;
     uint64_t y_full[2], y_empty[2];
     uint64_t xd_full, s_free, s_full, h_full;
+    uint64_t hin_bar;                    // G2's eight warps meet while building an entering state
     int32_t item_ring[8];                // work items in the order the CTA processes them (-1: none left)
     uint64_t item_full[8], item_empty[8];
     uint32_t tmem_base;
@@ -212,6 +213,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     *abort_flag = 1;
     record_timeout(hdr, (int)(smem_u32(bar) - smem_u32(tc_smem)));
     return false;
+}
+
+// A wait by every lane of a warp, with one outcome for the whole warp (each lane
+// acquires the barrier itself; if any gave up, every lane takes the abort path).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *hdr) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, hdr));
 }
 
 // A wait for the state of the previous segment (chained mode), recorded as
@@ -402,6 +410,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         mbar_init(&s.s_free, kMathPerRole);
         mbar_init(&s.s_full, 1);
         mbar_init(&s.h_full, kMathPerRole);
+        mbar_init(&s.hin_bar, kMathPerRole);
         s.abort_flag = 0;
         fence_mbar_init();
     }
@@ -753,6 +762,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
         uint32_t pc = 0, nit = 0;
+        uint32_t n_hin = 0;  // completed phases of hin_bar
         bool ok = true;
         while (ok) {
             const int w = take_item_warp(s, nit, abort_flag, p.hdr, lane);
@@ -803,7 +813,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 for (int i = 0; i < kVec; ++i) v4[i] = __ldg(src4 + i * 256 + g);
 #pragma unroll
                 for (int i = 0; i < kVec; ++i) raw4[i * 256 + g] = v4[i];
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                // the eight warps meet (a bounded wait: a warp that gave up earlier cannot
+                // leave the others blocked)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.hin_bar);
+                if (!wait_bar_warp(&s.hin_bar, par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
                 const float *raw = reinterpret_cast<const float *>(s.h_hi);
 #pragma unroll 1
                 for (int cs = c0; cs < c0 + kHalf; cs += 16) {
@@ -813,7 +827,9 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     tmem_st16(tl + Cfg::kColH + cs, v);
                 }
                 tmem_st_wait();
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.hin_bar);
+                if (!wait_bar_warp(&s.hin_bar, par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
 #pragma unroll 1
                 for (int cs = c0; cs < c0 + kHalf; cs += 16) {
                     uint32_t v[16];

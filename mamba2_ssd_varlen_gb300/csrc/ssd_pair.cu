@@ -94,6 +94,7 @@ struct __align__(1024) PairSmem {
     uint64_t x_full[2], x_empty[2], cb_full[2], m_full[2], m_done[2], wx_full[2], h_copy[2], h_scaled[2];
     uint64_t ye_done[2], y_scaled[2], y_done[2], y_empty[2], s_done[2], stage_free[2], z_full[2], drain[2];
     uint64_t bc_full, bc_empty;
+    uint64_t hin_bar[2];   // per slot: G2's four warps meet while building an entering state
     int32_t item_ring[kItemRing];
     uint64_t item_full[kItemRing], item_empty[kItemRing];
     uint32_t tmem_base;
@@ -321,6 +322,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
             mbar_init(&s.stage_free[k], 4);
             mbar_init(&s.z_full[k], 1);
             mbar_init(&s.drain[k], 1);
+            mbar_init(&s.hin_bar[k], 4);
         }
         mbar_init(&s.bc_full, 1);
         mbar_init(&s.bc_empty, 2);  // each slot's state MMA is the last reader of B and C
@@ -703,6 +705,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
         uint8_t *const zs = s.wx_lo[k];  // z tile (after the state MMA)
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
         uint32_t pc = 0, nit = 0, zissued = 0;
+        uint32_t n_hin = 0;  // completed phases of hin_bar[k]
         bool ok = true;
         while (ok) {
             const int w = take_item_warp(s, nit, abort_flag, p.hdr, lane);
@@ -749,7 +752,11 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     reinterpret_cast<float4 *>(i < 8 ? hh_t : hl_t)[(i & 7) * 128 + r] = v4[i];
-                asm volatile("bar.sync %0, 128;" ::"r"(1 + k) : "memory");
+                // the slot's four warps meet (a bounded wait: a warp that gave up earlier
+                // cannot leave the others blocked)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.hin_bar[k]);
+                if (!wait_bar_warp(&s.hin_bar[k], par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
 #pragma unroll 1
                 for (int cs = 0; cs < kP; cs += 16) {
                     const float *raw = reinterpret_cast<const float *>(cs < 32 ? hh_t : hl_t) + (size_t)(cs & 31) * 128;
@@ -759,7 +766,9 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                     tmem_st16(tH + cs, v);
                 }
                 tmem_st_wait();
-                asm volatile("bar.sync %0, 128;" ::"r"(1 + k) : "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.hin_bar[k]);
+                if (!wait_bar_warp(&s.hin_bar[k], par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
 #pragma unroll 1
                 for (int cs = 0; cs < kP; cs += 16) {
                     uint32_t v[16];
