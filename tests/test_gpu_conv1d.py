@@ -78,6 +78,18 @@ def test_strips_across_channel_groups(lengths):
     run_and_check(workloads.make_conv_problem(spec, seed=len(lengths), device="cuda", canary=1.25))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_silu_over_a_wide_range_of_arguments(dtype):
+    # inputs and conv states scaled by 25: the pre-activation values reach about
+    # +-100, through SiLU's saturation on both sides (about zero below, the
+    # identity above) and the region in between
+    prob = workloads.make_conv_problem(_spec(dtype=dtype, lengths=[130, 64, 1, 200]), seed=21, device="cuda",
+                                       canary=3.0)
+    prob["x"].mul_(25.0)
+    prob["conv_pool"].mul_(25.0)
+    run_and_check(prob)
+
+
 def test_no_activation_no_bias_many_channels():
     spec = _spec(D=2056, silu=False, has_bias=False, lengths=[200, 1, 1, 77])
     run_and_check(workloads.make_conv_problem(spec, seed=8, device="cuda", canary=0.5))
