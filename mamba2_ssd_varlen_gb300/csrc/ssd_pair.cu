@@ -95,6 +95,7 @@ struct __align__(1024) PairSmem {
     uint64_t ye_done[2], y_scaled[2], y_done[2], y_empty[2], s_done[2], stage_free[2], z_full[2], drain[2];
     uint64_t bc_full, bc_empty;
     uint64_t hin_bar[2];   // per slot: G2's four warps meet while building an entering state
+    uint64_t hin_full[2];  // per slot: the entering state's bulk copy has landed
     int32_t item_ring[kItemRing];
     uint64_t item_full[kItemRing], item_empty[kItemRing];
     uint32_t tmem_base;
@@ -323,6 +324,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
             mbar_init(&s.z_full[k], 1);
             mbar_init(&s.drain[k], 1);
             mbar_init(&s.hin_bar[k], 4);
+            mbar_init(&s.hin_full[k], 1);
         }
         mbar_init(&s.bc_full, 1);
         mbar_init(&s.bc_empty, 2);  // each slot's state MMA is the last reader of B and C
@@ -705,7 +707,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
         uint8_t *const zs = s.wx_lo[k];  // z tile (after the state MMA)
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
         uint32_t pc = 0, nit = 0, zissued = 0;
-        uint32_t n_hin = 0;  // completed phases of hin_bar[k]
+        uint32_t n_hin = 0;  // entering states loaded: phases of hin_full[k] and hin_bar[k]
         bool ok = true;
         while (ok) {
             const int w = take_item_warp(s, nit, abort_flag, p.hdr, lane);
@@ -741,22 +743,17 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
             // the first y_inter.  The previous item's last state MMA and y_inter
             // have completed (waited for below), so both are free.
             if (src) {
-                // the state (p rows of 128 floats, 32 KB) into the h^T tiles with one round of
-                // 16-byte loads by the slot's 128 threads (rows 0-31 to the hi tile, 32-63 to the
-                // lo tile); then all of it into H, and -- once every thread has read its
-                // column -- the hi/lo copy in place
-                const float4 *src4 = reinterpret_cast<const float4 *>(src);
-                float4 v4[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v4[i] = __ldg(src4 + i * 128 + r);
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    reinterpret_cast<float4 *>(i < 8 ? hh_t : hl_t)[(i & 7) * 128 + r] = v4[i];
-                // the slot's four warps meet (a bounded wait: a warp that gave up earlier
-                // cannot leave the others blocked)
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.hin_bar[k]);
-                if (!wait_bar_warp(&s.hin_bar[k], par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
+                // the state (p rows of 128 floats, 32 KB) into the h^T tiles by two bulk
+                // copies (rows 0-31 to the hi tile, 32-63 to the lo tile: no registers held
+                // while it is in flight); then all of it into H, and -- once every thread
+                // has read its column -- the hi/lo copy in place
+                if (q == 0 && lane == 0) {
+                    mbar_arrive_expect_tx(&s.hin_full[k], 2 * kTile);
+                    bulk_g2s(hh_t, src, kTile, &s.hin_full[k]);
+                    bulk_g2s(hl_t, src + 32 * 128, kTile, &s.hin_full[k]);
+                }
+                const uint32_t ph = par(n_hin++);
+                if (!wait_bar_warp(&s.hin_full[k], ph, abort_flag, p.hdr)) { ok = false; break; }
 #pragma unroll 1
                 for (int cs = 0; cs < kP; cs += 16) {
                     const float *raw = reinterpret_cast<const float *>(cs < 32 ? hh_t : hl_t) + (size_t)(cs & 31) * 128;
@@ -766,9 +763,11 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
                     tmem_st16(tH + cs, v);
                 }
                 tmem_st_wait();
+                // the slot's four warps meet (a bounded wait: a warp that gave up earlier
+                // cannot leave the others blocked)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.hin_bar[k]);
-                if (!wait_bar_warp(&s.hin_bar[k], par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
+                if (!wait_bar_warp(&s.hin_bar[k], ph, abort_flag, p.hdr)) { ok = false; break; }
 #pragma unroll 1
                 for (int cs = 0; cs < kP; cs += 16) {
                     uint32_t v[16];
@@ -982,6 +981,7 @@ ssd_pair_kernel(const FwdParams p, const __grid_constant__ PairMaps maps, int Qi
         // Never leave a copy in flight: the last z load has landed (waited for in its
         // epilogue unless a wait gave up first).
         if (zissued > 0) mbar_wait(&s.z_full[k], par(zissued - 1), kWaitNs);
+        if (q == 0 && lane == 0 && n_hin > 0) mbar_wait(&s.hin_full[k], par(n_hin - 1), kWaitNs);
     }
 
     tc_fence_before();
