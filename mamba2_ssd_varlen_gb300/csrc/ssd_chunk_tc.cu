@@ -126,6 +126,7 @@ struct __align__(1024) TcSmem {
     uint64_t y_full[2], y_empty[2];
     uint64_t xd_full, s_free, s_full, h_full;
     uint64_t hin_bar;                    // G2's eight warps meet while building an entering state
+    uint64_t hin_full;                   // the entering state's bulk copy has landed
     int32_t item_ring[8];                // work items in the order the CTA processes them (-1: none left)
     uint64_t item_full[8], item_empty[8];
     uint32_t tmem_base;
@@ -411,6 +412,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         mbar_init(&s.s_full, 1);
         mbar_init(&s.h_full, kMathPerRole);
         mbar_init(&s.hin_bar, kMathPerRole);
+        mbar_init(&s.hin_full, 1);
         s.abort_flag = 0;
         fence_mbar_init();
     }
@@ -762,7 +764,7 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
         const __nv_bfloat16 *__restrict__ zv = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *__restrict__ yv = static_cast<__nv_bfloat16 *>(p.y);
         uint32_t pc = 0, nit = 0;
-        uint32_t n_hin = 0;  // completed phases of hin_bar
+        uint32_t n_hin = 0;  // entering states loaded: phases of hin_full and hin_bar
         bool ok = true;
         while (ok) {
             const int w = take_item_warp(s, nit, abort_flag, p.hdr, lane);
@@ -801,23 +803,17 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
             // h^T in TMEM: thread r holds state column n = r (rows p along TMEM columns).
             if (!STATE_ONLY && src) {
                 // The state (P rows of 128 floats) into the h^T tiles (hi then lo, one
-                // region of P * 512 bytes) with one round of 16-byte loads by the eight
-                // warps; then this warp's columns into TMEM and -- once every warp has
-                // read its columns -- the hi/lo copy in place.
-                constexpr int kVec = P * 32 / 256;  // float4 per thread
-                const int g = (warp - 10) * 32 + lane;
-                const float4 *src4 = reinterpret_cast<const float4 *>(src);
-                float4 *raw4 = reinterpret_cast<float4 *>(s.h_hi);
-                float4 v4[kVec];
-#pragma unroll
-                for (int i = 0; i < kVec; ++i) v4[i] = __ldg(src4 + i * 256 + g);
-#pragma unroll
-                for (int i = 0; i < kVec; ++i) raw4[i * 256 + g] = v4[i];
-                // the eight warps meet (a bounded wait: a warp that gave up earlier cannot
-                // leave the others blocked)
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.hin_bar);
-                if (!wait_bar_warp(&s.hin_bar, par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
+                // region of P * 512 bytes) by bulk copies of 16 KB issued by one thread
+                // (no registers held while they are in flight); then this warp's columns
+                // into TMEM and -- once every warp has read its columns -- the hi/lo copy
+                // in place.
+                constexpr uint32_t kStateBytes = P * 512;
+                if (warp == 10 && lane == 0) {
+                    mbar_arrive_expect_tx(&s.hin_full, kStateBytes);
+                    for (uint32_t off = 0; off < kStateBytes; off += 16384)
+                        bulk_g2s(s.h_hi + off, reinterpret_cast<const uint8_t *>(src) + off, 16384, &s.hin_full);
+                }
+                if (!wait_bar_warp(&s.hin_full, par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
                 const float *raw = reinterpret_cast<const float *>(s.h_hi);
 #pragma unroll 1
                 for (int cs = c0; cs < c0 + kHalf; cs += 16) {
@@ -827,9 +823,11 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                     tmem_st16(tl + Cfg::kColH + cs, v);
                 }
                 tmem_st_wait();
+                // the eight warps meet (a bounded wait: a warp that gave up earlier cannot
+                // leave the others blocked)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.hin_bar);
-                if (!wait_bar_warp(&s.hin_bar, par(n_hin++), abort_flag, p.hdr)) { ok = false; break; }
+                if (!wait_bar_warp(&s.hin_bar, par(n_hin - 1), abort_flag, p.hdr)) { ok = false; break; }
 #pragma unroll 1
                 for (int cs = c0; cs < c0 + kHalf; cs += 16) {
                     uint32_t v[16];
@@ -1066,6 +1064,8 @@ ssd_chunk_tc_kernel(const FwdParams p, const __grid_constant__ TcMaps maps, int 
                 have_piece = has_next;
             }
         }
+        // Never leave a copy in flight: the last entering state's bulk copy has landed.
+        if (!STATE_ONLY && warp == 10 && lane == 0 && n_hin > 0) mbar_wait(&s.hin_full, par(n_hin - 1), kWaitNs);
     } else if (warp == kWarpBC) {
         // ------------------------------------------------------------ B and C loader
         if (lane == 0) {
