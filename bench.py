@@ -312,27 +312,51 @@ def cpu_baseline(prob, max_seconds=30.0):
             "sample_one_core": f"request {sel[0]} ({lens[sel[0]]} tokens, all heads) on one core, {dt1:.2f} s"}
 
 
+REF_SECONDS = 150.0  # the whole reference run (warm-up and timed steps) on the host cores
+
+
+def sized_reference(args, n_units, build, run, group=1):
+    """Times the oracle on a sample sized so that ``--warmup`` + ``--steps`` steps take
+    about REF_SECONDS in all, whatever K is.  ``build(n)`` returns (sample, tokens it
+    stands for, description) for the first n of ``n_units`` units of the workload;
+    ``run(sample)`` runs the oracle on it.  Samples are whole multiples of ``group``
+    units (the host's core count for an oracle that spreads units over threads, so
+    that every core has work), timed once at one group to size them.  Returns
+    (tokens/s: the median step, description)."""
+    g = max(1, min(group, n_units))
+    one, _, _ = build(g)
+    t0 = time.perf_counter()
+    run(one)
+    t_group = max(time.perf_counter() - t0, 1e-5)
+    per_step = REF_SECONDS / max(1, args.steps + args.warmup)
+    n = min(n_units, g * max(1, int(per_step / t_group)))
+    sample, tokens, what = build(n)
+    for _ in range(args.warmup):
+        run(sample)
+    vals = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run(sample)
+        vals.append(tokens / (time.perf_counter() - t0))
+    return sorted(vals)[len(vals) // 2], what
+
+
 def run_reference_decode(args, world):
-    """The oracle on the machine's host cores for a decode step: a bounded sample of
-    whole requests (all heads) per timed step."""
+    """The oracle on the machine's host cores for a decode step: a sample of whole
+    requests (all heads) per timed step, sized by sized_reference."""
     import oracle
     import workloads
     prob = workloads.make_decode_problem(args.config, device="cpu")
     R, T, H = prob["R"], prob["T"], prob["H"]
-    n_req = max(1, min(R, 8))
-    sel = list(range(n_req))
-    o = workloads.to_oracle_decode(prob, requests=sel)
-    tok = int(sum(prob["windows"][i] for i in sel))
     ncores = os.cpu_count() or 1
-    for _ in range(args.warmup):
-        oracle.decode(o, n_threads=ncores)
-    vals = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle.decode(o, n_threads=ncores)
-        vals.append(tok / (time.perf_counter() - t0))
-    value = sorted(vals)[len(vals) // 2]
-    sample = f"{n_req} of {R} requests ({tok} tokens, all {H} heads), fp64 token-by-token recurrence"
+
+    def build(n):
+        sel = list(range(n))
+        tok = int(sum(prob["windows"][i] for i in sel))
+        return (workloads.to_oracle_decode(prob, requests=sel), tok,
+                f"{n} of {R} requests ({tok} tokens, all {H} heads), fp64 token-by-token recurrence")
+
+    value, sample = sized_reference(args, R, build, lambda o: oracle.decode(o, n_threads=ncores), group=ncores)
     line = {"metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": T / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -346,27 +370,25 @@ def run_reference_decode(args, world):
 
 
 def run_reference_conv(args, world):
-    """The conv1d oracle on the host cores: a bounded channel sample per timed step."""
+    """The conv1d oracle on the host cores: a channel sample per timed step, sized by
+    sized_reference."""
     from oracle.conv1d import conv1d
     import workloads
     prob = workloads.make_conv_problem(args.config, device="cpu")
     T, D = prob["T"], prob["D"]
-    ch = list(range(0, D, max(1, D // 64)))[:64]
-    o = workloads.to_oracle_conv(prob, channels=ch)
-    for _ in range(args.warmup):
-        conv1d(o)
-    vals = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        conv1d(o)
-        vals.append(T * len(ch) / D / (time.perf_counter() - t0))
-    value = sorted(vals)[len(vals) // 2]
+
+    def build(n):
+        ch = list(range(0, D, max(1, D // n)))[:n]
+        return (workloads.to_oracle_conv(prob, channels=ch), T * len(ch) / D,
+                f"{len(ch)} of {D} channels, all {T} tokens, scaled to all channels")
+
+    value, sample = sized_reference(args, D, build, conv1d)
     line = {"metric": CONV_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": T / value * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.config, "T": T, "R": prob["R"], "D": D, "W": prob["W"]},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{len(ch)} of {D} channels, all {T} tokens, scaled to all channels"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -389,16 +411,23 @@ def gdn_oracle_sample(prob, max_seconds):
 
 
 def run_reference_gdn(args, world):
+    """The GDN oracle on the host: units are (request, value head) in order, the
+    heads of the first request before whole requests; the sample is sized by
+    sized_reference and scaled to all heads."""
+    from oracle.gdn import gdn_forward
     import workloads
     prob = workloads.make_gdn_problem(args.config, device="cpu")
-    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        gdn_oracle_sample(prob, budget)
-    vals, sample = [], ""
-    for _ in range(args.steps):
-        v, sample = gdn_oracle_sample(prob, budget)
-        vals.append(v)
-    value = sorted(vals)[len(vals) // 2]
+    lens, Hv = prob["lengths"], int(prob["v"].shape[1])
+
+    def build(n):
+        if n <= Hv:
+            return (workloads.to_oracle_gdn(prob, requests=[0], heads=list(range(n))), lens[0] * n / Hv,
+                    f"request 0 ({lens[0]} tokens), {n} of {Hv} value heads, numpy fp64, scaled to all heads")
+        k = min(len(lens), n // Hv)
+        return (workloads.to_oracle_gdn(prob, requests=list(range(k))), sum(lens[:k]),
+                f"{k} of {len(lens)} requests ({sum(lens[:k])} tokens, all heads), numpy fp64")
+
+    value, sample = sized_reference(args, len(lens) * Hv, build, gdn_forward)
     T = prob["T"]
     line = {"metric": GDN_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": T / value * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -419,17 +448,25 @@ def run_reference(args, rank, world):
         return run_reference_decode(args, world)
     if args.config in workloads.CONV_CONFIGS:
         return run_reference_conv(args, world)
+    import oracle
     prob = workloads.make_problem(args.config, device="cpu")
-    # Each step: a bounded sample (whole requests) sized so the run stays within minutes.
-    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        cpu_baseline(prob, max_seconds=budget)
-    vals = []
-    last = None
-    for _ in range(args.steps):
-        last = cpu_baseline(prob, max_seconds=budget)
-        vals.append(last["value"])
-    value = sorted(vals)[len(vals) // 2]
+    # Units are (request, head) in order, the heads of the first request before whole
+    # requests; the sample is sized by sized_reference and scaled to all heads.
+    lens, H = prob["lengths"], prob["H"]
+    ncores = os.cpu_count() or 1
+
+    def build(n):
+        if n <= H:
+            return (workloads.to_oracle(prob, requests=[0], heads=list(range(n))), lens[0] * n / H,
+                    f"request 0 ({lens[0]} tokens), {n} of {H} heads, fp64 token-by-token recurrence, "
+                    f"scaled to all heads")
+        k = min(len(lens), n // H)
+        return (workloads.to_oracle(prob, requests=list(range(k))), sum(lens[:k]),
+                f"{k} of {len(lens)} requests ({sum(lens[:k])} tokens, all {H} heads), "
+                f"fp64 token-by-token recurrence")
+
+    value, sample = sized_reference(args, len(lens) * H, build, lambda o: oracle.forward(o, n_threads=ncores),
+                                    group=ncores)
     T = prob["T"]
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": T / value * 1e3,
@@ -438,7 +475,8 @@ def run_reference(args, rank, world):
             "config": {"workload": args.config, "T": T, "R": prob["R"], "H": prob["H"],
                        "P": prob["P"], "N": prob["N"], "G": prob["G"],
                        "chunk_size": prob["chunk_size"]},
-            "cpu_baseline": {**last, "value": value},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
