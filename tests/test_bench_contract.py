@@ -48,3 +48,33 @@ def test_traffic_figures_are_keyed_to_source_and_workload():
         # another workload or another source never borrows a figure
         assert bench.read_traffic(f[2], f[3] + "_other") is None
         assert bench.read_traffic("0" * 16, f[3]) is None
+
+
+def test_reference_sample_is_sized_to_the_run(monkeypatch):
+    # sized_reference times one group of units, then takes whole groups so that
+    # warm-up + K steps fit REF_SECONDS (at least one group, at most every unit)
+    import types
+    clock = {"t": 0.0}
+    monkeypatch.setattr(bench.time, "perf_counter", lambda: clock["t"])
+    unit_s = 0.01  # simulated seconds per group of units
+
+    def build(n):
+        return n, 100.0 * n, f"{n} units"
+
+    def run(n):
+        clock["t"] += unit_s * -(-n // 4)  # groups of 4 run in parallel
+
+    def sized(steps, warmup, n_units):
+        args = types.SimpleNamespace(steps=steps, warmup=warmup)
+        return bench.sized_reference(args, n_units, build, run, group=4)
+
+    # K = 2500: 150 s / 2505 steps = 59.9 ms a step -> 5 groups of 4 units, 50 ms a step
+    value, what = sized(2500, 5, 1000)
+    assert what == "20 units"
+    assert abs(value - 2000.0 / 0.05) < 1e-6 * value
+    # few steps: the whole workload
+    assert sized(3, 3, 1000)[1] == "1000 units"
+    # a step budget below one group still takes one group
+    assert sized(10 ** 6, 5, 1000)[1] == "4 units"
+    # fewer units than a group
+    assert sized(2500, 5, 3)[1] == "3 units"
